@@ -1,0 +1,309 @@
+"""CPU oracle for the packed-state AdamW update -- test infrastructure only.
+
+The oracle is the plain, slow, scalar C program in ``oracle.c`` (its header
+lists the pages and the readings it follows).  This module compiles it with gcc
+on first use and wraps it with ctypes and numpy.  Only the tests, the smoke
+check and bench.py's CPU-baseline and reference legs may import it: the product
+package never does, and the two share no code.
+
+Every wrapper copies its inputs and returns fresh arrays, so callers' arrays
+are never modified.  ``threads > 1`` splits the elements (whole 2048-element
+blocks in the blockwise mode) into contiguous slices run on Python threads;
+ctypes releases the GIL during each call and elements are independent, so the
+result is identical to a single-threaded run.
+
+``Oracle(path)`` binds the same wrappers to another build of the C source; the
+tests use it to load copies with a planted mistake and check that the pins
+catch it.  The module-level functions use the default build.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+BLOCK = 2048
+
+CFLAGS = ["-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+
+
+def compile_source(src: str, out: str) -> str:
+    """Compile a C oracle source file into a shared library at ``out``."""
+    tmp = out + f".{os.getpid()}.tmp"
+    subprocess.run(["gcc", *CFLAGS, src, "-o", tmp, "-lm"], check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so (gcc, strict IEEE binary32)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(SOURCE):
+        compile_source(SOURCE, _LIB)
+    return _LIB
+
+
+_f32p = ctypes.POINTER(ctypes.c_float)
+_u32p = ctypes.POINTER(ctypes.c_uint32)
+_u16p = ctypes.POINTER(ctypes.c_uint16)
+_u8p = ctypes.POINTER(ctypes.c_uint8)
+_i64 = ctypes.c_int64
+_d = ctypes.c_double
+_HYP = [_i64, _d, _d, _d, _d, _d]  # step, lr, beta1, beta2, eps, wd
+
+_SIGNATURES = {
+    "oracle_e4m11_encode_array": (None, [_f32p, _u16p, _i64]),
+    "oracle_e4m12_encode_array": (None, [_f32p, _u16p, _i64]),
+    "oracle_fp16_encode_array": (None, [_f32p, _u16p, _i64]),
+    "oracle_e4m11_decode_array": (None, [_u16p, _f32p, _i64]),
+    "oracle_e4m12_decode_array": (None, [_u16p, _f32p, _i64]),
+    "oracle_fp16_decode_array": (None, [_u16p, _f32p, _i64]),
+    "oracle_bf16_round_array": (None, [_f32p, _u16p, _i64]),
+    "oracle_hyperparams": (None, [*_HYP, _f32p]),
+    "oracle_adamw_element": (None, [ctypes.c_float] * 4 + [*_HYP, _f32p]),
+    "oracle_step_packed_e4": (ctypes.c_uint64, [_f32p, _f32p, _u32p, _i64, *_HYP]),
+    "oracle_step_packed_fp16": (ctypes.c_uint64, [_f32p, _f32p, _u32p, _i64, *_HYP]),
+    "oracle_step_fp32": (ctypes.c_uint64, [_f32p, _f32p, _f32p, _f32p, _i64, *_HYP]),
+    "oracle_encode_state_e4": (ctypes.c_uint64, [_f32p, _f32p, _u32p, _i64]),
+    "oracle_decode_state_e4": (None, [_u32p, _f32p, _f32p, _i64]),
+    "oracle_encode_state_fp16": (ctypes.c_uint64, [_f32p, _f32p, _u32p, _i64]),
+    "oracle_decode_state_fp16": (None, [_u32p, _f32p, _f32p, _i64]),
+    "oracle_requantise": (None, [_f32p, _i64, _f32p, _u8p, _f32p]),
+    "oracle_step_blockwise8": (
+        ctypes.c_uint64,
+        [_f32p, _f32p, _u16p, _u8p, _f32p, _u8p, _f32p, _f32p, _f32p, _i64, *_HYP],
+    ),
+}
+
+
+def _ptr(a: np.ndarray, ctype):
+    assert a.flags.c_contiguous
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def _arr(x, dtype) -> np.ndarray:
+    return np.array(x, dtype=dtype, copy=True, order="C").reshape(-1)
+
+
+def _hyp(step, lr, beta1, beta2, eps, wd):
+    return (int(step), float(lr), float(beta1), float(beta2), float(eps), float(wd))
+
+
+def _slices(n: int, threads: int, align: int = 1):
+    """Contiguous [lo, hi) slices, each start a multiple of ``align``."""
+    units = -(-n // align)
+    threads = max(1, min(int(threads), max(1, units)))
+    per = -(-units // threads)
+    out = []
+    for t in range(threads):
+        lo = t * per * align
+        hi = min(n, (t + 1) * per * align)
+        if lo < hi:
+            out.append((lo, hi))
+    return out or [(0, n)]
+
+
+def _run_sliced(fn, n: int, threads: int, align: int = 1) -> int:
+    sl = _slices(n, threads, align)
+    if len(sl) == 1:
+        return int(fn(*sl[0]) or 0)
+    results = [0] * len(sl)
+
+    def work(k, lo, hi):
+        results[k] = int(fn(lo, hi) or 0)
+
+    ts = [threading.Thread(target=work, args=(k, lo, hi)) for k, (lo, hi) in enumerate(sl)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    return sum(results)
+
+
+class Oracle:
+    """ctypes/numpy wrappers over one build of the C oracle."""
+
+    def __init__(self, path: str | None = None):
+        self.path = path or build()
+        lib = ctypes.CDLL(self.path)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        self.lib = lib
+
+    # ---- lane codecs ----------------------------------------------------
+    def _enc(self, name, x):
+        x = _arr(x, np.float32)
+        out = np.empty(x.size, np.uint16)
+        getattr(self.lib, name)(_ptr(x, ctypes.c_float), _ptr(out, ctypes.c_uint16), x.size)
+        return out
+
+    def _dec(self, name, c):
+        c = _arr(c, np.uint16)
+        out = np.empty(c.size, np.float32)
+        getattr(self.lib, name)(_ptr(c, ctypes.c_uint16), _ptr(out, ctypes.c_float), c.size)
+        return out
+
+    def e4m11_encode(self, x):
+        """Signed E4M11 codes of FP32 values (first-moment lane)."""
+        return self._enc("oracle_e4m11_encode_array", x)
+
+    def e4m12_encode(self, x):
+        """Unsigned E4M12 codes of FP32 values (uncorrected-RMS lane)."""
+        return self._enc("oracle_e4m12_encode_array", x)
+
+    def fp16_encode(self, x):
+        """Saturating binary16 codes of FP32 values (FP16 comparison mode)."""
+        return self._enc("oracle_fp16_encode_array", x)
+
+    def e4m11_decode(self, c):
+        return self._dec("oracle_e4m11_decode_array", c)
+
+    def e4m12_decode(self, c):
+        return self._dec("oracle_e4m12_decode_array", c)
+
+    def fp16_decode(self, c):
+        return self._dec("oracle_fp16_decode_array", c)
+
+    def bf16_round(self, x):
+        """bfloat16 bit patterns of FP32 values, round to nearest even."""
+        return self._enc("oracle_bf16_round_array", x)
+
+    def hyperparams(self, step, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, wd=0.01):
+        """The eight FP32 scalars (b1, b2, c1, c2, bc2, ss, dk, ef)."""
+        out = np.empty(8, np.float32)
+        self.lib.oracle_hyperparams(*_hyp(step, lr, beta1, beta2, eps, wd),
+                                    _ptr(out, ctypes.c_float))
+        return out
+
+    def adamw_element(self, p, g, m, v, step, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8,
+                      wd=0.01):
+        """(p', m', v') of one FP32 element."""
+        out = np.empty(3, np.float32)
+        self.lib.oracle_adamw_element(
+            ctypes.c_float(p), ctypes.c_float(g), ctypes.c_float(m), ctypes.c_float(v),
+            *_hyp(step, lr, beta1, beta2, eps, wd), _ptr(out, ctypes.c_float))
+        return out
+
+    # ---- state-word codecs ----------------------------------------------
+    def encode_state(self, m, rms, mode="e4"):
+        """Pack (m, rms) into uint32 words; returns (words, nonfinite_count)."""
+        m = _arr(m, np.float32)
+        rms = _arr(rms, np.float32)
+        assert m.size == rms.size
+        w = np.empty(m.size, np.uint32)
+        fn = getattr(self.lib, f"oracle_encode_state_{mode}")
+        bad = fn(_ptr(m, ctypes.c_float), _ptr(rms, ctypes.c_float),
+                 _ptr(w, ctypes.c_uint32), m.size)
+        return w, int(bad)
+
+    def decode_state(self, words, mode="e4"):
+        """Unpack uint32 words into (m, rms) FP32 arrays."""
+        w = _arr(words, np.uint32)
+        m = np.empty(w.size, np.float32)
+        r = np.empty(w.size, np.float32)
+        fn = getattr(self.lib, f"oracle_decode_state_{mode}")
+        fn(_ptr(w, ctypes.c_uint32), _ptr(m, ctypes.c_float), _ptr(r, ctypes.c_float), w.size)
+        return m, r
+
+    # ---- steps ----------------------------------------------------------
+    def step_packed(self, p, g, state, step, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8,
+                    wd=0.01, mode="e4", threads=1):
+        """One packed step (mode 'e4' or 'fp16'); returns (p', state', nonfinite)."""
+        p = _arr(p, np.float32)
+        g = _arr(g, np.float32)
+        s = _arr(state, np.uint32)
+        assert p.size == g.size == s.size
+        fn = self.lib.oracle_step_packed_e4 if mode == "e4" else self.lib.oracle_step_packed_fp16
+        hy = _hyp(step, lr, beta1, beta2, eps, wd)
+
+        def run(lo, hi):
+            return fn(_ptr(p[lo:hi], ctypes.c_float), _ptr(g[lo:hi], ctypes.c_float),
+                      _ptr(s[lo:hi], ctypes.c_uint32), hi - lo, *hy)
+
+        bad = _run_sliced(run, p.size, threads)
+        return p, s, bad
+
+    def step_fp32(self, p, g, m, v, step, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, wd=0.01,
+                  threads=1):
+        """One FP32-moment step; returns (p', m', v', nonfinite)."""
+        p, g, m, v = (_arr(a, np.float32) for a in (p, g, m, v))
+        assert p.size == g.size == m.size == v.size
+        hy = _hyp(step, lr, beta1, beta2, eps, wd)
+        fn = self.lib.oracle_step_fp32
+
+        def run(lo, hi):
+            return fn(*(_ptr(a[lo:hi], ctypes.c_float) for a in (p, g, m, v)), hi - lo, *hy)
+
+        bad = _run_sliced(run, p.size, threads)
+        return p, m, v, bad
+
+    def requantise(self, x, qmap):
+        """Blockwise nearest-entry codes and per-block absmax of FP32 values."""
+        x = _arr(x, np.float32)
+        q = _arr(qmap, np.float32)
+        assert q.size == 256
+        nb = -(-x.size // BLOCK)
+        code = np.empty(x.size, np.uint8)
+        amax = np.empty(nb, np.float32)
+        self.lib.oracle_requantise(_ptr(x, ctypes.c_float), x.size, _ptr(q, ctypes.c_float),
+                                   _ptr(code, ctypes.c_uint8), _ptr(amax, ctypes.c_float))
+        return code, amax
+
+    def step_blockwise8(self, p, g, m_code, m_absmax, v_code, v_absmax, qmap1, qmap2, step,
+                        lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, wd=0.01, threads=1):
+        """One 8-bit blockwise step.
+
+        Returns (p_bf16_bits uint16, m_code', m_absmax', v_code', v_absmax', nonfinite).
+        """
+        p = _arr(p, np.float32)
+        g = _arr(g, np.float32)
+        mc = _arr(m_code, np.uint8)
+        vc = _arr(v_code, np.uint8)
+        ma = _arr(m_absmax, np.float32)
+        va = _arr(v_absmax, np.float32)
+        q1 = _arr(qmap1, np.float32)
+        q2 = _arr(qmap2, np.float32)
+        n = p.size
+        nb = -(-n // BLOCK)
+        assert g.size == n and mc.size == n and vc.size == n and ma.size == nb and va.size == nb
+        assert q1.size == 256 and q2.size == 256
+        out = np.empty(n, np.uint16)
+        hy = _hyp(step, lr, beta1, beta2, eps, wd)
+        fn = self.lib.oracle_step_blockwise8
+
+        def run(lo, hi):
+            b0 = lo // BLOCK
+            return fn(_ptr(p[lo:hi], ctypes.c_float), _ptr(g[lo:hi], ctypes.c_float),
+                      _ptr(out[lo:hi], ctypes.c_uint16), _ptr(mc[lo:hi], ctypes.c_uint8),
+                      _ptr(ma[b0:], ctypes.c_float), _ptr(vc[lo:hi], ctypes.c_uint8),
+                      _ptr(va[b0:], ctypes.c_float), _ptr(q1, ctypes.c_float),
+                      _ptr(q2, ctypes.c_float), hi - lo, *hy)
+
+        bad = _run_sliced(run, n, threads, align=BLOCK)
+        return out, mc, ma, vc, va, bad
+
+
+_default: Oracle | None = None
+_lock = threading.Lock()
+
+
+def default() -> Oracle:
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle()
+    return _default
+
+
+def __getattr__(name):
+    # module-level access to the default build's wrappers: oracle.step_packed(...)
+    if name.startswith("_"):
+        raise AttributeError(name)
+    return getattr(default(), name)
