@@ -1,0 +1,248 @@
+"""adamw_update_gb300 -- AdamW with packed, quantized persistent moment state on
+NVIDIA GB300 (sm_103a).
+
+A thin ctypes binding over libpackedadam.so (C ABI in include/packedadam.h).
+Each function has the name of its C entry point and only marshals arguments:
+torch CUDA tensors become device pointers, the stream defaults to torch's
+current stream, and a non-zero status raises PackedAdamError with the
+library's message.  Every step of the update runs in the library's kernels;
+there is no fallback.  Importing the package loads the library and fails with
+ImportError if it has not been built (python adamw_update_gb300/build.py).
+
+Sources: "Packed AdamW Reference" README v1.0.0, "The canonical format"
+(one uint32 word per FP32 parameter: E4M11 first moment low, E4M12
+uncorrected RMS high); "Packed AdamW / Reference / v1.0.0", "Release scope"
+and "Execution contract"; KBench "quantized-optimizer-state" reference.py,
+quantized_adamw_step (8-bit blockwise mode).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "PackedAdamError", "library_path", "pa_version", "pa_status_string",
+    "pa_encode_state", "pa_decode_state", "pa_encode_state_fp16", "pa_decode_state_fp16",
+    "pa_adamw_step_packed_e4", "pa_adamw_step_packed_fp16", "pa_adamw_step_fp32",
+    "pa_adamw_step_blockwise8", "pa_adamw_step_packed_e4_multi",
+    "pa_adamw_step_packed_fp16_multi", "pa_adamw_step_fp32_multi", "pa_release_tables",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def library_path(fast: bool = False) -> str:
+    return os.path.join(_HERE, "libpackedadam_fast.so" if fast else "libpackedadam.so")
+
+
+class PackedAdamError(RuntimeError):
+    def __init__(self, status: int, name: str, message: str):
+        super().__init__(f"{name}: {message}")
+        self.status = status
+
+
+class PaTensor(ctypes.Structure):
+    """pa_tensor: {float* p; const float* g; void* state; void* state2; int64 n}."""
+    _fields_ = [("p", ctypes.c_void_p), ("g", ctypes.c_void_p), ("state", ctypes.c_void_p),
+                ("state2", ctypes.c_void_p), ("n", ctypes.c_int64)]
+
+
+_vp, _i64, _i32, _d = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_double
+_HYP = [_i64, _d, _d, _d, _d, _d]  # step, lr, beta1, beta2, eps, wd
+_SIGNATURES = {
+    "pa_version": (_i32, []),
+    "pa_status_string": (ctypes.c_char_p, [_i32]),
+    "pa_last_error": (ctypes.c_char_p, []),
+    "pa_encode_state": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp]),
+    "pa_decode_state": (_i32, [_vp, _vp, _vp, _i64, _vp]),
+    "pa_encode_state_fp16": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp]),
+    "pa_decode_state_fp16": (_i32, [_vp, _vp, _vp, _i64, _vp]),
+    "pa_adamw_step_packed_e4": (_i32, [_vp, _vp, _vp, _i64, *_HYP, _vp, _vp]),
+    "pa_adamw_step_packed_fp16": (_i32, [_vp, _vp, _vp, _i64, *_HYP, _vp, _vp]),
+    "pa_adamw_step_fp32": (_i32, [_vp, _vp, _vp, _vp, _i64, *_HYP, _vp, _vp]),
+    "pa_adamw_step_blockwise8": (_i32, [_vp] * 9 + [_i64, *_HYP, _vp, _vp]),
+    "pa_adamw_step_packed_e4_multi": (_i32, [ctypes.POINTER(PaTensor), _i32, *_HYP, _vp, _vp]),
+    "pa_adamw_step_packed_fp16_multi": (_i32, [ctypes.POINTER(PaTensor), _i32, *_HYP, _vp, _vp]),
+    "pa_adamw_step_fp32_multi": (_i32, [ctypes.POINTER(PaTensor), _i32, *_HYP, _vp, _vp]),
+    "pa_release_tables": (_i32, []),
+}
+
+
+def load_library(path: str) -> ctypes.CDLL:
+    """Load a build of libpackedadam.so and declare its C signatures."""
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+if not os.path.exists(library_path()):
+    raise ImportError(f"{library_path()} is missing: build it with "
+                      "`python adamw_update_gb300/build.py` (needs nvcc)")
+_lib = load_library(library_path())
+
+
+def _check(status: int):
+    if status != 0:
+        name = _lib.pa_status_string(status).decode()
+        raise PackedAdamError(status, name, _lib.pa_last_error().decode())
+
+
+def _ptr(t, dtype=None):
+    """Device pointer of a contiguous CUDA tensor (None -> NULL)."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor (device memory)")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"expected dtype {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    return stream if isinstance(stream, int) else stream.cuda_stream
+
+
+def _hyp(step, lr, beta1, beta2, eps, wd):
+    return (int(step), float(lr), float(beta1), float(beta2), float(eps), float(wd))
+
+
+def _t():
+    import torch
+
+    return torch
+
+
+def pa_version() -> int:
+    return _lib.pa_version()
+
+
+def pa_status_string(status: int) -> str:
+    return _lib.pa_status_string(status).decode()
+
+
+# ---- codecs -----------------------------------------------------------------
+
+def pa_encode_state(m, rms, word, nonfinite=None, stream=None):
+    """word[i] = E4M12(rms[i]) << 16 | E4M11(m[i])."""
+    torch = _t()
+    _check(_lib.pa_encode_state(_ptr(m, torch.float32), _ptr(rms, torch.float32),
+                                _ptr(word, torch.int32), m.numel(), _ptr(nonfinite),
+                                _stream(stream)))
+
+
+def pa_decode_state(word, m, rms, stream=None):
+    torch = _t()
+    _check(_lib.pa_decode_state(_ptr(word, torch.int32), _ptr(m, torch.float32),
+                                _ptr(rms, torch.float32), word.numel(), _stream(stream)))
+
+
+def pa_encode_state_fp16(m, rms, word, nonfinite=None, stream=None):
+    torch = _t()
+    _check(_lib.pa_encode_state_fp16(_ptr(m, torch.float32), _ptr(rms, torch.float32),
+                                     _ptr(word, torch.int32), m.numel(), _ptr(nonfinite),
+                                     _stream(stream)))
+
+
+def pa_decode_state_fp16(word, m, rms, stream=None):
+    torch = _t()
+    _check(_lib.pa_decode_state_fp16(_ptr(word, torch.int32), _ptr(m, torch.float32),
+                                     _ptr(rms, torch.float32), word.numel(), _stream(stream)))
+
+
+# ---- single-tensor steps (state words are int32 tensors holding uint32 bits) --
+
+def pa_adamw_step_packed_e4(p, g, state, step, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8,
+                            wd=0.0, nonfinite=None, stream=None):
+    torch = _t()
+    _check(_lib.pa_adamw_step_packed_e4(_ptr(p, torch.float32), _ptr(g, torch.float32),
+                                        _ptr(state, torch.int32), p.numel(),
+                                        *_hyp(step, lr, beta1, beta2, eps, wd),
+                                        _ptr(nonfinite), _stream(stream)))
+
+
+def pa_adamw_step_packed_fp16(p, g, state, step, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8,
+                              wd=0.0, nonfinite=None, stream=None):
+    torch = _t()
+    _check(_lib.pa_adamw_step_packed_fp16(_ptr(p, torch.float32), _ptr(g, torch.float32),
+                                          _ptr(state, torch.int32), p.numel(),
+                                          *_hyp(step, lr, beta1, beta2, eps, wd),
+                                          _ptr(nonfinite), _stream(stream)))
+
+
+def pa_adamw_step_fp32(p, g, m, v, step, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, wd=0.0,
+                       nonfinite=None, stream=None):
+    torch = _t()
+    _check(_lib.pa_adamw_step_fp32(_ptr(p, torch.float32), _ptr(g, torch.float32),
+                                   _ptr(m, torch.float32), _ptr(v, torch.float32), p.numel(),
+                                   *_hyp(step, lr, beta1, beta2, eps, wd),
+                                   _ptr(nonfinite), _stream(stream)))
+
+
+def pa_adamw_step_blockwise8(p, g, p_bf16, m_code, m_absmax, v_code, v_absmax, qmap1, qmap2,
+                             step, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, wd=0.01,
+                             nonfinite=None, stream=None):
+    torch = _t()
+    _check(_lib.pa_adamw_step_blockwise8(
+        _ptr(p, torch.float32), _ptr(g, torch.float32), _ptr(p_bf16, torch.bfloat16),
+        _ptr(m_code, torch.uint8), _ptr(m_absmax, torch.float32), _ptr(v_code, torch.uint8),
+        _ptr(v_absmax, torch.float32), _ptr(qmap1, torch.float32), _ptr(qmap2, torch.float32),
+        p.numel(), *_hyp(step, lr, beta1, beta2, eps, wd), _ptr(nonfinite), _stream(stream)))
+
+
+# ---- multi-tensor steps --------------------------------------------------------
+
+def tensor_list(entries, fp32: bool = False):
+    """ctypes pa_tensor array from (p, g, state) or (p, g, m, v) tuples."""
+    torch = _t()
+    arr = (PaTensor * len(entries))()
+    for k, e in enumerate(entries):
+        if fp32:
+            p, g, m, v = e
+            arr[k] = PaTensor(_ptr(p, torch.float32), _ptr(g, torch.float32),
+                              _ptr(m, torch.float32), _ptr(v, torch.float32), p.numel())
+        else:
+            p, g, s = e
+            arr[k] = PaTensor(_ptr(p, torch.float32), _ptr(g, torch.float32),
+                              _ptr(s, torch.int32), None, p.numel())
+    return arr
+
+
+def _multi(fn, entries, fp32, step, lr, beta1, beta2, eps, wd, nonfinite, stream):
+    arr = entries if isinstance(entries, ctypes.Array) else tensor_list(entries, fp32)
+    _check(fn(arr, len(arr), *_hyp(step, lr, beta1, beta2, eps, wd), _ptr(nonfinite),
+              _stream(stream)))
+
+
+def pa_adamw_step_packed_e4_multi(entries, step, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8,
+                                  wd=0.0, nonfinite=None, stream=None):
+    """One launch over a list of (p, g, state) tensors (or a tensor_list array)."""
+    _multi(_lib.pa_adamw_step_packed_e4_multi, entries, False, step, lr, beta1, beta2, eps, wd,
+           nonfinite, stream)
+
+
+def pa_adamw_step_packed_fp16_multi(entries, step, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8,
+                                    wd=0.0, nonfinite=None, stream=None):
+    _multi(_lib.pa_adamw_step_packed_fp16_multi, entries, False, step, lr, beta1, beta2, eps,
+           wd, nonfinite, stream)
+
+
+def pa_adamw_step_fp32_multi(entries, step, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, wd=0.0,
+                             nonfinite=None, stream=None):
+    """One launch over a list of (p, g, m, v) tensors (or a tensor_list array)."""
+    _multi(_lib.pa_adamw_step_fp32_multi, entries, True, step, lr, beta1, beta2, eps, wd,
+           nonfinite, stream)
+
+
+def pa_release_tables():
+    _check(_lib.pa_release_tables())

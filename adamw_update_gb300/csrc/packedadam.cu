@@ -1,0 +1,906 @@
+// packedadam.cu -- CUDA kernels (sm_103a) and the C ABI of libpackedadam.so.
+//
+// The AdamW update with packed persistent moment state ("Packed AdamW
+// Reference" README v1.0.0, "The canonical format"; "Packed AdamW / Reference
+// / v1.0.0" code page, "Release scope"), its FP32 and FP16-first/FP16-RMS
+// comparison modes, and the 8-bit blockwise mode of KBench
+// "quantized-optimizer-state" reference.py (quantized_adamw_step,
+// _requantise).  The declarations, numerics and error rules are documented in
+// include/packedadam.h.
+//
+// Design.  The step is elementwise and bound by HBM bandwidth (20 bytes per
+// parameter for the packed modes), so the kernels are built for bytes in
+// flight: a persistent grid (resident CTAs per SM x SM count) strides over
+// 4096-element chunks; every thread issues all of its 16-byte loads of p, g
+// and the state for a chunk before any arithmetic, then stores with streaming
+// hints.  A multi-tensor list becomes one launch over a device-side
+// descriptor table, whose chunk prefix sums let each CTA walk from tensor to
+// tensor without a search.  No tensor cores: nothing here is a contraction.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "codecs.cuh"
+#include "packedadam.h"
+
+namespace pa {
+
+constexpr int kThreads = 256;         // threads per CTA
+#ifndef PA_UNROLL
+#define PA_UNROLL 4
+#endif
+constexpr int kUnroll = PA_UNROLL;    // 16-byte vectors per thread per chunk
+constexpr int64_t kChunk = (int64_t)kThreads * kUnroll * 4;  // elements per chunk
+
+enum Mode : int { kE4 = 0, kFP16 = 1, kF32 = 2 };
+
+// One tensor of a step.  The 16-byte body starts `head` elements in; `vec`
+// is 0 when p, g and the state do not share their address modulo 16, and the
+// tensor then runs on 4-byte accesses.
+struct Desc {
+    float *p;
+    const float *g;
+    void *s1;        // uint32 words (packed modes) or FP32 m
+    void *s2;        // FP32 v (FP32 mode)
+    int64_t n;
+    int64_t chunk0;  // first global chunk index of this tensor
+    int32_t head;
+    int32_t vec;
+};
+
+// ---- memory access helpers --------------------------------------------------
+__device__ __forceinline__ float4 load_stream(const float *a) { return __ldcs(reinterpret_cast<const float4 *>(a)); }
+__device__ __forceinline__ uint4 load_stream(const uint32_t *a) { return __ldcs(reinterpret_cast<const uint4 *>(a)); }
+__device__ __forceinline__ float4 load_readonly(const float *a) { return __ldg(reinterpret_cast<const float4 *>(a)); }
+__device__ __forceinline__ void store_stream(float *a, float4 x) { __stcs(reinterpret_cast<float4 *>(a), x); }
+__device__ __forceinline__ void store_stream(uint32_t *a, uint4 x) { __stcs(reinterpret_cast<uint4 *>(a), x); }
+
+// ---- one element of a packed step -------------------------------------------
+// Decode the prior state, v = r*r, FP32 update, encode m' and sqrt(v') into the
+// next word ("Release scope": the state is stored only after the update).
+template <int MODE>
+__device__ __forceinline__ uint32_t packed_element(float &p, float g, uint32_t w,
+                                                   const Scalars &s, uint32_t &bad)
+{
+    const float m = MODE == kE4 ? decode_m_lane(w) : decode_fp16_low(w);
+    const float r = MODE == kE4 ? decode_rms_lane(w) : decode_fp16_high(w);
+    const Moments o = adamw_element(p, g, m, __fmul_rn(r, r), s);
+    bad += any_nonfinite(o);
+    p = o.p;
+    const float rn = __fsqrt_rn(o.v);
+    return MODE == kE4 ? encode_word_e4(o.m, rn) : encode_word_fp16(o.m, rn);
+}
+
+// Element i of tensor d with 4-byte accesses (heads, tails, unaligned tensors).
+template <int MODE>
+__device__ __forceinline__ void scalar_element(const Desc &d, int64_t i, const Scalars &s,
+                                               uint32_t &bad)
+{
+    float p = d.p[i];
+    const float g = __ldg(d.g + i);
+    if constexpr (MODE == kF32) {
+        float *m = static_cast<float *>(d.s1);
+        float *v = static_cast<float *>(d.s2);
+        const Moments o = adamw_element(p, g, m[i], v[i], s);
+        bad += any_nonfinite(o);
+        d.p[i] = o.p;
+        m[i] = o.m;
+        v[i] = o.v;
+    } else {
+        uint32_t *w = static_cast<uint32_t *>(d.s1);
+        const uint32_t nw = packed_element<MODE>(p, g, w[i], s, bad);
+        d.p[i] = p;
+        w[i] = nw;
+    }
+}
+
+// Chunk k of a 16-byte-path tensor: body elements [k*kChunk, (k+1)*kChunk)
+// counted from d.head.  All loads of the chunk are issued before any compute.
+template <int MODE>
+__device__ __forceinline__ void vector_chunk(const Desc &d, int64_t k, const Scalars &s,
+                                             uint32_t &bad)
+{
+    const int tid = threadIdx.x;
+    const int64_t nb = d.n - d.head;
+    const int64_t base = k * kChunk;
+    if (k == 0 && tid < d.head)
+        scalar_element<MODE>(d, tid, s, bad);
+    float *P = d.p + d.head;
+    const float *G = d.g + d.head;
+
+    float4 pv[kUnroll], gv[kUnroll];
+    uint4 wv[kUnroll];
+    float4 mv[kUnroll], vv[kUnroll];
+    bool full[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+        const int64_t e = base + 4 * ((int64_t)u * kThreads + tid);
+        full[u] = e + 4 <= nb;
+        if (full[u]) {
+            pv[u] = load_stream(P + e);
+            gv[u] = load_readonly(G + e);
+            if constexpr (MODE == kF32) {
+                mv[u] = load_stream(static_cast<float *>(d.s1) + d.head + e);
+                vv[u] = load_stream(static_cast<float *>(d.s2) + d.head + e);
+            } else {
+                wv[u] = load_stream(static_cast<uint32_t *>(d.s1) + d.head + e);
+            }
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+        const int64_t e = base + 4 * ((int64_t)u * kThreads + tid);
+        if (full[u]) {
+            float pp[4] = {pv[u].x, pv[u].y, pv[u].z, pv[u].w};
+            const float gg[4] = {gv[u].x, gv[u].y, gv[u].z, gv[u].w};
+            if constexpr (MODE == kF32) {
+                float mm[4] = {mv[u].x, mv[u].y, mv[u].z, mv[u].w};
+                float vq[4] = {vv[u].x, vv[u].y, vv[u].z, vv[u].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const Moments o = adamw_element(pp[j], gg[j], mm[j], vq[j], s);
+                    bad += any_nonfinite(o);
+                    pp[j] = o.p;
+                    mm[j] = o.m;
+                    vq[j] = o.v;
+                }
+                store_stream(static_cast<float *>(d.s1) + d.head + e, make_float4(mm[0], mm[1], mm[2], mm[3]));
+                store_stream(static_cast<float *>(d.s2) + d.head + e, make_float4(vq[0], vq[1], vq[2], vq[3]));
+            } else {
+                uint32_t ww[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    ww[j] = packed_element<MODE>(pp[j], gg[j], ww[j], s, bad);
+                store_stream(static_cast<uint32_t *>(d.s1) + d.head + e, make_uint4(ww[0], ww[1], ww[2], ww[3]));
+            }
+            store_stream(P + e, make_float4(pp[0], pp[1], pp[2], pp[3]));
+        } else if (e < nb) {
+            // the one vector that straddles the end of the tensor
+            for (int64_t i = e; i < nb; ++i)
+                scalar_element<MODE>(d, d.head + i, s, bad);
+        }
+    }
+}
+
+// Chunk k of a 4-byte-path tensor: elements [k*kChunk, (k+1)*kChunk).
+template <int MODE>
+__device__ __forceinline__ void scalar_chunk(const Desc &d, int64_t k, const Scalars &s,
+                                             uint32_t &bad)
+{
+    const int64_t base = k * kChunk;
+#pragma unroll 4
+    for (int u = 0; u < kUnroll * 4; ++u) {
+        const int64_t i = base + (int64_t)u * kThreads + threadIdx.x;
+        if (i < d.n)
+            scalar_element<MODE>(d, i, s, bad);
+    }
+}
+
+__device__ __forceinline__ void flush_nonfinite(uint32_t bad, unsigned long long *nonfinite)
+{
+    if (nonfinite == nullptr)
+        return;
+    const uint32_t total = __reduce_add_sync(0xFFFFFFFFu, bad);
+    if ((threadIdx.x & 31) == 0 && total != 0)
+        atomicAdd(nonfinite, (unsigned long long)total);
+}
+
+// The persistent step kernel.  MULTI: walk the device descriptor table (each
+// CTA visits chunks in increasing order, so the tensor index only moves
+// forward); otherwise the single descriptor passed by value.
+template <int MODE, bool MULTI>
+__global__ void __launch_bounds__(kThreads)
+adamw_step_kernel(const Desc *__restrict__ table, int32_t ntensors, int64_t total_chunks,
+                  const Desc single, const Scalars s, unsigned long long *nonfinite)
+{
+    uint32_t bad = 0;
+    int32_t t = 0;
+    Desc d = single;
+    int64_t next = total_chunks;
+    if constexpr (MULTI) {
+        d = table[0];
+        next = ntensors > 1 ? table[1].chunk0 : total_chunks;
+    }
+    for (int64_t c = blockIdx.x; c < total_chunks; c += gridDim.x) {
+        if constexpr (MULTI) {
+            while (c >= next) {
+                ++t;
+                d = table[t];
+                next = t + 1 < ntensors ? table[t + 1].chunk0 : total_chunks;
+            }
+        }
+        const int64_t k = c - d.chunk0;
+        if (d.vec)
+            vector_chunk<MODE>(d, k, s, bad);
+        else
+            scalar_chunk<MODE>(d, k, s, bad);
+    }
+    flush_nonfinite(bad, nonfinite);
+}
+
+// ---- standalone codecs ("Packed AdamW Reference" README: inspect-formats) -------
+template <int MODE>
+__global__ void __launch_bounds__(kThreads)
+encode_state_kernel(const float *__restrict__ m, const float *__restrict__ rms,
+                    uint32_t *__restrict__ word, int64_t n, unsigned long long *nonfinite)
+{
+    uint32_t bad = 0;
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < n; i += stride) {
+        const float a = __ldg(m + i), b = __ldg(rms + i);
+        word[i] = MODE == kE4 ? encode_word_e4(a, b) : encode_word_fp16(a, b);
+        const uint32_t ea = __float_as_uint(a) & 0x7FFFFFFFu, eb = __float_as_uint(b) & 0x7FFFFFFFu;
+        bad += max(ea, eb) >= 0x7F800000u ? 1u : 0u;
+    }
+    flush_nonfinite(bad, nonfinite);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads)
+decode_state_kernel(const uint32_t *__restrict__ word, float *__restrict__ m,
+                    float *__restrict__ rms, int64_t n)
+{
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < n; i += stride) {
+        const uint32_t w = __ldg(word + i);
+        m[i] = MODE == kE4 ? decode_m_lane(w) : decode_fp16_low(w);
+        rms[i] = MODE == kE4 ? decode_rms_lane(w) : decode_fp16_high(w);
+    }
+}
+
+// ---- 8-bit blockwise mode (KBench quantized_adamw_step, _requantise) -------------
+// One CTA of 256 threads owns one 2048-element block per iteration of a
+// persistent loop.  Thread t holds elements 4t..4t+3 and 1024+4t..1024+4t+3 of
+// the block (16-byte loads of p and g, 4-byte loads of each code array).  The
+// new block absmax is a warp max (redux.sync on the binary32 bits of |x|,
+// which orders non-negative floats and lets a NaN win) followed by a max over
+// the 8 warp results in shared memory.  The code is the count of midpoints
+// below x / max(absmax, 1e-30), found by an 8-step binary search over the
+// midpoints held in shared memory.
+constexpr int kBlock = 2048;
+
+__device__ __forceinline__ int count_below(const float *mid, float c)
+{
+    int pos = 0;
+#pragma unroll
+    for (int step = 128; step >= 1; step >>= 1)
+        pos += (mid[pos + step - 1] < c) ? step : 0;
+    return pos;
+}
+
+__global__ void __launch_bounds__(kThreads)
+blockwise8_kernel(const float *__restrict__ p, const float *__restrict__ g,
+                  uint16_t *__restrict__ p_bf16, uint8_t *__restrict__ m_code,
+                  float *__restrict__ m_absmax, uint8_t *__restrict__ v_code,
+                  float *__restrict__ v_absmax, const float *__restrict__ qmap1,
+                  const float *__restrict__ qmap2, int64_t n, int64_t nblocks, const Scalars s,
+                  unsigned long long *nonfinite)
+{
+    __shared__ float q1[256], q2[256], mid1[256], mid2[256];
+    __shared__ uint32_t warp_max[2][2][kThreads / 32];  // [iteration parity][m, v][warp]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    q1[tid] = __ldg(qmap1 + tid);
+    q2[tid] = __ldg(qmap2 + tid);
+    __syncthreads();
+    mid1[tid] = tid < 255 ? __fmul_rn(__fadd_rn(q1[tid], q1[tid + 1]), 0.5f) : INFINITY;
+    mid2[tid] = tid < 255 ? __fmul_rn(__fadd_rn(q2[tid], q2[tid + 1]), 0.5f) : INFINITY;
+    __syncthreads();
+
+    const uint32_t floor_bits = __float_as_uint(1e-30f);
+    uint32_t bad = 0;
+    int parity = 0;
+    for (int64_t b = blockIdx.x; b < nblocks; b += gridDim.x, parity ^= 1) {
+        const int64_t base = b * kBlock;
+        const bool whole = base + kBlock <= n;
+        const float am = m_absmax[b], av = v_absmax[b];
+        float mn[8], vn[8];
+        uint32_t um = 0, uv = 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int64_t e0 = base + 1024 * h + 4 * tid;
+            float pv[4], gv[4];
+            uint32_t mc, vc;
+            if (whole) {
+                const float4 a = __ldg(reinterpret_cast<const float4 *>(p + e0));
+                const float4 c = __ldg(reinterpret_cast<const float4 *>(g + e0));
+                pv[0] = a.x; pv[1] = a.y; pv[2] = a.z; pv[3] = a.w;
+                gv[0] = c.x; gv[1] = c.y; gv[2] = c.z; gv[3] = c.w;
+                mc = *reinterpret_cast<const uint32_t *>(m_code + e0);
+                vc = *reinterpret_cast<const uint32_t *>(v_code + e0);
+            } else {
+                mc = vc = 0;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const bool in = e0 + j < n;
+                    pv[j] = in ? p[e0 + j] : 0.0f;
+                    gv[j] = in ? g[e0 + j] : 0.0f;
+                    mc |= (in ? (uint32_t)m_code[e0 + j] : 0u) << (8 * j);
+                    vc |= (in ? (uint32_t)v_code[e0 + j] : 0u) << (8 * j);
+                }
+            }
+            float po[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float m = __fmul_rn(q1[(mc >> (8 * j)) & 0xFFu], am);
+                const float v = __fmul_rn(q2[(vc >> (8 * j)) & 0xFFu], av);
+                const Moments o = adamw_element(pv[j], gv[j], m, v, s);
+                const bool in = whole || e0 + j < n;
+                bad += in ? any_nonfinite(o) : 0u;
+                po[j] = o.p;
+                mn[4 * h + j] = in ? o.m : 0.0f;
+                vn[4 * h + j] = in ? o.v : 0.0f;
+                um = max(um, __float_as_uint(mn[4 * h + j]) & 0x7FFFFFFFu);
+                uv = max(uv, __float_as_uint(vn[4 * h + j]) & 0x7FFFFFFFu);
+            }
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(po[0], po[1]);
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(po[2], po[3]);
+            if (whole) {
+                uint2 packed;
+                packed.x = *reinterpret_cast<const uint32_t *>(&lo);
+                packed.y = *reinterpret_cast<const uint32_t *>(&hi);
+                __stcs(reinterpret_cast<uint2 *>(p_bf16 + e0), packed);
+            } else {
+                const __nv_bfloat16 hv[4] = {lo.x, lo.y, hi.x, hi.y};
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (e0 + j < n)
+                        p_bf16[e0 + j] = *reinterpret_cast<const uint16_t *>(&hv[j]);
+            }
+        }
+        // block absmax of m' and v'
+        um = __reduce_max_sync(0xFFFFFFFFu, um);
+        uv = __reduce_max_sync(0xFFFFFFFFu, uv);
+        if (lane == 0) {
+            warp_max[parity][0][warp] = um;
+            warp_max[parity][1][warp] = uv;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) {
+            um = max(um, warp_max[parity][0][w]);
+            uv = max(uv, warp_max[parity][1][w]);
+        }
+        if (tid == 0) {
+            m_absmax[b] = __uint_as_float(um);
+            v_absmax[b] = __uint_as_float(uv);
+        }
+        const float sm = __uint_as_float(max(um, floor_bits));  // NaN bits stay NaN
+        const float sv = __uint_as_float(max(uv, floor_bits));
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int64_t e0 = base + 1024 * h + 4 * tid;
+            uint32_t mc = 0, vc = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                mc |= (uint32_t)count_below(mid1, __fdiv_rn(mn[4 * h + j], sm)) << (8 * j);
+                vc |= (uint32_t)count_below(mid2, __fdiv_rn(vn[4 * h + j], sv)) << (8 * j);
+            }
+            if (whole) {
+                *reinterpret_cast<uint32_t *>(m_code + e0) = mc;
+                *reinterpret_cast<uint32_t *>(v_code + e0) = vc;
+            } else {
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    if (e0 + j < n) {
+                        m_code[e0 + j] = (uint8_t)(mc >> (8 * j));
+                        v_code[e0 + j] = (uint8_t)(vc >> (8 * j));
+                    }
+            }
+        }
+    }
+    flush_nonfinite(bad, nonfinite);
+}
+
+}  // namespace pa
+
+// ===========================================================================
+// Host side
+// ===========================================================================
+namespace {
+
+using pa::Desc;
+using pa::Scalars;
+
+thread_local std::string g_last_error;
+
+pa_status fail(pa_status code, const char *fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return code;
+}
+
+pa_status ok()
+{
+    g_last_error.clear();
+    return PA_OK;
+}
+
+pa_status cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(PA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void *ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+// Hyperparameters -> FP32 scalars: each formed in double, rounded once to
+// float (KBench quantized_adamw_step forms them in double precision).
+// step is the 1-based global step ("Execution contract": one global step).
+pa_status make_scalars(int64_t step, double lr, double beta1, double beta2, double eps,
+                       double wd, Scalars *s)
+{
+    if (step < 1)
+        return fail(PA_ERR_ARG, "step must be >= 1 (got %lld)", (long long)step);
+    if (!std::isfinite(lr) || !std::isfinite(eps) || !std::isfinite(wd) ||
+        !std::isfinite(beta1) || !std::isfinite(beta2))
+        return fail(PA_ERR_ARG, "hyperparameters must be finite");
+    if (!(beta1 >= 0.0 && beta1 < 1.0) || !(beta2 >= 0.0 && beta2 < 1.0))
+        return fail(PA_ERR_ARG, "betas must lie in [0, 1) (got %g, %g)", beta1, beta2);
+    if (eps < 0.0)
+        return fail(PA_ERR_ARG, "eps must be >= 0 (got %g)", eps);
+    s->b1 = (float)beta1;
+    s->b2 = (float)beta2;
+    s->c1 = (float)(1.0 - beta1);
+    s->c2 = (float)(1.0 - beta2);
+    s->bc2 = (float)(1.0 - std::pow(beta2, (double)step));
+    s->ss = (float)(lr / (1.0 - std::pow(beta1, (double)step)));
+    s->dk = (float)(1.0 - lr * wd);
+    s->ef = (float)eps;
+    return PA_OK;
+}
+
+// ---- per-device launch geometry --------------------------------------------
+struct DeviceInfo {
+    bool ready = false;
+    int sms = 0;
+    int occ[8] = {0};  // resident CTAs per SM, by kernel slot
+};
+
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+
+enum KernelSlot { kSlotE4, kSlotFP16, kSlotF32, kSlotE4Multi, kSlotFP16Multi, kSlotF32Multi, kSlotBlockwise, kSlotCodec };
+
+const void *kernel_of(int slot)
+{
+    switch (slot) {
+    case kSlotE4: return (const void *)pa::adamw_step_kernel<pa::kE4, false>;
+    case kSlotFP16: return (const void *)pa::adamw_step_kernel<pa::kFP16, false>;
+    case kSlotF32: return (const void *)pa::adamw_step_kernel<pa::kF32, false>;
+    case kSlotE4Multi: return (const void *)pa::adamw_step_kernel<pa::kE4, true>;
+    case kSlotFP16Multi: return (const void *)pa::adamw_step_kernel<pa::kFP16, true>;
+    case kSlotF32Multi: return (const void *)pa::adamw_step_kernel<pa::kF32, true>;
+    case kSlotBlockwise: return (const void *)pa::blockwise8_kernel;
+    default: return (const void *)pa::encode_state_kernel<pa::kE4>;
+    }
+}
+
+// Persistent grid size for a kernel on the current device: resident CTAs per
+// SM times the SM count, capped by the work items.
+pa_status grid_for(int slot, int64_t work, int *grid)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64)
+        return fail(PA_ERR_CUDA, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    DeviceInfo &di = g_dev[dev];
+    if (!di.ready) {
+        e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        for (int k = 0; k < 8; ++k) {
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&di.occ[k], kernel_of(k), pa::kThreads, 0);
+            if (e != cudaSuccess)
+                return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+            if (di.occ[k] < 1)
+                di.occ[k] = 1;
+        }
+        di.ready = true;
+    }
+    const int64_t full = (int64_t)di.sms * di.occ[slot];
+    *grid = (int)(work < full ? (work > 0 ? work : 1) : full);
+    return PA_OK;
+}
+
+pa_status check_launch(const char *what)
+{
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return cuda_fail(e, what);
+    return ok();
+}
+
+// ---- descriptors -------------------------------------------------------------
+// Fill d for one tensor; returns its chunk count.  The 16-byte path needs p, g
+// and the state (and v in FP32 mode) to share their address modulo 16; the
+// head peels the elements before the first 16-byte boundary.
+int64_t describe(const pa_tensor &t, int mode, Desc *d)
+{
+    d->p = t.p;
+    d->g = t.g;
+    d->s1 = t.state;
+    d->s2 = t.state2;
+    d->n = t.n;
+    const uintptr_t ph = reinterpret_cast<uintptr_t>(t.p) & 15u;
+    bool same = (reinterpret_cast<uintptr_t>(t.g) & 15u) == ph &&
+                (reinterpret_cast<uintptr_t>(t.state) & 15u) == ph;
+    if (mode == pa::kF32)
+        same = same && (reinterpret_cast<uintptr_t>(t.state2) & 15u) == ph;
+    d->vec = same ? 1 : 0;
+    int64_t head = same ? (int64_t)(((16u - ph) & 15u) / 4u) : 0;
+    if (head > t.n)
+        head = t.n;
+    d->head = (int32_t)head;
+    if (t.n == 0)
+        return 0;
+    const int64_t body = same ? t.n - head : t.n;
+    const int64_t chunks = (body + pa::kChunk - 1) / pa::kChunk;
+    return chunks > 0 ? chunks : 1;
+}
+
+pa_status check_tensor(const pa_tensor &t, int mode, int index)
+{
+    if (t.n < 0)
+        return fail(PA_ERR_ARG, "tensor %d: n must be >= 0 (got %lld)", index, (long long)t.n);
+    if (t.n == 0)
+        return PA_OK;
+    if (!t.p || !t.g || !t.state || (mode == pa::kF32 && !t.state2))
+        return fail(PA_ERR_NULL, "tensor %d: NULL pointer with n = %lld", index, (long long)t.n);
+    if (!aligned(t.p, 4) || !aligned(t.g, 4) || !aligned(t.state, 4) ||
+        (mode == pa::kF32 && !aligned(t.state2, 4)))
+        return fail(PA_ERR_ALIGN, "tensor %d: pointers must be 4-byte aligned", index);
+    return PA_OK;
+}
+
+pa_status check_counter(const unsigned long long *nonfinite)
+{
+    if (nonfinite && !aligned(nonfinite, 8))
+        return fail(PA_ERR_ALIGN, "nonfinite counter must be 8-byte aligned");
+    return PA_OK;
+}
+
+template <int MODE>
+pa_status step_single(const pa_tensor &t, int64_t step, double lr, double beta1, double beta2,
+                      double eps, double wd, unsigned long long *nonfinite, pa_stream stream)
+{
+    Scalars s;
+    pa_status st = make_scalars(step, lr, beta1, beta2, eps, wd, &s);
+    if (st != PA_OK)
+        return st;
+    if ((st = check_tensor(t, MODE, 0)) != PA_OK || (st = check_counter(nonfinite)) != PA_OK)
+        return st;
+    if (t.n == 0)
+        return ok();
+    Desc d;
+    const int64_t chunks = describe(t, MODE, &d);
+    d.chunk0 = 0;
+    int grid = 0;
+    if ((st = grid_for(MODE, chunks, &grid)) != PA_OK)
+        return st;
+    pa::adamw_step_kernel<MODE, false><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
+        nullptr, 1, chunks, d, s, nonfinite);
+    return check_launch("adamw_step_kernel launch");
+}
+
+// ---- cached device descriptor tables (multi-tensor calls) -----------------------
+// A list is uploaded once per device and reused while it is unchanged, so a
+// training loop that steps the same tensors pays no host-to-device copy.  The
+// table of a list is immutable once uploaded, so calls on different streams
+// never see a table change under them.
+struct Table {
+    int device;
+    int mode;
+    std::vector<Desc> host;
+    Desc *dev;
+    int64_t chunks;
+    uint64_t last_use;
+};
+
+std::mutex g_tab_mu;
+std::vector<Table> g_tables;
+uint64_t g_tick = 0;
+constexpr size_t kMaxTables = 64;
+
+pa_status table_for(const pa_tensor *list, int32_t ntensors, int mode, const Desc **dev_table,
+                    int64_t *chunks)
+{
+    std::vector<Desc> host((size_t)ntensors);
+    int64_t total = 0;
+    for (int32_t i = 0; i < ntensors; ++i) {
+        const int64_t c = describe(list[i], mode, &host[(size_t)i]);
+        host[(size_t)i].chunk0 = total;
+        total += c;
+    }
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lock(g_tab_mu);
+    ++g_tick;
+    for (Table &t : g_tables) {
+        if (t.device == dev && t.mode == mode && t.host.size() == host.size() &&
+            std::memcmp(t.host.data(), host.data(), host.size() * sizeof(Desc)) == 0) {
+            t.last_use = g_tick;
+            *dev_table = t.dev;
+            *chunks = t.chunks;
+            return PA_OK;
+        }
+    }
+    if (g_tables.size() >= kMaxTables) {  // free the least recently used list
+        size_t old = 0;
+        for (size_t k = 1; k < g_tables.size(); ++k)
+            if (g_tables[k].last_use < g_tables[old].last_use)
+                old = k;
+        int cur = dev;
+        cudaSetDevice(g_tables[old].device);
+        cudaFree(g_tables[old].dev);  // synchronises that device: no kernel still reads it
+        cudaSetDevice(cur);
+        g_tables.erase(g_tables.begin() + (long)old);
+    }
+    Table t;
+    t.device = dev;
+    t.mode = mode;
+    t.chunks = total;
+    t.last_use = g_tick;
+    t.dev = nullptr;
+    const size_t bytes = host.size() * sizeof(Desc);
+    e = cudaMalloc((void **)&t.dev, bytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(PA_ERR_NOMEM, "cudaMalloc of a %zu-byte descriptor table: %s", bytes,
+                    cudaGetErrorString(e));
+    }
+    // synchronous copy: the table is complete before any kernel can read it
+    e = cudaMemcpy(t.dev, host.data(), bytes, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) {
+        cudaFree(t.dev);
+        return cuda_fail(e, "descriptor table upload");
+    }
+    t.host = std::move(host);
+    g_tables.push_back(std::move(t));
+    *dev_table = g_tables.back().dev;
+    *chunks = g_tables.back().chunks;
+    return PA_OK;
+}
+
+template <int MODE>
+pa_status step_multi(const pa_tensor *list, int32_t ntensors, int64_t step, double lr,
+                     double beta1, double beta2, double eps, double wd,
+                     unsigned long long *nonfinite, pa_stream stream)
+{
+    Scalars s;
+    pa_status st = make_scalars(step, lr, beta1, beta2, eps, wd, &s);
+    if (st != PA_OK)
+        return st;
+    if (ntensors < 0)
+        return fail(PA_ERR_ARG, "ntensors must be >= 0 (got %d)", ntensors);
+    if (ntensors == 0)
+        return ok();
+    if (!list)
+        return fail(PA_ERR_NULL, "tensor list is NULL with ntensors = %d", ntensors);
+    if ((st = check_counter(nonfinite)) != PA_OK)
+        return st;
+    int64_t total = 0;
+    for (int32_t i = 0; i < ntensors; ++i) {
+        if ((st = check_tensor(list[i], MODE, i)) != PA_OK)
+            return st;
+        total += list[i].n;
+    }
+    if (total == 0)
+        return ok();
+    const Desc *table = nullptr;
+    int64_t chunks = 0;
+    if ((st = table_for(list, ntensors, MODE, &table, &chunks)) != PA_OK)
+        return st;
+    int grid = 0;
+    if ((st = grid_for(MODE + 3, chunks, &grid)) != PA_OK)
+        return st;
+    Desc none;
+    std::memset(&none, 0, sizeof none);
+    pa::adamw_step_kernel<MODE, true><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
+        table, ntensors, chunks, none, s, nonfinite);
+    return check_launch("adamw_step_kernel (multi) launch");
+}
+
+template <int MODE>
+pa_status encode(const float *m, const float *rms, uint32_t *word, int64_t n,
+                 unsigned long long *nonfinite, pa_stream stream)
+{
+    if (n < 0)
+        return fail(PA_ERR_ARG, "n must be >= 0 (got %lld)", (long long)n);
+    if (n == 0)
+        return ok();
+    if (!m || !rms || !word)
+        return fail(PA_ERR_NULL, "NULL pointer with n = %lld", (long long)n);
+    if (!aligned(m, 4) || !aligned(rms, 4) || !aligned(word, 4))
+        return fail(PA_ERR_ALIGN, "pointers must be 4-byte aligned");
+    pa_status st = check_counter(nonfinite);
+    if (st != PA_OK)
+        return st;
+    int grid = 0;
+    if ((st = grid_for(kSlotCodec, (n + pa::kThreads - 1) / pa::kThreads, &grid)) != PA_OK)
+        return st;
+    pa::encode_state_kernel<MODE><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(m, rms, word, n, nonfinite);
+    return check_launch("encode_state_kernel launch");
+}
+
+template <int MODE>
+pa_status decode(const uint32_t *word, float *m, float *rms, int64_t n, pa_stream stream)
+{
+    if (n < 0)
+        return fail(PA_ERR_ARG, "n must be >= 0 (got %lld)", (long long)n);
+    if (n == 0)
+        return ok();
+    if (!m || !rms || !word)
+        return fail(PA_ERR_NULL, "NULL pointer with n = %lld", (long long)n);
+    if (!aligned(m, 4) || !aligned(rms, 4) || !aligned(word, 4))
+        return fail(PA_ERR_ALIGN, "pointers must be 4-byte aligned");
+    int grid = 0;
+    pa_status st = grid_for(kSlotCodec, (n + pa::kThreads - 1) / pa::kThreads, &grid);
+    if (st != PA_OK)
+        return st;
+    pa::decode_state_kernel<MODE><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(word, m, rms, n);
+    return check_launch("decode_state_kernel launch");
+}
+
+}  // namespace
+
+// ===========================================================================
+// C ABI
+// ===========================================================================
+extern "C" {
+
+int32_t pa_version(void) { return 10000; }
+
+const char *pa_status_string(pa_status status)
+{
+    switch (status) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_NULL: return "PA_ERR_NULL";
+    case PA_ERR_ARG: return "PA_ERR_ARG";
+    case PA_ERR_ALIGN: return "PA_ERR_ALIGN";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    case PA_ERR_NOMEM: return "PA_ERR_NOMEM";
+    default: return "PA_ERR_UNKNOWN";
+    }
+}
+
+const char *pa_last_error(void) { return g_last_error.c_str(); }
+
+pa_status pa_encode_state(const float *m, const float *rms, uint32_t *word, int64_t n,
+                          unsigned long long *nonfinite, pa_stream stream)
+{
+    return encode<pa::kE4>(m, rms, word, n, nonfinite, stream);
+}
+
+pa_status pa_decode_state(const uint32_t *word, float *m, float *rms, int64_t n, pa_stream stream)
+{
+    return decode<pa::kE4>(word, m, rms, n, stream);
+}
+
+pa_status pa_encode_state_fp16(const float *m, const float *rms, uint32_t *word, int64_t n,
+                               unsigned long long *nonfinite, pa_stream stream)
+{
+    return encode<pa::kFP16>(m, rms, word, n, nonfinite, stream);
+}
+
+pa_status pa_decode_state_fp16(const uint32_t *word, float *m, float *rms, int64_t n,
+                               pa_stream stream)
+{
+    return decode<pa::kFP16>(word, m, rms, n, stream);
+}
+
+pa_status pa_adamw_step_packed_e4(float *p, const float *g, uint32_t *state, int64_t n,
+                                  int64_t step, double lr, double beta1, double beta2,
+                                  double eps, double wd, unsigned long long *nonfinite,
+                                  pa_stream stream)
+{
+    const pa_tensor t = {p, g, state, nullptr, n};
+    return step_single<pa::kE4>(t, step, lr, beta1, beta2, eps, wd, nonfinite, stream);
+}
+
+pa_status pa_adamw_step_packed_fp16(float *p, const float *g, uint32_t *state, int64_t n,
+                                    int64_t step, double lr, double beta1, double beta2,
+                                    double eps, double wd, unsigned long long *nonfinite,
+                                    pa_stream stream)
+{
+    const pa_tensor t = {p, g, state, nullptr, n};
+    return step_single<pa::kFP16>(t, step, lr, beta1, beta2, eps, wd, nonfinite, stream);
+}
+
+pa_status pa_adamw_step_fp32(float *p, const float *g, float *m, float *v, int64_t n,
+                             int64_t step, double lr, double beta1, double beta2, double eps,
+                             double wd, unsigned long long *nonfinite, pa_stream stream)
+{
+    const pa_tensor t = {p, g, m, v, n};
+    return step_single<pa::kF32>(t, step, lr, beta1, beta2, eps, wd, nonfinite, stream);
+}
+
+pa_status pa_adamw_step_packed_e4_multi(const pa_tensor *list, int32_t ntensors, int64_t step,
+                                        double lr, double beta1, double beta2, double eps,
+                                        double wd, unsigned long long *nonfinite,
+                                        pa_stream stream)
+{
+    return step_multi<pa::kE4>(list, ntensors, step, lr, beta1, beta2, eps, wd, nonfinite, stream);
+}
+
+pa_status pa_adamw_step_packed_fp16_multi(const pa_tensor *list, int32_t ntensors,
+                                          int64_t step, double lr, double beta1, double beta2,
+                                          double eps, double wd, unsigned long long *nonfinite,
+                                          pa_stream stream)
+{
+    return step_multi<pa::kFP16>(list, ntensors, step, lr, beta1, beta2, eps, wd, nonfinite,
+                                 stream);
+}
+
+pa_status pa_adamw_step_fp32_multi(const pa_tensor *list, int32_t ntensors, int64_t step,
+                                   double lr, double beta1, double beta2, double eps,
+                                   double wd, unsigned long long *nonfinite, pa_stream stream)
+{
+    return step_multi<pa::kF32>(list, ntensors, step, lr, beta1, beta2, eps, wd, nonfinite, stream);
+}
+
+pa_status pa_adamw_step_blockwise8(const float *p, const float *g, uint16_t *p_bf16,
+                                   uint8_t *m_code, float *m_absmax, uint8_t *v_code,
+                                   float *v_absmax, const float *qmap1, const float *qmap2,
+                                   int64_t n, int64_t step, double lr, double beta1,
+                                   double beta2, double eps, double wd,
+                                   unsigned long long *nonfinite, pa_stream stream)
+{
+    Scalars s;
+    pa_status st = make_scalars(step, lr, beta1, beta2, eps, wd, &s);
+    if (st != PA_OK)
+        return st;
+    if (n < 0)
+        return fail(PA_ERR_ARG, "n must be >= 0 (got %lld)", (long long)n);
+    if (n == 0)
+        return ok();
+    if (!p || !g || !p_bf16 || !m_code || !m_absmax || !v_code || !v_absmax || !qmap1 || !qmap2)
+        return fail(PA_ERR_NULL, "NULL pointer with n = %lld", (long long)n);
+    if (!aligned(p, 16) || !aligned(g, 16))
+        return fail(PA_ERR_ALIGN, "p and g must be 16-byte aligned");
+    if (!aligned(p_bf16, 8))
+        return fail(PA_ERR_ALIGN, "p_bf16 must be 8-byte aligned");
+    if (!aligned(m_code, 4) || !aligned(v_code, 4))
+        return fail(PA_ERR_ALIGN, "m_code and v_code must be 4-byte aligned");
+    if (!aligned(m_absmax, 4) || !aligned(v_absmax, 4) || !aligned(qmap1, 4) || !aligned(qmap2, 4))
+        return fail(PA_ERR_ALIGN, "absmax arrays and maps must be 4-byte aligned");
+    if ((st = check_counter(nonfinite)) != PA_OK)
+        return st;
+    const int64_t nblocks = (n + pa::kBlock - 1) / pa::kBlock;
+    int grid = 0;
+    if ((st = grid_for(kSlotBlockwise, nblocks, &grid)) != PA_OK)
+        return st;
+    pa::blockwise8_kernel<<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
+        p, g, p_bf16, m_code, m_absmax, v_code, v_absmax, qmap1, qmap2, n, nblocks, s, nonfinite);
+    return check_launch("blockwise8_kernel launch");
+}
+
+pa_status pa_release_tables(void)
+{
+    std::lock_guard<std::mutex> lock(g_tab_mu);
+    int cur = 0;
+    cudaGetDevice(&cur);
+    for (Table &t : g_tables) {
+        cudaSetDevice(t.device);
+        cudaFree(t.dev);
+    }
+    g_tables.clear();
+    cudaSetDevice(cur);
+    return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,188 @@
+/*
+ * packedadam.h -- C ABI of libpackedadam.so: the AdamW parameter update with
+ * packed, quantized persistent moment state, as hand-written CUDA kernels for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * Sources (page title, section):
+ *   "Packed AdamW Reference" README v1.0.0, "The canonical format": one uint32
+ *     state word per FP32 parameter; low 16 bits a signed finite E4M11 first
+ *     moment m, high 16 bits an unsigned finite E4M12 uncorrected RMS
+ *     r = sqrt(v); no shadow moments, block scales or stochastic rounding.
+ *     The paragraph after it: gradients, bias correction, weight decay and the
+ *     update are FP32; the new moments are used in FP32 and packed afterwards.
+ *     Same page: FP32 AdamW and packed FP16-first/FP16-RMS comparison modes.
+ *   "Packed AdamW / Reference / v1.0.0" code page, "Release scope" (decode,
+ *     square the RMS, update in FP32, store afterwards; no conversion at the
+ *     finite bound) and "Execution contract" (contiguous FP32 tensors on one
+ *     device, a dense gradient every update, one global step).
+ *   "TurboAdam" README, "The AdamW update remains AdamW": the recurrences.
+ *   KBench "quantized-optimizer-state" reference.py, quantized_adamw_step and
+ *     _requantise: the FP32 operation order and the 8-bit blockwise mode.
+ *
+ * Numerics (every entry point).  The host forms, in double and rounding once
+ * to float: beta1, beta2, 1-beta1, 1-beta2, 1-beta2^step, lr/(1-beta1^step),
+ * 1-lr*wd and eps.  Each element then computes, one IEEE binary32 rounding per
+ * operation and no fused multiply-add:
+ *     m' = beta1*m + (1-beta1)*g
+ *     v' = beta2*v + ((1-beta2)*g)*g
+ *     p' = p*(1-lr*wd) - ((lr/bc1)*m') / (sqrt(v'/bc2) + eps)
+ * E4 lanes: IEEE-style layout without Inf/NaN codes, exponent bias 15 (E4M11
+ * largest 2-2^-11, E4M12 largest 2-2^-12), subnormals kept, round to nearest
+ * even, saturation at the largest finite value, NaN -> +0, the sign of zero
+ * kept on the m lane, negative values -> 0 on the RMS lane.  FP16 lanes: IEEE
+ * binary16, round to nearest even, saturation at +-65504, NaN -> +0.
+ *
+ * Conventions for every call:
+ *   - Pointers are DEVICE pointers of the current CUDA device unless stated;
+ *     the caller owns all memory and the stream.  Element counts are int64.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and return after the launch.  Argument errors are found
+ *     on the host before anything is launched.
+ *   - `nonfinite` (nullable, device, 8-byte aligned): the number of elements
+ *     whose new p, m or v is NaN or +-Inf is ADDED to *nonfinite.  Nothing is
+ *     repaired: a NaN moment is stored as +0, an infinite one saturates.
+ *   - n == 0 is a no-op returning PA_OK.  Buffers of one call must not overlap
+ *     except where a parameter is updated in place.
+ *   - Return value: PA_OK or an error code; pa_last_error() gives a one-line
+ *     description of the most recent error on the calling thread.
+ */
+#ifndef PACKEDADAM_H
+#define PACKEDADAM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t pa_status;
+#define PA_OK 0
+#define PA_ERR_NULL 1  /* a required pointer is NULL while n > 0              */
+#define PA_ERR_ARG 2   /* step < 1, beta outside [0,1), eps < 0, a non-finite
+                          hyperparameter, n < 0, ntensors < 0, bad mode       */
+#define PA_ERR_ALIGN 3 /* a pointer below its element alignment (see call)   */
+#define PA_ERR_CUDA 4  /* a CUDA runtime call or launch failed                */
+#define PA_ERR_NOMEM 5 /* the library could not allocate its descriptor table */
+
+typedef void *pa_stream; /* cudaStream_t */
+
+/* Library version, major*10000 + minor*100 + patch. */
+int32_t pa_version(void);
+
+/* Static name of a status code ("PA_OK", "PA_ERR_ARG", ...). */
+const char *pa_status_string(pa_status status);
+
+/* One-line description of the last error returned on this thread ("" if none). */
+const char *pa_last_error(void);
+
+/* ---------------------------------------------------------------------------
+ * Packed-state codecs ("Packed AdamW Reference" README, "The canonical
+ * format"; the README's inspect-formats command).
+ *   pa_encode_state:  word[i] = E4M12(rms[i]) << 16 | E4M11(m[i])
+ *   pa_decode_state:  m[i] = E4M11 value of the low 16 bits,
+ *                     rms[i] = E4M12 value of the high 16 bits (exact)
+ *   *_fp16 variants: the same with IEEE binary16 lanes (FP16-first/FP16-RMS).
+ * Layout: m, rms float[n]; word uint32[n]; 4-byte aligned.  For encode,
+ * `nonfinite` (nullable) counts elements with a non-finite m or rms.
+ * ------------------------------------------------------------------------- */
+pa_status pa_encode_state(const float *m, const float *rms, uint32_t *word, int64_t n,
+                          unsigned long long *nonfinite, pa_stream stream);
+pa_status pa_decode_state(const uint32_t *word, float *m, float *rms, int64_t n,
+                          pa_stream stream);
+pa_status pa_encode_state_fp16(const float *m, const float *rms, uint32_t *word, int64_t n,
+                               unsigned long long *nonfinite, pa_stream stream);
+pa_status pa_decode_state_fp16(const uint32_t *word, float *m, float *rms, int64_t n,
+                               pa_stream stream);
+
+/* ---------------------------------------------------------------------------
+ * Single-tensor AdamW steps.  p (float[n]) and the state are updated in place;
+ * g (float[n]) is read.  step is the 1-based global step.  All arrays 4-byte
+ * aligned; when p, g and the state share their address modulo 16 the kernel
+ * uses 16-byte accesses after peeling up to 3 leading elements, otherwise
+ * 4-byte accesses.
+ *
+ * pa_adamw_step_packed_e4 -- the packed E4 step ("Packed AdamW / Reference /
+ *   v1.0.0", "Release scope"): decode m and r from state[i], v = r*r, the FP32
+ *   update, then state[i] = E4M12(sqrt(v')) << 16 | E4M11(m').
+ * pa_adamw_step_packed_fp16 -- the same with binary16 lanes.
+ * pa_adamw_step_fp32 -- ordinary AdamW with FP32 m and v (float[n] each).
+ * ------------------------------------------------------------------------- */
+pa_status pa_adamw_step_packed_e4(float *p, const float *g, uint32_t *state, int64_t n,
+                                  int64_t step, double lr, double beta1, double beta2,
+                                  double eps, double wd, unsigned long long *nonfinite,
+                                  pa_stream stream);
+pa_status pa_adamw_step_packed_fp16(float *p, const float *g, uint32_t *state, int64_t n,
+                                    int64_t step, double lr, double beta1, double beta2,
+                                    double eps, double wd, unsigned long long *nonfinite,
+                                    pa_stream stream);
+pa_status pa_adamw_step_fp32(float *p, const float *g, float *m, float *v, int64_t n,
+                             int64_t step, double lr, double beta1, double beta2, double eps,
+                             double wd, unsigned long long *nonfinite, pa_stream stream);
+
+/* ---------------------------------------------------------------------------
+ * 8-bit blockwise AdamW (KBench "quantized-optimizer-state" reference.py,
+ * quantized_adamw_step and _requantise).  Blocks of 2048 consecutive
+ * elements; nb = ceil(n / 2048) (the last block may be short and its absmax
+ * covers its own elements only).
+ *   m = qmap1[m_code[i]] * m_absmax[b],  v = qmap2[v_code[i]] * v_absmax[b]
+ *   FP32 update as above; p_bf16[i] = bfloat16 round-to-nearest-even of p'.
+ *   New m_absmax[b] = max |m'| over the block (NaN propagates), and
+ *   m_code[i] = number of the 255 binary32 midpoints (qmap1[j]+qmap1[j+1])*0.5
+ *   strictly below m' / max(absmax, 1e-30); likewise for v with qmap2.
+ * p and g are read only (float[n], 16-byte aligned); p_bf16 uint16[n] (8-byte
+ * aligned) receives the new parameters; m_code, v_code uint8[n] (4-byte
+ * aligned) and m_absmax, v_absmax float[nb] are replaced in place; qmap1 and
+ * qmap2 are ascending float[256] in device memory.
+ * ------------------------------------------------------------------------- */
+pa_status pa_adamw_step_blockwise8(const float *p, const float *g, uint16_t *p_bf16,
+                                   uint8_t *m_code, float *m_absmax, uint8_t *v_code,
+                                   float *v_absmax, const float *qmap1, const float *qmap2,
+                                   int64_t n, int64_t step, double lr, double beta1,
+                                   double beta2, double eps, double wd,
+                                   unsigned long long *nonfinite, pa_stream stream);
+
+/* ---------------------------------------------------------------------------
+ * Multi-tensor steps: one persistent grid-stride launch over every tensor of
+ * a list ("Packed AdamW / Reference / v1.0.0", "Execution contract", lists one
+ * launch per tensor; this library replaces that with one launch per list).
+ * The result equals the single-tensor call on each tensor.
+ *
+ * list[t] describes tensor t (host memory, read during the call only):
+ *   p      float[n], updated in place
+ *   g      float[n]
+ *   state  uint32[n] (packed modes) or float m[n] (FP32 mode)
+ *   state2 NULL (packed modes) or float v[n] (FP32 mode)
+ * The library keeps a device copy of each distinct list it is given (its
+ * descriptor table, allocated with cudaMalloc on first use of that list on
+ * the current device and reused while the list is unchanged; at most 64 lists
+ * are kept, the oldest is freed first).  pa_release_tables() frees them all;
+ * it synchronises the device.
+ * ------------------------------------------------------------------------- */
+typedef struct pa_tensor {
+    float *p;
+    const float *g;
+    void *state;
+    void *state2;
+    int64_t n;
+} pa_tensor;
+
+pa_status pa_adamw_step_packed_e4_multi(const pa_tensor *list, int32_t ntensors, int64_t step,
+                                        double lr, double beta1, double beta2, double eps,
+                                        double wd, unsigned long long *nonfinite,
+                                        pa_stream stream);
+pa_status pa_adamw_step_packed_fp16_multi(const pa_tensor *list, int32_t ntensors,
+                                          int64_t step, double lr, double beta1, double beta2,
+                                          double eps, double wd, unsigned long long *nonfinite,
+                                          pa_stream stream);
+pa_status pa_adamw_step_fp32_multi(const pa_tensor *list, int32_t ntensors, int64_t step,
+                                   double lr, double beta1, double beta2, double eps,
+                                   double wd, unsigned long long *nonfinite, pa_stream stream);
+
+/* Frees every cached descriptor table on every device (synchronises them). */
+pa_status pa_release_tables(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PACKEDADAM_H */
