@@ -78,10 +78,12 @@ def load_library(path: str) -> ctypes.CDLL:
     return lib
 
 
-if not os.path.exists(library_path()):
-    raise ImportError(f"{library_path()} is missing: build it with "
+# PA_LIBRARY_VARIANT=fast selects the contracted-arithmetic build of the same source
+_PATH = library_path(fast=os.environ.get("PA_LIBRARY_VARIANT", "") == "fast")
+if not os.path.exists(_PATH):
+    raise ImportError(f"{_PATH} is missing: build it with "
                       "`python adamw_update_gb300/build.py` (needs nvcc)")
-_lib = load_library(library_path())
+_lib = load_library(_PATH)
 
 
 def _check(status: int):

@@ -1,0 +1,623 @@
+"""Benchmark of the packed-E4 AdamW step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--mode e4|fp16|fp32] [--impl ours|reference] [--no-e2e]
+
+One step is one pass of the whole hot path over one batch of synthetic input:
+the multi-tensor packed step (one persistent launch over the workload's
+tensor list) with inputs resident in HBM.  The default workload is flat-7e9:
+one FP32 tensor of 7e9 parameters (28 GB each for p, g and the state words;
+g = 1e-3 * t(df=3) with a 1e-4 fraction scaled by 1e4), 3 warm-up and 20
+timed steps.  Every step moves 140 GB, far more than the 129 MB L2, so no
+flush is needed; workloads whose bytes per step are under 4x the L2 get an
+L2 flush (a 512 MB write) between timed steps, outside the timed launch.
+
+Printed (rank 0, one JSON line): params/s of the whole job (the units every
+rank processed / the slowest rank's time), the roofline of the step kernel
+against the measured HBM copy bandwidth, the CPU oracle on a bounded sample
+of the same workload (cpu_baseline), the end-to-end rate through the public
+API with host buffers (host-to-device copies of p, g and the state, the step,
+device-to-host copies of p and the state, all inside the timed region), and
+the SM clocks sampled during the timed region.
+
+N > 1 (torchrun): each rank steps its own shard of the same size on its own
+GPU (elements are independent, so no collective is on the data path); a
+barrier and a max-reduction of the timings are the only communication.
+
+--impl reference times the CPU oracle, as it stands, on this machine's cores on a
+bounded sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+BYTES_PER_PARAM = {"e4": 20, "fp16": 20, "fp32": 28, "blockwise": 14 + 16 / 2048}
+KERNEL_NAME = {"e4": "adamw_step_kernel<0,true>", "fp16": "adamw_step_kernel<1,true>",
+               "fp32": "adamw_step_kernel<2,true>", "blockwise": "blockwise8_kernel"}
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="flat-7e9", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--mode", default="e4", choices=["e4", "fp16", "fp32"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer measurement")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target CPU time of the oracle sample")
+    ap.add_argument("--fast", action="store_true", help="use libpackedadam_fast.so")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_per_param(mode):
+    """DRAM bytes per parameter of the step kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    src = os.path.join(ROOT, "adamw_update_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in ("packedadam.cu", "codecs.cuh"):
+        with open(os.path.join(src, name), "rb") as f:
+            h.update(f.read())
+    entry = d.get(mode)
+    if not entry or entry.get("source_sha256") != h.hexdigest():
+        return None
+    return float(entry["dram_bytes_per_param"])
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) while the timed region runs."""
+
+    QUERY = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id: str | None):
+        self.bus_id = (bus_id or "").lower()
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        threading.Thread(target=self._read, daemon=True).start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        mhz, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            bus = f[1].lower()
+            if self.bus_id and not (bus.endswith(self.bus_id[-12:]) or self.bus_id.endswith(bus[-12:])):
+                continue
+            try:
+                mhz.append(float(f[2]))
+                mx.append(float(f[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(mhz), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# Workload construction (device buffers, seeded; outside every timed region)
+# ---------------------------------------------------------------------------
+
+def tensor_sizes(name):
+    if name == "gpt-52":
+        return [n for _, n in wl.GPT52_SHAPES]
+    if name == "gpt2-148":
+        return [n for _, n in wl.GPT2_148_SHAPES]
+    return [wl.WORKLOADS[name]["n"]]
+
+
+def fill_gradient_(name, g, sizes, seed):
+    if name == "flat-7e9":
+        wl.fill_student_t_saturating_(g, seed)
+    elif name == "gpt2-148":
+        wl.fill_gpt2_grads_(g, sizes, seed)
+    else:
+        wl.fill_normal_(g, 1e-3, seed, stream=1)
+
+
+class Workload:
+    """Flat device buffers for a workload; tensors are contiguous slices."""
+
+    def __init__(self, name, mode, device, seed):
+        import torch
+
+        self.name, self.mode = name, mode
+        self.sizes = tensor_sizes(name)
+        self.n = sum(self.sizes)
+        n = self.n
+        f32 = torch.float32
+        if name == "blockwise-1e9":
+            self.mode = mode = "blockwise"
+            q1, q2 = wl.dynamic_qmap_signed(), wl.dynamic_qmap_unsigned()
+            nb = wl.blocks(n)
+            self.p = wl.fill_normal_(torch.empty(n, dtype=f32, device=device), 0.02, seed)
+            self.g = torch.empty(n, dtype=f32, device=device)
+            wl.fill_normal_(self.g, 1e-3, seed, stream=1)
+            self.p_bf16 = torch.empty(n, dtype=torch.bfloat16, device=device)
+            self.m_code = torch.full((n,), wl.nearest_zero_code(q1), dtype=torch.uint8, device=device)
+            self.v_code = torch.full((n,), wl.nearest_zero_code(q2), dtype=torch.uint8, device=device)
+            self.m_absmax = torch.zeros(nb, dtype=f32, device=device)
+            self.v_absmax = torch.zeros(nb, dtype=f32, device=device)
+            self.q1 = torch.from_numpy(q1).to(device)
+            self.q2 = torch.from_numpy(q2).to(device)
+            return
+        self.p = wl.fill_normal_(torch.empty(n, dtype=f32, device=device), 0.02, seed)
+        self.g = torch.empty(n, dtype=f32, device=device)
+        fill_gradient_(name, self.g, self.sizes, seed)
+        if mode == "fp32":
+            self.s = [torch.zeros(n, dtype=f32, device=device), torch.zeros(n, dtype=f32, device=device)]
+        else:
+            self.s = [torch.zeros(n, dtype=torch.int32, device=device)]
+        self.fresh_g = None
+        if name == "single-4096":  # the workload draws g afresh every step
+            self.fresh_g = []
+
+    def bytes_per_step(self):
+        return BYTES_PER_PARAM[self.mode] * self.n
+
+    def tensor_array(self, pa, g=None):
+        g = self.g if g is None else g
+        offs = np.cumsum([0] + self.sizes)
+        ents = []
+        for a, b in zip(offs[:-1], offs[1:]):
+            ents.append((self.p[a:b], g[a:b], *[s[a:b] for s in self.s]))
+        return pa.tensor_list(ents, fp32=self.mode == "fp32")
+
+
+def step_fn(pa, w, hy, nonfinite):
+    """A closure running one step on torch's current stream."""
+    import torch
+
+    if w.mode == "blockwise":
+        def run(t):
+            pa.pa_adamw_step_blockwise8(w.p, w.g, w.p_bf16, w.m_code, w.m_absmax, w.v_code,
+                                        w.v_absmax, w.q1, w.q2, t, nonfinite=nonfinite, **hy)
+        return run
+    fn = {"e4": pa.pa_adamw_step_packed_e4_multi, "fp16": pa.pa_adamw_step_packed_fp16_multi,
+          "fp32": pa.pa_adamw_step_fp32_multi}[w.mode]
+    arrays = [w.tensor_array(pa)]
+    if w.fresh_g is not None:
+        arrays = []
+        for k in range(64):
+            gk = torch.empty_like(w.g)
+            wl.fill_normal_(gk, 1e-3, seed=1000 + k, stream=1)
+            w.fresh_g.append(gk)
+            arrays.append(w.tensor_array(pa, gk))
+
+    def run(t):
+        fn(arrays[t % len(arrays)], t, nonfinite=nonfinite, **hy)
+    return run
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle on a bounded sample of the workload
+# ---------------------------------------------------------------------------
+
+def oracle_sample_rate(arrays, mode, seconds, threads, q=None):
+    """Time the oracle (as it stands, `threads` host threads) on a bounded
+    sample; repeats whole passes until `seconds` have elapsed (at least one).
+    Returns (params/s, elements per pass, passes)."""
+    import oracle
+
+    hy = wl.HYPER
+    n = arrays[0].size
+    passes, t0 = 0, time.perf_counter()
+    st = [a.copy() for a in arrays]
+    while True:
+        passes += 1
+        if mode == "blockwise":
+            p, g, mc, ma, vc, va = st
+            ob, mc, ma, vc, va, _ = oracle.step_blockwise8(p, g, mc, ma, vc, va, q[0], q[1],
+                                                           passes, threads=threads, **hy)
+            st = [p, g, mc, ma, vc, va]
+        elif mode == "fp32":
+            st[0], st[2], st[3], _ = oracle.step_fp32(st[0], st[1], st[2], st[3], passes,
+                                                      threads=threads, **hy)
+        else:
+            st[0], st[2], _ = oracle.step_packed(st[0], st[1], st[2], passes, mode=mode,
+                                                 threads=threads, **hy)
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            return n * passes / el, n, passes
+
+
+def sample_size(mode, seconds, threads, total):
+    """Elements for about `seconds` of oracle work on `threads` threads,
+    calibrated on a 2^20-element run, capped at 2^27 and at the workload."""
+    import oracle
+
+    k = 1 << 20
+    rng = np.random.default_rng(0)
+    p = rng.normal(0, 0.02, k).astype(np.float32)
+    g = rng.normal(0, 1e-3, k).astype(np.float32)
+    t0 = time.perf_counter()
+    if mode == "fp32":
+        z = np.zeros(k, np.float32)
+        oracle.step_fp32(p, g, z, z, 1, threads=threads)
+    elif mode == "blockwise":
+        z8 = np.zeros(k, np.uint8)
+        za = np.zeros(k // 2048, np.float32)
+        q = wl.dynamic_qmap_signed()
+        oracle.step_blockwise8(p, g, z8, za, z8, za, q, q, 1, threads=threads)
+    else:
+        oracle.step_packed(p, g, np.zeros(k, np.uint32), 1, mode=mode, threads=threads)
+    rate = k / max(time.perf_counter() - t0, 1e-6)
+    s = int(min(total, 1 << 27, max(1 << 20, rate * seconds)))
+    return (s // 2048) * 2048 if s >= 2048 else s
+
+
+def sample_gradient(name, s, seed):
+    """Host FP32 gradient sample of s elements with the workload's distribution."""
+    import torch
+
+    g = torch.empty(s, dtype=torch.float32)
+    if name == "gpt2-148":
+        sizes, left = [], s
+        for n in tensor_sizes(name):
+            if left == 0:
+                break
+            sizes.append(min(n, left))
+            left -= sizes[-1]
+        return wl.fill_gpt2_grads_(g, sizes, seed)
+    fill_gradient_(name, g, [s], seed)
+    return g
+
+
+def host_sample(w, s):
+    """First s elements of the workload's inputs, as host numpy arrays."""
+    if w.mode == "blockwise":
+        nb = wl.blocks(s)
+        arrays = [w.p[:s].cpu().numpy(), w.g[:s].cpu().numpy(), w.m_code[:s].cpu().numpy(),
+                  w.m_absmax[:nb].cpu().numpy(), w.v_code[:s].cpu().numpy(),
+                  w.v_absmax[:nb].cpu().numpy()]
+        return arrays, (w.q1.cpu().numpy(), w.q2.cpu().numpy())
+    arrays = [w.p[:s].cpu().numpy(), w.g[:s].cpu().numpy()]
+    for st in w.s:
+        a = st[:s].cpu().numpy()
+        arrays.append(a.view(np.uint32) if a.dtype == np.int32 else a)
+    return arrays, None
+
+
+def host_available_bytes():
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        return None
+    return None
+
+
+def cpu_baseline(w, seconds):
+    cores = host_cores()
+    s = sample_size(w.mode, seconds / 4, cores, w.n)
+    arrays, q = host_sample(w, s)
+    rate, n, passes = oracle_sample_rate(arrays, w.mode, seconds, cores, q)
+    return {"value": rate, "unit": "params/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {n} parameters of the {w.name} workload, {passes} oracle "
+                      f"steps in {cores} host threads"}
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if args.fast:
+        os.environ["PA_LIBRARY_VARIANT"] = "fast"
+    import adamw_update_gb300 as lib
+    w = Workload(args.workload, args.mode, device, seed=1234 + rank)
+    hy = wl.HYPER
+    nonfinite = torch.zeros(1, dtype=torch.int64, device=device)
+    run = step_fn(lib, w, hy, nonfinite)
+    stream = torch.cuda.current_stream()
+    flush = None
+    if w.bytes_per_step() < 4 * L2_BYTES:
+        flush = torch.empty(512 * 2 ** 20 // 4, dtype=torch.float32, device=device)
+
+    for t in range(1, args.warmup + 1):
+        run(t)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    props = torch.cuda.get_device_properties(device)
+    sampler = ClockSampler(getattr(props, "pci_bus_id", None) and
+                           f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0")
+    sampler.start()
+    time.sleep(0.5)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    first = torch.cuda.Event(enable_timing=True)
+    last = torch.cuda.Event(enable_timing=True)
+    first.record(stream)
+    for k in range(args.steps):
+        if flush is not None:
+            flush.fill_(float(k))
+        starts[k].record(stream)
+        run(args.warmup + 1 + k)
+        ends[k].record(stream)
+    last.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    region_ms = first.elapsed_time(last)
+    step_ms = statistics.mean(launch_ms) if flush is not None else region_ms / args.steps
+    kernel_ms = statistics.mean(launch_ms)
+    t = torch.tensor([step_ms, kernel_ms], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    step_ms, kernel_ms = float(t[0]), float(t[1])
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = measure_e2e(lib, w, hy, args, stream, nonfinite)
+        if world > 1:
+            et = torch.tensor([e2e["_ms"]], dtype=torch.float64, device=device)
+            dist.all_reduce(et, op=dist.ReduceOp.MAX)
+            e2e["_ms"] = float(et[0])
+        e2e["value"] = w.n * world / (e2e.pop("_ms") / 1e3)
+
+    cpu = None
+    if rank == 0 and world == 1:
+        cpu = cpu_baseline(w, args.cpu_seconds)
+
+    if rank == 0:
+        peak, peak_kind = measured_peak()
+        bpp = BYTES_PER_PARAM[w.mode]
+        achieved = bpp * w.n / (kernel_ms / 1e3) / 1e9
+        traffic = traffic_per_param(w.mode)
+        line = {
+            "metric": "packed-E4 AdamW step: params/s and HBM GB/s as % of GB300 peak, 1 GPU"
+                      if w.mode == "e4" else f"{w.mode} AdamW step: params/s and HBM GB/s",
+            "value": w.n * world / (step_ms / 1e3),
+            "unit": "params/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": step_ms,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f32",
+            "data": "synthetic",
+            "config": {
+                "workload": w.name, "mode": w.mode, "params_per_gpu": w.n,
+                "tensors": len(w.sizes), "bytes_per_param": bpp,
+                "l2": "flushed between steps (512 MB write)" if flush is not None
+                      else f"inputs larger than L2 ({w.bytes_per_step() / 1e9:.1f} GB per step)",
+                "parallelism": f"{world} independent shards, no data-path collective",
+                "library": "libpackedadam_fast.so" if args.fast else "libpackedadam.so",
+            },
+            "roofline": {
+                "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "peak_source": peak_kind,
+                "traffic": None if traffic is None else traffic * w.n,
+                "kernel": KERNEL_NAME[w.mode], "kernel_ms": kernel_ms,
+            },
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "nonfinite": int(nonfinite.item()),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def measure_e2e(pa, w, hy, args, stream, nonfinite):
+    """The step through the public API with the workload in pinned host
+    memory: per step, copy p, g and the state host->device, run the step,
+    copy p and the state device->host; all inside the timed region."""
+    import torch
+
+    if w.mode == "blockwise":
+        dev_in = [w.p, w.g, w.m_code, w.m_absmax, w.v_code, w.v_absmax]
+        dev_out = [w.p_bf16, w.m_code, w.m_absmax, w.v_code, w.v_absmax]
+    else:
+        dev_in = [w.p, w.g, *w.s]
+        dev_out = [w.p, *w.s]
+    need = sum(t.numel() * t.element_size() for t in set(dev_in + dev_out))
+    avail = host_available_bytes()
+    if avail is not None and need > 0.6 * avail:
+        return {"_ms": float("nan"), "unit": "params/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0,
+                "skipped": f"pinned host buffers of {need / 1e9:.0f} GB exceed 60% of the "
+                           f"{avail / 1e9:.0f} GB available"}
+    host = {id(t): torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in dev_in + dev_out}
+    for t in dev_in + dev_out:
+        host[id(t)].copy_(t)
+    run = step_fn(pa, w, hy, nonfinite)
+    h2d = sum(t.numel() * t.element_size() for t in dev_in)
+    d2h = sum(t.numel() * t.element_size() for t in dev_out)
+
+    def one(t):
+        for d in dev_in:
+            d.copy_(host[id(d)], non_blocking=True)
+        run(t)
+        for d in dev_out:
+            host[id(d)].copy_(d, non_blocking=True)
+
+    one(10_000)
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for k in range(args.e2e_steps):
+        one(10_001 + k)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.e2e_steps
+    del host
+    return {"_ms": ms, "unit": "params/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": args.e2e_steps, "api": "pa_adamw_step_*_multi with pinned-host copies"}
+
+
+# ---------------------------------------------------------------------------
+# Reference arm: the CPU oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import torch
+
+    mode = "blockwise" if args.workload == "blockwise-1e9" else args.mode
+    cores = host_cores()
+    total = wl.WORKLOADS[args.workload]["n"]
+    budget = 150.0  # seconds for the whole run
+    per_step = min(10.0, budget / max(1, args.steps + args.warmup))
+    s = sample_size(mode, per_step, cores, total)
+    p = wl.fill_normal_(torch.empty(s, dtype=torch.float32), 0.02, 1234)
+    g = sample_gradient(args.workload, s, 1234)
+    p, g = p.numpy(), g.numpy()
+    import oracle
+
+    hy = wl.HYPER
+    if mode == "blockwise":
+        q1, q2 = wl.dynamic_qmap_signed(), wl.dynamic_qmap_unsigned()
+        nb = wl.blocks(s)
+        st = [np.full(s, wl.nearest_zero_code(q1), np.uint8), np.zeros(nb, np.float32),
+              np.full(s, wl.nearest_zero_code(q2), np.uint8), np.zeros(nb, np.float32)]
+    elif mode == "fp32":
+        st = [np.zeros(s, np.float32), np.zeros(s, np.float32)]
+    else:
+        st = [np.zeros(s, np.uint32)]
+
+    def one(t):
+        nonlocal p, st
+        if mode == "blockwise":
+            _, mc, ma, vc, va, _ = oracle.step_blockwise8(p, g, st[0], st[1], st[2], st[3], q1, q2,
+                                                          t, threads=cores, **hy)
+            st = [mc, ma, vc, va]
+        elif mode == "fp32":
+            p, st[0], st[1], _ = oracle.step_fp32(p, g, st[0], st[1], t, threads=cores, **hy)
+        else:
+            p, st[0], _ = oracle.step_packed(p, g, st[0], t, mode=mode, threads=cores, **hy)
+
+    for t in range(1, args.warmup + 1):
+        one(t)
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        one(args.warmup + 1 + k)
+    el = time.perf_counter() - t0
+    value = s * args.steps / el
+    sample = (f"first {s} parameters of the {args.workload} workload per step "
+              f"(of {total}), {cores} host threads")
+    line = {
+        "impl": "reference",
+        "metric": "packed-E4 AdamW step: params/s and HBM GB/s as % of GB300 peak, 1 GPU"
+                  if mode == "e4" else f"{mode} AdamW step: params/s and HBM GB/s",
+        "value": value, "unit": "params/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "mode": mode, "params_per_step": s,
+                   "parallelism": "host threads"},
+        "cpu_baseline": {"value": value, "unit": "params/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()
