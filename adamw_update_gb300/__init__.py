@@ -26,6 +26,7 @@ __all__ = [
     "pa_adamw_step_packed_e4", "pa_adamw_step_packed_fp16", "pa_adamw_step_fp32",
     "pa_adamw_step_blockwise8", "pa_adamw_step_packed_e4_multi",
     "pa_adamw_step_packed_fp16_multi", "pa_adamw_step_fp32_multi", "pa_release_tables",
+    "shard_bounds",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -248,3 +249,23 @@ def pa_adamw_step_fp32_multi(entries, step, lr=1e-3, beta1=0.9, beta2=0.999, eps
 
 def pa_release_tables():
     _check(_lib.pa_release_tables())
+
+
+# ---- sharding of a flattened parameter space ------------------------------------
+
+def shard_bounds(n: int, world: int, rank: int, align: int = 4):
+    """[lo, hi) of rank's contiguous shard of n elements split over world ranks.
+
+    Shards start on multiples of `align` (4 elements keeps every shard's
+    16-byte phase equal to the whole buffer's; use 2048 for the blockwise mode
+    so no quantisation block is split).  Elements are independent, so stepping
+    each shard on its own rank gives the same bits as stepping the whole; the
+    step itself needs no collective (gradients arrive by reduce-scatter and
+    parameters leave by all-gather, outside this library).
+    """
+    if world < 1 or not 0 <= rank < world or align < 1 or n < 0:
+        raise ValueError("bad shard request")
+    units = -(-n // align)
+    per = -(-units // world) * align
+    lo = min(n, rank * per)
+    return lo, min(n, lo + per)

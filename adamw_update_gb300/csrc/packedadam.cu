@@ -11,7 +11,7 @@
 // Design.  The step is elementwise and bound by HBM bandwidth (20 bytes per
 // parameter for the packed modes), so the kernels are built for bytes in
 // flight: a persistent grid (resident CTAs per SM x SM count) strides over
-// 4096-element chunks; every thread issues all of its 16-byte loads of p, g
+// 2048-element chunks; every thread issues all of its 16-byte loads of p, g
 // and the state for a chunk before any arithmetic, then stores with streaming
 // hints.  A multi-tensor list becomes one launch over a device-side
 // descriptor table, whose chunk prefix sums let each CTA walk from tensor to
@@ -33,9 +33,17 @@ namespace pa {
 
 constexpr int kThreads = 256;         // threads per CTA
 #ifndef PA_UNROLL
-#define PA_UNROLL 4
+#define PA_UNROLL 2
+#endif
+#ifndef PA_MIN_BLOCKS
+#define PA_MIN_BLOCKS 4
 #endif
 constexpr int kUnroll = PA_UNROLL;    // 16-byte vectors per thread per chunk
+// Resident CTAs per SM the step kernels are compiled for (caps registers at
+// 65536 / (256 * 4) = 64): measured on GB300, 4 x 256 threads with two
+// 16-byte vectors of each stream per thread beat 3 CTAs with four vectors by
+// 19 %, the larger body also missing in the instruction cache.
+constexpr int kMinBlocks = PA_MIN_BLOCKS;
 constexpr int64_t kChunk = (int64_t)kThreads * kUnroll * 4;  // elements per chunk
 
 enum Mode : int { kE4 = 0, kFP16 = 1, kF32 = 2 };
@@ -64,21 +72,23 @@ __device__ __forceinline__ void store_stream(uint32_t *a, uint4 x) { __stcs(rein
 // ---- one element of a packed step -------------------------------------------
 // Decode the prior state, v = r*r, FP32 update, encode m' and sqrt(v') into the
 // next word ("Release scope": the state is stored only after the update).
-template <int MODE>
+template <int MODE, bool UNIT_BC2>
 __device__ __forceinline__ uint32_t packed_element(float &p, float g, uint32_t w,
                                                    const Scalars &s, uint32_t &bad)
 {
     const float m = MODE == kE4 ? decode_m_lane(w) : decode_fp16_low(w);
     const float r = MODE == kE4 ? decode_rms_lane(w) : decode_fp16_high(w);
-    const Moments o = adamw_element(p, g, m, __fmul_rn(r, r), s);
+    float rn = 0.0f;
+    const Moments o = adamw_element<UNIT_BC2>(p, g, m, __fmul_rn(r, r), s, &rn);
     bad += any_nonfinite(o);
     p = o.p;
-    const float rn = __fsqrt_rn(o.v);
+    if (!UNIT_BC2)
+        rn = __fsqrt_rn(o.v);  // with bc2 == 1 the update already took sqrt(v')
     return MODE == kE4 ? encode_word_e4(o.m, rn) : encode_word_fp16(o.m, rn);
 }
 
 // Element i of tensor d with 4-byte accesses (heads, tails, unaligned tensors).
-template <int MODE>
+template <int MODE, bool U1>
 __device__ __forceinline__ void scalar_element(const Desc &d, int64_t i, const Scalars &s,
                                                uint32_t &bad)
 {
@@ -87,14 +97,14 @@ __device__ __forceinline__ void scalar_element(const Desc &d, int64_t i, const S
     if constexpr (MODE == kF32) {
         float *m = static_cast<float *>(d.s1);
         float *v = static_cast<float *>(d.s2);
-        const Moments o = adamw_element(p, g, m[i], v[i], s);
+        const Moments o = adamw_element<U1>(p, g, m[i], v[i], s);
         bad += any_nonfinite(o);
         d.p[i] = o.p;
         m[i] = o.m;
         v[i] = o.v;
     } else {
         uint32_t *w = static_cast<uint32_t *>(d.s1);
-        const uint32_t nw = packed_element<MODE>(p, g, w[i], s, bad);
+        const uint32_t nw = packed_element<MODE, U1>(p, g, w[i], s, bad);
         d.p[i] = p;
         w[i] = nw;
     }
@@ -102,7 +112,7 @@ __device__ __forceinline__ void scalar_element(const Desc &d, int64_t i, const S
 
 // Chunk k of a 16-byte-path tensor: body elements [k*kChunk, (k+1)*kChunk)
 // counted from d.head.  All loads of the chunk are issued before any compute.
-template <int MODE>
+template <int MODE, bool U1>
 __device__ __forceinline__ void vector_chunk(const Desc &d, int64_t k, const Scalars &s,
                                              uint32_t &bad)
 {
@@ -110,9 +120,10 @@ __device__ __forceinline__ void vector_chunk(const Desc &d, int64_t k, const Sca
     const int64_t nb = d.n - d.head;
     const int64_t base = k * kChunk;
     if (k == 0 && tid < d.head)
-        scalar_element<MODE>(d, tid, s, bad);
+        scalar_element<MODE, U1>(d, tid, s, bad);
     float *P = d.p + d.head;
     const float *G = d.g + d.head;
+    const bool whole = base + kChunk <= nb;  // uniform: no per-vector bound checks
 
     float4 pv[kUnroll], gv[kUnroll];
     uint4 wv[kUnroll];
@@ -121,7 +132,7 @@ __device__ __forceinline__ void vector_chunk(const Desc &d, int64_t k, const Sca
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
         const int64_t e = base + 4 * ((int64_t)u * kThreads + tid);
-        full[u] = e + 4 <= nb;
+        full[u] = whole || e + 4 <= nb;
         if (full[u]) {
             pv[u] = load_stream(P + e);
             gv[u] = load_readonly(G + e);
@@ -144,7 +155,7 @@ __device__ __forceinline__ void vector_chunk(const Desc &d, int64_t k, const Sca
                 float vq[4] = {vv[u].x, vv[u].y, vv[u].z, vv[u].w};
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const Moments o = adamw_element(pp[j], gg[j], mm[j], vq[j], s);
+                    const Moments o = adamw_element<U1>(pp[j], gg[j], mm[j], vq[j], s);
                     bad += any_nonfinite(o);
                     pp[j] = o.p;
                     mm[j] = o.m;
@@ -156,20 +167,20 @@ __device__ __forceinline__ void vector_chunk(const Desc &d, int64_t k, const Sca
                 uint32_t ww[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    ww[j] = packed_element<MODE>(pp[j], gg[j], ww[j], s, bad);
+                    ww[j] = packed_element<MODE, U1>(pp[j], gg[j], ww[j], s, bad);
                 store_stream(static_cast<uint32_t *>(d.s1) + d.head + e, make_uint4(ww[0], ww[1], ww[2], ww[3]));
             }
             store_stream(P + e, make_float4(pp[0], pp[1], pp[2], pp[3]));
         } else if (e < nb) {
             // the one vector that straddles the end of the tensor
             for (int64_t i = e; i < nb; ++i)
-                scalar_element<MODE>(d, d.head + i, s, bad);
+                scalar_element<MODE, U1>(d, d.head + i, s, bad);
         }
     }
 }
 
 // Chunk k of a 4-byte-path tensor: elements [k*kChunk, (k+1)*kChunk).
-template <int MODE>
+template <int MODE, bool U1>
 __device__ __forceinline__ void scalar_chunk(const Desc &d, int64_t k, const Scalars &s,
                                              uint32_t &bad)
 {
@@ -178,7 +189,7 @@ __device__ __forceinline__ void scalar_chunk(const Desc &d, int64_t k, const Sca
     for (int u = 0; u < kUnroll * 4; ++u) {
         const int64_t i = base + (int64_t)u * kThreads + threadIdx.x;
         if (i < d.n)
-            scalar_element<MODE>(d, i, s, bad);
+            scalar_element<MODE, U1>(d, i, s, bad);
     }
 }
 
@@ -193,9 +204,9 @@ __device__ __forceinline__ void flush_nonfinite(uint32_t bad, unsigned long long
 
 // The persistent step kernel.  MULTI: walk the device descriptor table (each
 // CTA visits chunks in increasing order, so the tensor index only moves
-// forward); otherwise the single descriptor passed by value.
-template <int MODE, bool MULTI>
-__global__ void __launch_bounds__(kThreads)
+// forward); otherwise the single descriptor passed by value.  U1: bc2 == 1.
+template <int MODE, bool MULTI, bool U1>
+__global__ void __launch_bounds__(kThreads, kMinBlocks)
 adamw_step_kernel(const Desc *__restrict__ table, int32_t ntensors, int64_t total_chunks,
                   const Desc single, const Scalars s, unsigned long long *nonfinite)
 {
@@ -217,9 +228,9 @@ adamw_step_kernel(const Desc *__restrict__ table, int32_t ntensors, int64_t tota
         }
         const int64_t k = c - d.chunk0;
         if (d.vec)
-            vector_chunk<MODE>(d, k, s, bad);
+            vector_chunk<MODE, U1>(d, k, s, bad);
         else
-            scalar_chunk<MODE>(d, k, s, bad);
+            scalar_chunk<MODE, U1>(d, k, s, bad);
     }
     flush_nonfinite(bad, nonfinite);
 }
@@ -474,12 +485,12 @@ enum KernelSlot { kSlotE4, kSlotFP16, kSlotF32, kSlotE4Multi, kSlotFP16Multi, kS
 const void *kernel_of(int slot)
 {
     switch (slot) {
-    case kSlotE4: return (const void *)pa::adamw_step_kernel<pa::kE4, false>;
-    case kSlotFP16: return (const void *)pa::adamw_step_kernel<pa::kFP16, false>;
-    case kSlotF32: return (const void *)pa::adamw_step_kernel<pa::kF32, false>;
-    case kSlotE4Multi: return (const void *)pa::adamw_step_kernel<pa::kE4, true>;
-    case kSlotFP16Multi: return (const void *)pa::adamw_step_kernel<pa::kFP16, true>;
-    case kSlotF32Multi: return (const void *)pa::adamw_step_kernel<pa::kF32, true>;
+    case kSlotE4: return (const void *)pa::adamw_step_kernel<pa::kE4, false, false>;
+    case kSlotFP16: return (const void *)pa::adamw_step_kernel<pa::kFP16, false, false>;
+    case kSlotF32: return (const void *)pa::adamw_step_kernel<pa::kF32, false, false>;
+    case kSlotE4Multi: return (const void *)pa::adamw_step_kernel<pa::kE4, true, false>;
+    case kSlotFP16Multi: return (const void *)pa::adamw_step_kernel<pa::kFP16, true, false>;
+    case kSlotF32Multi: return (const void *)pa::adamw_step_kernel<pa::kF32, true, false>;
     case kSlotBlockwise: return (const void *)pa::blockwise8_kernel;
     default: return (const void *)pa::encode_state_kernel<pa::kE4>;
     }
@@ -590,8 +601,12 @@ pa_status step_single(const pa_tensor &t, int64_t step, double lr, double beta1,
     int grid = 0;
     if ((st = grid_for(MODE, chunks, &grid)) != PA_OK)
         return st;
-    pa::adamw_step_kernel<MODE, false><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
-        nullptr, 1, chunks, d, s, nonfinite);
+    if (s.bc2 == 1.0f)
+        pa::adamw_step_kernel<MODE, false, true><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
+            nullptr, 1, chunks, d, s, nonfinite);
+    else
+        pa::adamw_step_kernel<MODE, false, false><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
+            nullptr, 1, chunks, d, s, nonfinite);
     return check_launch("adamw_step_kernel launch");
 }
 
@@ -710,8 +725,12 @@ pa_status step_multi(const pa_tensor *list, int32_t ntensors, int64_t step, doub
         return st;
     Desc none;
     std::memset(&none, 0, sizeof none);
-    pa::adamw_step_kernel<MODE, true><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
-        table, ntensors, chunks, none, s, nonfinite);
+    if (s.bc2 == 1.0f)
+        pa::adamw_step_kernel<MODE, true, true><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
+            table, ntensors, chunks, none, s, nonfinite);
+    else
+        pa::adamw_step_kernel<MODE, true, false><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
+            table, ntensors, chunks, none, s, nonfinite);
     return check_launch("adamw_step_kernel (multi) launch");
 }
 

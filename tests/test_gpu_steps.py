@@ -265,3 +265,36 @@ def test_argument_errors(pa):
     raw = x.data_ptr() + 2  # not 4-byte aligned
     assert pa._lib.pa_adamw_step_packed_e4(raw, raw, raw, 4, 1, 1e-3, .9, .999, 1e-8, 0,
                                            None, None) == 3
+
+
+@pytest.mark.parametrize("mode", ["e4", "fp16", "fp32"])
+def test_late_steps_unit_bias_correction(pa, mode):
+    """Global steps where 1 - beta2^step rounds to 1.0f take the kernel
+    instantiation that skips v'/bc2; the bits must not change."""
+    import torch
+
+    n = 9001
+    rng = np.random.default_rng(21)
+    p = rng.normal(0, 0.02, n).astype(np.float32)
+    gs = [rng.normal(0, 1e-3, n).astype(np.float32) for _ in range(2)]
+    assert oracle.hyperparams(100_000, **HY)[4] == 1.0  # bc2
+    if mode == "fp32":
+        m = rng.normal(0, 1e-4, n).astype(np.float32)
+        v = (rng.normal(0, 1e-3, n) ** 2).astype(np.float32)
+        dp, dm, dv = dev(p), dev(m), dev(v)
+        for k, g in enumerate(gs):
+            pa.pa_adamw_step_fp32_multi([(dp, dev(g), dm, dv)], 100_000 + k, **HY)
+            p, m, v, _ = oracle.step_fp32(p, g, m, v, 100_000 + k, **HY)
+        torch.cuda.synchronize()
+        assert_same_bits(host_f32(dp), p, "p")
+        assert_same_bits(host_f32(dm), m, "m")
+        assert_same_bits(host_f32(dv), v, "v")
+        return
+    st = rng.integers(0, 1 << 32, n, dtype=np.uint64).astype(np.uint32)
+    if mode == "fp16":
+        st = (st & 0x7BFF7BFF).astype(np.uint32)
+    gp, gw, gb = _run_packed(pa, mode, p, gs, st, first_step=100_000)
+    ep, ew, eb = _oracle_packed(mode, p, gs, st, first_step=100_000)
+    assert_same_bits(gp, ep, f"{mode} p")
+    assert_same_bits(gw, ew, f"{mode} state")
+    assert gb == eb
