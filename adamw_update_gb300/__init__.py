@@ -26,7 +26,7 @@ __all__ = [
     "pa_adamw_step_packed_e4", "pa_adamw_step_packed_fp16", "pa_adamw_step_fp32",
     "pa_adamw_step_blockwise8", "pa_adamw_step_packed_e4_multi",
     "pa_adamw_step_packed_fp16_multi", "pa_adamw_step_fp32_multi", "pa_release_tables",
-    "shard_bounds",
+    "shard_bounds", "pa_adamw_step_packed_e4_multi_noalloc",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -269,3 +269,22 @@ def shard_bounds(n: int, world: int, rank: int, align: int = 4):
     per = -(-units // world) * align
     lo = min(n, rank * per)
     return lo, min(n, lo + per)
+
+
+# ---- the multi-tensor packed-E4 step that allocates nothing -------------------
+
+_lib.pa_adamw_step_packed_e4_multi_noalloc.restype = _i32
+_lib.pa_adamw_step_packed_e4_multi_noalloc.argtypes = [
+    ctypes.POINTER(PaTensor), _i32, *_HYP, _vp, _vp]
+
+
+def pa_adamw_step_packed_e4_multi_noalloc(entries, step, lr=1e-3, beta1=0.9, beta2=0.999,
+                                          eps=1e-8, wd=0.0, nonfinite=None, stream=None):
+    """pa_adamw_step_packed_e4_multi without any device allocation by the
+    library, for callers whose device memory is owned by their own allocator
+    or who must not meet cudaMalloc's synchronisation: the descriptor table
+    goes to a fixed device array of 1024 entries.  Calls that overlap on the
+    GPU race on that array; the first call on a device should come before any
+    stream capture."""
+    _multi(_lib.pa_adamw_step_packed_e4_multi_noalloc, entries, False, step, lr, beta1, beta2,
+           eps, wd, nonfinite, stream)

@@ -44,6 +44,9 @@ constexpr int kUnroll = PA_UNROLL;    // 16-byte vectors per thread per chunk
 // 16-byte vectors of each stream per thread beat 3 CTAs with four vectors by
 // 19 %, the larger body also missing in the instruction cache.
 constexpr int kMinBlocks = PA_MIN_BLOCKS;
+#ifndef PA_NOALLOC_MAX_TENSORS
+#define PA_NOALLOC_MAX_TENSORS 1024
+#endif
 constexpr int64_t kChunk = (int64_t)kThreads * kUnroll * 4;  // elements per chunk
 
 enum Mode : int { kE4 = 0, kFP16 = 1, kF32 = 2 };
@@ -923,3 +926,107 @@ pa_status pa_release_tables(void)
 }
 
 }  // extern "C"
+
+// ===========================================================================
+// Multi-tensor packed-E4 step that allocates nothing
+// ===========================================================================
+// pa_adamw_step_packed_e4_multi keeps each list's descriptor table in device
+// memory that the library obtains with cudaMalloc.  Some callers cannot let a
+// library do that: a framework whose caching allocator has reserved the
+// device's memory and expects every allocation to go through it, or a loop
+// that must not meet cudaMalloc's and cudaFree's implicit synchronisation.
+// For them this variant keeps the table in a fixed device array that is part
+// of the library image: every device that loads the library holds the
+// PA_NOALLOC_MAX_TENSORS descriptors (56 bytes each) until the process exits.
+namespace {
+
+constexpr int32_t kNoAllocMaxTensors = PA_NOALLOC_MAX_TENSORS;
+
+}  // namespace
+
+static __device__ __align__(256) pa::Desc g_noalloc_table[PA_NOALLOC_MAX_TENSORS];
+
+namespace {
+
+std::mutex g_noalloc_mu;
+pa::Desc *g_noalloc_ptr[64] = {nullptr};  // device address of the array, per device
+thread_local pa::Desc g_noalloc_host[PA_NOALLOC_MAX_TENSORS];
+
+// The array's name is only a host-side stand-in in host code; its device
+// address is looked up once per device, with that device current.
+pa_status noalloc_table_address(pa::Desc **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64)
+        return fail(PA_ERR_CUDA, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void *ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_noalloc_table);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaGetSymbolAddress of the descriptor array");
+        g_noalloc_ptr[dev] = static_cast<pa::Desc *>(ptr);
+    }
+    *out = g_noalloc_ptr[dev];
+    return PA_OK;
+}
+
+}  // namespace
+
+extern "C" pa_status pa_adamw_step_packed_e4_multi_noalloc(
+    const pa_tensor *list, int32_t ntensors, int64_t step, double lr, double beta1,
+    double beta2, double eps, double wd, unsigned long long *nonfinite, pa_stream stream)
+{
+    Scalars s;
+    pa_status st = make_scalars(step, lr, beta1, beta2, eps, wd, &s);
+    if (st != PA_OK)
+        return st;
+    if (ntensors < 0)
+        return fail(PA_ERR_ARG, "ntensors must be >= 0 (got %d)", ntensors);
+    if (ntensors > kNoAllocMaxTensors)
+        return fail(PA_ERR_ARG,
+                    "ntensors = %d exceeds the %d descriptors of the fixed device array; "
+                    "use pa_adamw_step_packed_e4_multi or split the list",
+                    ntensors, kNoAllocMaxTensors);
+    if (ntensors == 0)
+        return ok();
+    if (!list)
+        return fail(PA_ERR_NULL, "tensor list is NULL with ntensors = %d", ntensors);
+    if ((st = check_counter(nonfinite)) != PA_OK)
+        return st;
+    int64_t total = 0, chunks = 0;
+    for (int32_t i = 0; i < ntensors; ++i) {
+        if ((st = check_tensor(list[i], pa::kE4, i)) != PA_OK)
+            return st;
+        total += list[i].n;
+        const int64_t c = describe(list[i], pa::kE4, &g_noalloc_host[i]);
+        g_noalloc_host[i].chunk0 = chunks;
+        chunks += c;
+    }
+    if (total == 0)
+        return ok();
+    pa::Desc *table = nullptr;
+    if ((st = noalloc_table_address(&table)) != PA_OK)
+        return st;
+    // The whole used prefix is rewritten, so nothing of an earlier call is read.
+    // A pageable-to-device async copy returns once the source has been staged.
+    cudaError_t e = cudaMemcpyAsync(table, g_noalloc_host, (size_t)ntensors * sizeof(pa::Desc),
+                                    cudaMemcpyHostToDevice, (cudaStream_t)stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "descriptor upload to the fixed device array");
+    int grid = 0;
+    if ((st = grid_for(kSlotE4Multi, chunks, &grid)) != PA_OK)
+        return st;
+    pa::Desc none;
+    std::memset(&none, 0, sizeof none);
+    if (s.bc2 == 1.0f)
+        pa::adamw_step_kernel<pa::kE4, true, true><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
+            table, ntensors, chunks, none, s, nonfinite);
+    else
+        pa::adamw_step_kernel<pa::kE4, true, false><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
+            table, ntensors, chunks, none, s, nonfinite);
+    return check_launch("adamw_step_kernel (no-alloc multi) launch");
+}

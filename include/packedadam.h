@@ -178,6 +178,32 @@ pa_status pa_adamw_step_fp32_multi(const pa_tensor *list, int32_t ntensors, int6
                                    double lr, double beta1, double beta2, double eps,
                                    double wd, unsigned long long *nonfinite, pa_stream stream);
 
+/* ---------------------------------------------------------------------------
+ * pa_adamw_step_packed_e4_multi_noalloc -- the step of
+ * pa_adamw_step_packed_e4_multi (same arguments, same bits) for callers that
+ * cannot have a library allocate device memory: for example a framework whose
+ * caching allocator has reserved the device's memory and expects every
+ * allocation to go through it, or a loop that must not meet the implicit
+ * synchronisation of cudaMalloc and cudaFree.  The pages have no counterpart;
+ * this entry point is an addition of this library.
+ *
+ * It calls no cudaMalloc, cudaFree or other allocating routine.  The list's
+ * descriptor table is copied (cudaMemcpyAsync on `stream`) into a fixed device
+ * array compiled into the library: PA_NOALLOC_MAX_TENSORS = 1024 descriptors
+ * of 56 bytes, which every device that loads the library holds until the
+ * process exits.  ntensors > 1024 returns PA_ERR_ARG.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  All calls share the array and each rewrites the
+ * part it uses: calls that overlap on the GPU (on different streams, or from
+ * racing host threads) race on it.
+ * ------------------------------------------------------------------------- */
+pa_status pa_adamw_step_packed_e4_multi_noalloc(const pa_tensor *list, int32_t ntensors,
+                                                int64_t step, double lr, double beta1,
+                                                double beta2, double eps, double wd,
+                                                unsigned long long *nonfinite,
+                                                pa_stream stream);
+
 /* Frees every cached descriptor table on every device (synchronises them). */
 pa_status pa_release_tables(void);
 
