@@ -11,7 +11,7 @@
 // Design.  The step is elementwise and bound by HBM bandwidth (20 bytes per
 // parameter for the packed modes), so the kernels are built for bytes in
 // flight: a persistent grid (resident CTAs per SM x SM count) strides over
-// 2048-element chunks; every thread issues all of its 16-byte loads of p, g
+// 16384-element chunks (8 waves of 2048); every thread issues all of its 16-byte loads of p, g
 // and the state for a chunk before any arithmetic, then stores with streaming
 // hints.  A multi-tensor list becomes one launch over a device-side
 // descriptor table, whose chunk prefix sums let each CTA walk from tensor to
@@ -47,7 +47,12 @@ constexpr int kMinBlocks = PA_MIN_BLOCKS;
 #ifndef PA_NOALLOC_MAX_TENSORS
 #define PA_NOALLOC_MAX_TENSORS 1024
 #endif
-constexpr int64_t kChunk = (int64_t)kThreads * kUnroll * 4;  // elements per chunk
+constexpr int64_t kWave = (int64_t)kThreads * kUnroll * 4;  // elements per wave
+#ifndef PA_WAVES
+#define PA_WAVES 8
+#endif
+constexpr int kWaves = PA_WAVES;                       // waves per chunk
+constexpr int64_t kChunk = kWave * kWaves;             // elements per chunk
 
 enum Mode : int { kE4 = 0, kFP16 = 1, kF32 = 2 };
 
@@ -87,7 +92,7 @@ __device__ __forceinline__ uint32_t packed_element(float &p, float g, uint32_t w
     p = o.p;
     if (!UNIT_BC2)
         rn = __fsqrt_rn(o.v);  // with bc2 == 1 the update already took sqrt(v')
-    return MODE == kE4 ? encode_word_e4(o.m, rn) : encode_word_fp16(o.m, rn);
+    return MODE == kE4 ? encode_step_word_e4(o.m, o.v, rn) : encode_word_fp16(o.m, rn);
 }
 
 // Element i of tensor d with 4-byte accesses (heads, tails, unaligned tensors).
@@ -114,70 +119,80 @@ __device__ __forceinline__ void scalar_element(const Desc &d, int64_t i, const S
 }
 
 // Chunk k of a 16-byte-path tensor: body elements [k*kChunk, (k+1)*kChunk)
-// counted from d.head.  All loads of the chunk are issued before any compute.
+// counted from d.head, walked as kWaves waves of kWave elements.  In a wave a
+// thread issues all of its 16-byte loads (kUnroll vectors of p, g and the
+// state) before any arithmetic; the per-thread pointers are set up once per
+// chunk and advanced by a constant per wave.
 template <int MODE, bool U1>
 __device__ __forceinline__ void vector_chunk(const Desc &d, int64_t k, const Scalars &s,
                                              uint32_t &bad)
 {
     const int tid = threadIdx.x;
     const int64_t nb = d.n - d.head;
-    const int64_t base = k * kChunk;
+    int64_t base = k * kChunk;
     if (k == 0 && tid < d.head)
         scalar_element<MODE, U1>(d, tid, s, bad);
-    float *P = d.p + d.head;
-    const float *G = d.g + d.head;
-    const bool whole = base + kChunk <= nb;  // uniform: no per-vector bound checks
-
-    float4 pv[kUnroll], gv[kUnroll];
-    uint4 wv[kUnroll];
-    float4 mv[kUnroll], vv[kUnroll];
-    bool full[kUnroll];
+    const int64_t end = base + kChunk < nb ? base + kChunk : nb;
+    const int64_t off = d.head + base + 4 * tid;
+    float *P = d.p + off;
+    const float *G = d.g + off;
+    uint32_t *W = static_cast<uint32_t *>(d.s1) + off;   // packed modes
+    float *M = static_cast<float *>(d.s1) + off;         // FP32 mode
+    float *V = static_cast<float *>(d.s2) + off;
+    constexpr int kStride = kThreads * 4;  // elements between a thread's vectors
+#pragma unroll 1
+    for (; base < end; base += kWave, P += kWave, G += kWave, W += kWave, M += kWave, V += kWave) {
+        const bool whole = base + kWave <= nb;  // uniform: no per-vector bound checks
+        float4 pv[kUnroll], gv[kUnroll];
+        uint4 wv[kUnroll];
+        float4 mv[kUnroll], vv[kUnroll];
+        bool full[kUnroll];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-        const int64_t e = base + 4 * ((int64_t)u * kThreads + tid);
-        full[u] = whole || e + 4 <= nb;
-        if (full[u]) {
-            pv[u] = load_stream(P + e);
-            gv[u] = load_readonly(G + e);
-            if constexpr (MODE == kF32) {
-                mv[u] = load_stream(static_cast<float *>(d.s1) + d.head + e);
-                vv[u] = load_stream(static_cast<float *>(d.s2) + d.head + e);
-            } else {
-                wv[u] = load_stream(static_cast<uint32_t *>(d.s1) + d.head + e);
+        for (int u = 0; u < kUnroll; ++u) {
+            full[u] = whole || base + 4 * ((int64_t)u * kThreads + tid) + 4 <= nb;
+            if (full[u]) {
+                pv[u] = load_stream(P + u * kStride);
+                gv[u] = load_readonly(G + u * kStride);
+                if constexpr (MODE == kF32) {
+                    mv[u] = load_stream(M + u * kStride);
+                    vv[u] = load_stream(V + u * kStride);
+                } else {
+                    wv[u] = load_stream(W + u * kStride);
+                }
             }
         }
-    }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-        const int64_t e = base + 4 * ((int64_t)u * kThreads + tid);
-        if (full[u]) {
-            float pp[4] = {pv[u].x, pv[u].y, pv[u].z, pv[u].w};
-            const float gg[4] = {gv[u].x, gv[u].y, gv[u].z, gv[u].w};
-            if constexpr (MODE == kF32) {
-                float mm[4] = {mv[u].x, mv[u].y, mv[u].z, mv[u].w};
-                float vq[4] = {vv[u].x, vv[u].y, vv[u].z, vv[u].w};
+        for (int u = 0; u < kUnroll; ++u) {
+            if (full[u]) {
+                float pp[4] = {pv[u].x, pv[u].y, pv[u].z, pv[u].w};
+                const float gg[4] = {gv[u].x, gv[u].y, gv[u].z, gv[u].w};
+                if constexpr (MODE == kF32) {
+                    float mm[4] = {mv[u].x, mv[u].y, mv[u].z, mv[u].w};
+                    float vq[4] = {vv[u].x, vv[u].y, vv[u].z, vv[u].w};
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const Moments o = adamw_element<U1>(pp[j], gg[j], mm[j], vq[j], s);
-                    bad += any_nonfinite(o);
-                    pp[j] = o.p;
-                    mm[j] = o.m;
-                    vq[j] = o.v;
+                    for (int j = 0; j < 4; ++j) {
+                        const Moments o = adamw_element<U1>(pp[j], gg[j], mm[j], vq[j], s);
+                        bad += any_nonfinite(o);
+                        pp[j] = o.p;
+                        mm[j] = o.m;
+                        vq[j] = o.v;
+                    }
+                    store_stream(M + u * kStride, make_float4(mm[0], mm[1], mm[2], mm[3]));
+                    store_stream(V + u * kStride, make_float4(vq[0], vq[1], vq[2], vq[3]));
+                } else {
+                    uint32_t ww[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        ww[j] = packed_element<MODE, U1>(pp[j], gg[j], ww[j], s, bad);
+                    store_stream(W + u * kStride, make_uint4(ww[0], ww[1], ww[2], ww[3]));
                 }
-                store_stream(static_cast<float *>(d.s1) + d.head + e, make_float4(mm[0], mm[1], mm[2], mm[3]));
-                store_stream(static_cast<float *>(d.s2) + d.head + e, make_float4(vq[0], vq[1], vq[2], vq[3]));
+                store_stream(P + u * kStride, make_float4(pp[0], pp[1], pp[2], pp[3]));
             } else {
-                uint32_t ww[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    ww[j] = packed_element<MODE, U1>(pp[j], gg[j], ww[j], s, bad);
-                store_stream(static_cast<uint32_t *>(d.s1) + d.head + e, make_uint4(ww[0], ww[1], ww[2], ww[3]));
+                // the one vector that straddles the end of the tensor
+                const int64_t e = base + 4 * ((int64_t)u * kThreads + tid);
+                for (int64_t i = e; i < nb; ++i)
+                    scalar_element<MODE, U1>(d, d.head + i, s, bad);
             }
-            store_stream(P + e, make_float4(pp[0], pp[1], pp[2], pp[3]));
-        } else if (e < nb) {
-            // the one vector that straddles the end of the tensor
-            for (int64_t i = e; i < nb; ++i)
-                scalar_element<MODE, U1>(d, d.head + i, s, bad);
         }
     }
 }
@@ -188,12 +203,10 @@ __device__ __forceinline__ void scalar_chunk(const Desc &d, int64_t k, const Sca
                                              uint32_t &bad)
 {
     const int64_t base = k * kChunk;
+    const int64_t end = base + kChunk < d.n ? base + kChunk : d.n;
 #pragma unroll 4
-    for (int u = 0; u < kUnroll * 4; ++u) {
-        const int64_t i = base + (int64_t)u * kThreads + threadIdx.x;
-        if (i < d.n)
-            scalar_element<MODE, U1>(d, i, s, bad);
-    }
+    for (int64_t i = base + threadIdx.x; i < end; i += kThreads)
+        scalar_element<MODE, U1>(d, i, s, bad);
 }
 
 __device__ __forceinline__ void flush_nonfinite(uint32_t bad, unsigned long long *nonfinite)
