@@ -18,6 +18,7 @@
 // tensor without a search.  No tensor cores: nothing here is a contraction.
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -26,6 +27,7 @@
 #include <string>
 #include <vector>
 
+#include "blockwise.cuh"
 #include "codecs.cuh"
 #include "packedadam.h"
 
@@ -48,11 +50,7 @@ constexpr int kMinBlocks = PA_MIN_BLOCKS;
 #define PA_NOALLOC_MAX_TENSORS 1024
 #endif
 constexpr int64_t kWave = (int64_t)kThreads * kUnroll * 4;  // elements per wave
-#ifndef PA_WAVES
-#define PA_WAVES 8
-#endif
-constexpr int kWaves = PA_WAVES;                       // waves per chunk
-constexpr int64_t kChunk = kWave * kWaves;             // elements per chunk
+constexpr int kMaxWaves = 8;  // waves per chunk, at most (chosen per launch)
 
 enum Mode : int { kE4 = 0, kFP16 = 1, kF32 = 2 };
 
@@ -118,21 +116,21 @@ __device__ __forceinline__ void scalar_element(const Desc &d, int64_t i, const S
     }
 }
 
-// Chunk k of a 16-byte-path tensor: body elements [k*kChunk, (k+1)*kChunk)
-// counted from d.head, walked as kWaves waves of kWave elements.  In a wave a
+// Chunk k of a 16-byte-path tensor: body elements [k*chunk, (k+1)*chunk)
+// counted from d.head, walked as waves of kWave elements.  In a wave a
 // thread issues all of its 16-byte loads (kUnroll vectors of p, g and the
 // state) before any arithmetic; the per-thread pointers are set up once per
 // chunk and advanced by a constant per wave.
 template <int MODE, bool U1>
-__device__ __forceinline__ void vector_chunk(const Desc &d, int64_t k, const Scalars &s,
-                                             uint32_t &bad)
+__device__ __forceinline__ void vector_chunk(const Desc &d, int64_t k, int64_t chunk,
+                                             const Scalars &s, uint32_t &bad)
 {
     const int tid = threadIdx.x;
     const int64_t nb = d.n - d.head;
-    int64_t base = k * kChunk;
+    int64_t base = k * chunk;
     if (k == 0 && tid < d.head)
         scalar_element<MODE, U1>(d, tid, s, bad);
-    const int64_t end = base + kChunk < nb ? base + kChunk : nb;
+    const int64_t end = base + chunk < nb ? base + chunk : nb;
     const int64_t off = d.head + base + 4 * tid;
     float *P = d.p + off;
     const float *G = d.g + off;
@@ -197,13 +195,13 @@ __device__ __forceinline__ void vector_chunk(const Desc &d, int64_t k, const Sca
     }
 }
 
-// Chunk k of a 4-byte-path tensor: elements [k*kChunk, (k+1)*kChunk).
+// Chunk k of a 4-byte-path tensor: elements [k*chunk, (k+1)*chunk).
 template <int MODE, bool U1>
-__device__ __forceinline__ void scalar_chunk(const Desc &d, int64_t k, const Scalars &s,
-                                             uint32_t &bad)
+__device__ __forceinline__ void scalar_chunk(const Desc &d, int64_t k, int64_t chunk,
+                                             const Scalars &s, uint32_t &bad)
 {
-    const int64_t base = k * kChunk;
-    const int64_t end = base + kChunk < d.n ? base + kChunk : d.n;
+    const int64_t base = k * chunk;
+    const int64_t end = base + chunk < d.n ? base + chunk : d.n;
 #pragma unroll 4
     for (int64_t i = base + threadIdx.x; i < end; i += kThreads)
         scalar_element<MODE, U1>(d, i, s, bad);
@@ -224,7 +222,8 @@ __device__ __forceinline__ void flush_nonfinite(uint32_t bad, unsigned long long
 template <int MODE, bool MULTI, bool U1>
 __global__ void __launch_bounds__(kThreads, kMinBlocks)
 adamw_step_kernel(const Desc *__restrict__ table, int32_t ntensors, int64_t total_chunks,
-                  const Desc single, const Scalars s, unsigned long long *nonfinite)
+                  int64_t chunk, const Desc single, const Scalars s,
+                  unsigned long long *nonfinite)
 {
     uint32_t bad = 0;
     int32_t t = 0;
@@ -244,9 +243,9 @@ adamw_step_kernel(const Desc *__restrict__ table, int32_t ntensors, int64_t tota
         }
         const int64_t k = c - d.chunk0;
         if (d.vec)
-            vector_chunk<MODE, U1>(d, k, s, bad);
+            vector_chunk<MODE, U1>(d, k, chunk, s, bad);
         else
-            scalar_chunk<MODE, U1>(d, k, s, bad);
+            scalar_chunk<MODE, U1>(d, k, chunk, s, bad);
     }
     flush_nonfinite(bad, nonfinite);
 }
@@ -287,138 +286,259 @@ decode_state_kernel(const uint32_t *__restrict__ word, float *__restrict__ m,
 // the block (16-byte loads of p and g, 4-byte loads of each code array).  The
 // new block absmax is a warp max (redux.sync on the binary32 bits of |x|,
 // which orders non-negative floats and lets a NaN win) followed by a max over
-// the 8 warp results in shared memory.  The code is the count of midpoints
-// below x / max(absmax, 1e-30), found by an 8-step binary search over the
-// midpoints held in shared memory.
-constexpr int kBlock = 2048;
-
-__device__ __forceinline__ int count_below(const float *mid, float c)
+// the 8 warp results in shared memory.
+//
+// Requantisation, per element: c = x / max(absmax, 1e-30) and code = the
+// number of the map's 255 midpoints strictly below c.
+//  * Division.  When the block scale is a normal number in [2^-100, 2^100),
+//    each thread takes y = RN(1/scale) once per block (__frcp_rn) and forms
+//    c = RN(q0 + r*y) with q0 = RN(x*y) and r = x - scale*q0 (exact by FMA):
+//    Markstein's theorem (P. Markstein, IBM J. Res. Dev. 34(1), 1990) makes
+//    this the correctly rounded quotient when y is the correctly rounded
+//    reciprocal and nothing under- or overflows; here |x| <= scale, so that
+//    holds for |x| >= 2^-100; zeros keep their sign by an OR of the sign bit;
+//    other |x| < 2^-100 use the IEEE divide.
+//  * Search.  A per-CTA table splits [-2, 2) into 4096 buckets on the
+//    order-preserving integer image of a binary32 (sign-magnitude flipped),
+//    2^19 consecutive values each; an entry holds the number of midpoints
+//    below the bucket's first value and how many midpoints fall inside the
+//    bucket.  The code is that count plus one comparison per midpoint inside
+//    c's bucket -- exact for any ascending map; for the log-linear maps a
+//    bucket rarely holds more than one midpoint.
+//  * A block whose scale is NaN, infinite or outside [2^-100, 2^100) takes
+//    the IEEE divide and an 8-step binary search over the midpoints.
+// Rare path: requantise a thread's 8 values with the IEEE divide and the
+// binary search (block scale NaN, infinite or outside [2^-100, 2^100)).  Out
+// of line to keep the hot loop's code small.
+__device__ __noinline__ uint2 requantise_slow(float x0, float x1, float x2, float x3, float x4,
+                                              float x5, float x6, float x7, float scale,
+                                              const float *mid)
 {
-    int pos = 0;
+    const float x[8] = {x0, x1, x2, x3, x4, x5, x6, x7};
+    uint2 code = make_uint2(0u, 0u);
 #pragma unroll
-    for (int step = 128; step >= 1; step >>= 1)
-        pos += (mid[pos + step - 1] < c) ? step : 0;
-    return pos;
+    for (int j = 0; j < 4; ++j) {
+        code.x |= (uint32_t)count_below(mid, __fdiv_rn(x[j], scale)) << (8 * j);
+        code.y |= (uint32_t)count_below(mid, __fdiv_rn(x[4 + j], scale)) << (8 * j);
+    }
+    return code;
 }
 
-__global__ void __launch_bounds__(kThreads)
-blockwise8_kernel(const float *__restrict__ p, const float *__restrict__ g,
-                  uint16_t *__restrict__ p_bf16, uint8_t *__restrict__ m_code,
-                  float *__restrict__ m_absmax, uint8_t *__restrict__ v_code,
-                  float *__restrict__ v_absmax, const float *__restrict__ qmap1,
-                  const float *__restrict__ qmap2, int64_t n, int64_t nblocks, const Scalars s,
+struct BlockwiseArgs {
+    const float *p;
+    const float *g;
+    uint16_t *p_bf16;
+    uint8_t *m_code;
+    float *m_absmax;
+    uint8_t *v_code;
+    float *v_absmax;
+    int64_t n;
+};
+
+struct BlockwiseShared {
+    float q1[256], q2[256], mid1[512], mid2[512];  // midpoints padded with +Inf
+    uint16_t bucket1[kBuckets], bucket2[kBuckets];
+    uint32_t warp_max[2][2][kThreads / 32];  // [iteration parity][m, v][warp]
+    uint32_t red[2][32];
+};
+
+// One 2048-element block.  WHOLE: every element is in range (all blocks but
+// a short last one), so no per-element bound logic is compiled in.
+// Redo, with the IEEE divide, the codes of the values that need it.
+__device__ __noinline__ uint2 requantise_fixup(float x0, float x1, float x2, float x3, float x4,
+                                               float x5, float x6, float x7, float scale,
+                                               uint32_t floor, const float *mid, uint2 code)
+{
+    const float x[8] = {x0, x1, x2, x3, x4, x5, x6, x7};
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        if (needs_ieee_divide(x[j], floor)) {
+            const uint32_t cj = (uint32_t)count_below(mid, __fdiv_rn(x[j], scale));
+            const int sh = 8 * (j & 3);
+            if (j < 4)
+                code.x = (code.x & ~(0xFFu << sh)) | (cj << sh);
+            else
+                code.y = (code.y & ~(0xFFu << sh)) | (cj << sh);
+        }
+    return code;
+}
+
+// Codes of a thread's 8 values of one moment, block scale bits sb in the
+// FMA-division range.  Values that need the IEEE divide (tiny nonzero x) are
+// redone in a fix-up pass that is rarely entered.
+template <int K>
+__device__ __forceinline__ uint2 requantise_fast(const float *x, uint32_t sb, const float *mid,
+                                                 const uint16_t *table, int k)
+{
+    const float scale = __uint_as_float(sb), y = __frcp_rn(scale);
+    const uint32_t floor = fast_quotient_floor(sb);
+    uint2 code = make_uint2(0u, 0u);
+    bool fix = false;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        fix |= needs_ieee_divide(x[j], floor);
+        const uint32_t cj = code_by_bucket<K>(mid, table, divide_by_scale_fma(x[j], scale, y), k);
+        if (j < 4)
+            code.x |= cj << (8 * j);
+        else
+            code.y |= cj << (8 * (j - 4));
+    }
+    if (fix)
+        code = requantise_fixup(x[0], x[1], x[2], x[3], x[4], x[5], x[6], x[7], scale, floor, mid,
+                                code);
+    return code;
+}
+
+template <bool WHOLE, int K>
+__device__ __forceinline__ void blockwise_block(const BlockwiseArgs &a, BlockwiseShared &sh,
+                                                int64_t b, int parity, const Scalars &s,
+                                                int k1, int k2, uint32_t &bad)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t base = b * kBlock;
+    const float am = a.m_absmax[b], av = a.v_absmax[b];
+    float mn[8], vn[8];
+    uint32_t um = 0, uv = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int64_t e0 = base + 1024 * h + 4 * tid;
+        float pv[4], gv[4];
+        uint32_t mc, vc;
+        if (WHOLE) {
+            const float4 x = __ldg(reinterpret_cast<const float4 *>(a.p + e0));
+            const float4 y = __ldg(reinterpret_cast<const float4 *>(a.g + e0));
+            pv[0] = x.x; pv[1] = x.y; pv[2] = x.z; pv[3] = x.w;
+            gv[0] = y.x; gv[1] = y.y; gv[2] = y.z; gv[3] = y.w;
+            mc = *reinterpret_cast<const uint32_t *>(a.m_code + e0);
+            vc = *reinterpret_cast<const uint32_t *>(a.v_code + e0);
+        } else {
+            mc = vc = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const bool in = e0 + j < a.n;
+                pv[j] = in ? a.p[e0 + j] : 0.0f;
+                gv[j] = in ? a.g[e0 + j] : 0.0f;
+                mc |= (in ? (uint32_t)a.m_code[e0 + j] : 0u) << (8 * j);
+                vc |= (in ? (uint32_t)a.v_code[e0 + j] : 0u) << (8 * j);
+            }
+        }
+        float po[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float m = __fmul_rn(sh.q1[__byte_perm(mc, 0u, 0x4440u + j)], am);
+            const float v = __fmul_rn(sh.q2[__byte_perm(vc, 0u, 0x4440u + j)], av);
+            const Moments o = adamw_element(pv[j], gv[j], m, v, s);
+            po[j] = o.p;
+            if (WHOLE || e0 + j < a.n) {
+                bad += any_nonfinite(o);
+                mn[4 * h + j] = o.m;
+                vn[4 * h + j] = o.v;
+            } else {
+                mn[4 * h + j] = 0.0f;  // |0| never raises the block max
+                vn[4 * h + j] = 0.0f;
+            }
+            um = max(um, __float_as_uint(mn[4 * h + j]) & 0x7FFFFFFFu);
+            uv = max(uv, __float_as_uint(vn[4 * h + j]) & 0x7FFFFFFFu);
+        }
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(po[0], po[1]);
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(po[2], po[3]);
+        if (WHOLE) {
+            uint2 packed;
+            packed.x = *reinterpret_cast<const uint32_t *>(&lo);
+            packed.y = *reinterpret_cast<const uint32_t *>(&hi);
+            __stcs(reinterpret_cast<uint2 *>(a.p_bf16 + e0), packed);
+        } else {
+            const __nv_bfloat16 hv[4] = {lo.x, lo.y, hi.x, hi.y};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (e0 + j < a.n)
+                    a.p_bf16[e0 + j] = *reinterpret_cast<const uint16_t *>(&hv[j]);
+        }
+    }
+    // block absmax of m' and v' (NaN bits win the unsigned max)
+    um = __reduce_max_sync(0xFFFFFFFFu, um);
+    uv = __reduce_max_sync(0xFFFFFFFFu, uv);
+    if (lane == 0) {
+        sh.warp_max[parity][0][warp] = um;
+        sh.warp_max[parity][1][warp] = uv;
+    }
+    __syncthreads();
+    um = __reduce_max_sync(0xFFFFFFFFu, lane < kThreads / 32 ? sh.warp_max[parity][0][lane] : 0u);
+    uv = __reduce_max_sync(0xFFFFFFFFu, lane < kThreads / 32 ? sh.warp_max[parity][1][lane] : 0u);
+    if (tid == 0) {
+        a.m_absmax[b] = __uint_as_float(um);
+        a.v_absmax[b] = __uint_as_float(uv);
+    }
+    const uint32_t floor_bits = __float_as_uint(1e-30f);
+    const uint32_t smb = max(um, floor_bits), svb = max(uv, floor_bits);  // NaN bits stay NaN
+    uint32_t mcode[2], vcode[2];
+    if (scale_in_fast_range(smb)) {  // uniform over the CTA
+        const uint2 cm = requantise_fast<K>(mn, smb, sh.mid1, sh.bucket1, k1);
+        mcode[0] = cm.x;
+        mcode[1] = cm.y;
+    } else {
+        const uint2 cm = requantise_slow(mn[0], mn[1], mn[2], mn[3], mn[4], mn[5], mn[6], mn[7],
+                                         __uint_as_float(smb), sh.mid1);
+        mcode[0] = cm.x;
+        mcode[1] = cm.y;
+    }
+    if (scale_in_fast_range(svb)) {
+        const uint2 cv = requantise_fast<K>(vn, svb, sh.mid2, sh.bucket2, k2);
+        vcode[0] = cv.x;
+        vcode[1] = cv.y;
+    } else {
+        const uint2 cv = requantise_slow(vn[0], vn[1], vn[2], vn[3], vn[4], vn[5], vn[6], vn[7],
+                                         __uint_as_float(svb), sh.mid2);
+        vcode[0] = cv.x;
+        vcode[1] = cv.y;
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int64_t e0 = base + 1024 * h + 4 * tid;
+        if (WHOLE) {
+            *reinterpret_cast<uint32_t *>(a.m_code + e0) = mcode[h];
+            *reinterpret_cast<uint32_t *>(a.v_code + e0) = vcode[h];
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (e0 + j < a.n) {
+                    a.m_code[e0 + j] = (uint8_t)(mcode[h] >> (8 * j));
+                    a.v_code[e0 + j] = (uint8_t)(vcode[h] >> (8 * j));
+                }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 4)
+blockwise8_kernel(const BlockwiseArgs a, const float *__restrict__ qmap1,
+                  const float *__restrict__ qmap2, int64_t nblocks, const Scalars s,
                   unsigned long long *nonfinite)
 {
-    __shared__ float q1[256], q2[256], mid1[256], mid2[256];
-    __shared__ uint32_t warp_max[2][2][kThreads / 32];  // [iteration parity][m, v][warp]
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    q1[tid] = __ldg(qmap1 + tid);
-    q2[tid] = __ldg(qmap2 + tid);
+    __shared__ BlockwiseShared sh;
+    const int tid = threadIdx.x;
+    sh.q1[tid] = __ldg(qmap1 + tid);
+    sh.q2[tid] = __ldg(qmap2 + tid);
     __syncthreads();
-    mid1[tid] = tid < 255 ? __fmul_rn(__fadd_rn(q1[tid], q1[tid + 1]), 0.5f) : INFINITY;
-    mid2[tid] = tid < 255 ? __fmul_rn(__fadd_rn(q2[tid], q2[tid + 1]), 0.5f) : INFINITY;
+    sh.mid1[tid] = tid < 255 ? __fmul_rn(__fadd_rn(sh.q1[tid], sh.q1[tid + 1]), 0.5f) : INFINITY;
+    sh.mid2[tid] = tid < 255 ? __fmul_rn(__fadd_rn(sh.q2[tid], sh.q2[tid + 1]), 0.5f) : INFINITY;
+    sh.mid1[256 + tid] = INFINITY;
+    sh.mid2[256 + tid] = INFINITY;
     __syncthreads();
-
-    const uint32_t floor_bits = __float_as_uint(1e-30f);
+    const int k1 = build_buckets(sh.mid1, sh.bucket1, sh.red[0]);
+    const int k2 = build_buckets(sh.mid2, sh.bucket2, sh.red[1]);
+    __syncthreads();
+    const int64_t whole_blocks = a.n / kBlock;
     uint32_t bad = 0;
     int parity = 0;
+    const bool two = k1 <= 2 && k2 <= 2;  // every bucket holds at most two midpoints
     for (int64_t b = blockIdx.x; b < nblocks; b += gridDim.x, parity ^= 1) {
-        const int64_t base = b * kBlock;
-        const bool whole = base + kBlock <= n;
-        const float am = m_absmax[b], av = v_absmax[b];
-        float mn[8], vn[8];
-        uint32_t um = 0, uv = 0;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int64_t e0 = base + 1024 * h + 4 * tid;
-            float pv[4], gv[4];
-            uint32_t mc, vc;
-            if (whole) {
-                const float4 a = __ldg(reinterpret_cast<const float4 *>(p + e0));
-                const float4 c = __ldg(reinterpret_cast<const float4 *>(g + e0));
-                pv[0] = a.x; pv[1] = a.y; pv[2] = a.z; pv[3] = a.w;
-                gv[0] = c.x; gv[1] = c.y; gv[2] = c.z; gv[3] = c.w;
-                mc = *reinterpret_cast<const uint32_t *>(m_code + e0);
-                vc = *reinterpret_cast<const uint32_t *>(v_code + e0);
-            } else {
-                mc = vc = 0;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const bool in = e0 + j < n;
-                    pv[j] = in ? p[e0 + j] : 0.0f;
-                    gv[j] = in ? g[e0 + j] : 0.0f;
-                    mc |= (in ? (uint32_t)m_code[e0 + j] : 0u) << (8 * j);
-                    vc |= (in ? (uint32_t)v_code[e0 + j] : 0u) << (8 * j);
-                }
-            }
-            float po[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float m = __fmul_rn(q1[(mc >> (8 * j)) & 0xFFu], am);
-                const float v = __fmul_rn(q2[(vc >> (8 * j)) & 0xFFu], av);
-                const Moments o = adamw_element(pv[j], gv[j], m, v, s);
-                const bool in = whole || e0 + j < n;
-                bad += in ? any_nonfinite(o) : 0u;
-                po[j] = o.p;
-                mn[4 * h + j] = in ? o.m : 0.0f;
-                vn[4 * h + j] = in ? o.v : 0.0f;
-                um = max(um, __float_as_uint(mn[4 * h + j]) & 0x7FFFFFFFu);
-                uv = max(uv, __float_as_uint(vn[4 * h + j]) & 0x7FFFFFFFu);
-            }
-            const __nv_bfloat162 lo = __floats2bfloat162_rn(po[0], po[1]);
-            const __nv_bfloat162 hi = __floats2bfloat162_rn(po[2], po[3]);
-            if (whole) {
-                uint2 packed;
-                packed.x = *reinterpret_cast<const uint32_t *>(&lo);
-                packed.y = *reinterpret_cast<const uint32_t *>(&hi);
-                __stcs(reinterpret_cast<uint2 *>(p_bf16 + e0), packed);
-            } else {
-                const __nv_bfloat16 hv[4] = {lo.x, lo.y, hi.x, hi.y};
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (e0 + j < n)
-                        p_bf16[e0 + j] = *reinterpret_cast<const uint16_t *>(&hv[j]);
-            }
-        }
-        // block absmax of m' and v'
-        um = __reduce_max_sync(0xFFFFFFFFu, um);
-        uv = __reduce_max_sync(0xFFFFFFFFu, uv);
-        if (lane == 0) {
-            warp_max[parity][0][warp] = um;
-            warp_max[parity][1][warp] = uv;
-        }
-        __syncthreads();
-#pragma unroll
-        for (int w = 0; w < kThreads / 32; ++w) {
-            um = max(um, warp_max[parity][0][w]);
-            uv = max(uv, warp_max[parity][1][w]);
-        }
-        if (tid == 0) {
-            m_absmax[b] = __uint_as_float(um);
-            v_absmax[b] = __uint_as_float(uv);
-        }
-        const float sm = __uint_as_float(max(um, floor_bits));  // NaN bits stay NaN
-        const float sv = __uint_as_float(max(uv, floor_bits));
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int64_t e0 = base + 1024 * h + 4 * tid;
-            uint32_t mc = 0, vc = 0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                mc |= (uint32_t)count_below(mid1, __fdiv_rn(mn[4 * h + j], sm)) << (8 * j);
-                vc |= (uint32_t)count_below(mid2, __fdiv_rn(vn[4 * h + j], sv)) << (8 * j);
-            }
-            if (whole) {
-                *reinterpret_cast<uint32_t *>(m_code + e0) = mc;
-                *reinterpret_cast<uint32_t *>(v_code + e0) = vc;
-            } else {
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    if (e0 + j < n) {
-                        m_code[e0 + j] = (uint8_t)(mc >> (8 * j));
-                        v_code[e0 + j] = (uint8_t)(vc >> (8 * j));
-                    }
-            }
+        if (b < whole_blocks) {
+            if (two)
+                blockwise_block<true, 2>(a, sh, b, parity, s, k1, k2, bad);
+            else
+                blockwise_block<true, 0>(a, sh, b, parity, s, k1, k2, bad);
+        } else {
+            blockwise_block<false, 0>(a, sh, b, parity, s, k1, k2, bad);
         }
     }
     flush_nonfinite(bad, nonfinite);
@@ -542,6 +662,22 @@ pa_status grid_for(int slot, int64_t work, int *grid)
     return PA_OK;
 }
 
+// Elements per chunk for a launch over `elements` parameters: as many waves
+// (at most kMaxWaves) as keep at least 32 chunks per resident CTA, so that
+// large launches amortise the per-chunk set-up and small ones still spread
+// over every SM.
+pa_status chunk_size(int slot, int64_t elements, int64_t *chunk)
+{
+    int full = 0;
+    pa_status st = grid_for(slot, INT64_MAX, &full);
+    if (st != PA_OK)
+        return st;
+    int64_t waves = elements / (pa::kWave * (int64_t)full * 32);
+    waves = waves < 1 ? 1 : (waves > pa::kMaxWaves ? pa::kMaxWaves : waves);
+    *chunk = waves * pa::kWave;
+    return PA_OK;
+}
+
 pa_status check_launch(const char *what)
 {
     cudaError_t e = cudaGetLastError();
@@ -554,7 +690,7 @@ pa_status check_launch(const char *what)
 // Fill d for one tensor; returns its chunk count.  The 16-byte path needs p, g
 // and the state (and v in FP32 mode) to share their address modulo 16; the
 // head peels the elements before the first 16-byte boundary.
-int64_t describe(const pa_tensor &t, int mode, Desc *d)
+int64_t describe(const pa_tensor &t, int mode, int64_t chunk, Desc *d)
 {
     d->p = t.p;
     d->g = t.g;
@@ -574,7 +710,7 @@ int64_t describe(const pa_tensor &t, int mode, Desc *d)
     if (t.n == 0)
         return 0;
     const int64_t body = same ? t.n - head : t.n;
-    const int64_t chunks = (body + pa::kChunk - 1) / pa::kChunk;
+    const int64_t chunks = (body + chunk - 1) / chunk;
     return chunks > 0 ? chunks : 1;
 }
 
@@ -612,17 +748,20 @@ pa_status step_single(const pa_tensor &t, int64_t step, double lr, double beta1,
     if (t.n == 0)
         return ok();
     Desc d;
-    const int64_t chunks = describe(t, MODE, &d);
+    int64_t chunk = 0;
+    if ((st = chunk_size(MODE, t.n, &chunk)) != PA_OK)
+        return st;
+    const int64_t chunks = describe(t, MODE, chunk, &d);
     d.chunk0 = 0;
     int grid = 0;
     if ((st = grid_for(MODE, chunks, &grid)) != PA_OK)
         return st;
     if (s.bc2 == 1.0f)
         pa::adamw_step_kernel<MODE, false, true><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
-            nullptr, 1, chunks, d, s, nonfinite);
+            nullptr, 1, chunks, chunk, d, s, nonfinite);
     else
         pa::adamw_step_kernel<MODE, false, false><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
-            nullptr, 1, chunks, d, s, nonfinite);
+            nullptr, 1, chunks, chunk, d, s, nonfinite);
     return check_launch("adamw_step_kernel launch");
 }
 
@@ -634,6 +773,7 @@ pa_status step_single(const pa_tensor &t, int64_t step, double lr, double beta1,
 struct Table {
     int device;
     int mode;
+    int64_t chunk;
     std::vector<Desc> host;
     Desc *dev;
     int64_t chunks;
@@ -645,13 +785,13 @@ std::vector<Table> g_tables;
 uint64_t g_tick = 0;
 constexpr size_t kMaxTables = 64;
 
-pa_status table_for(const pa_tensor *list, int32_t ntensors, int mode, const Desc **dev_table,
-                    int64_t *chunks)
+pa_status table_for(const pa_tensor *list, int32_t ntensors, int mode, int64_t chunk,
+                    const Desc **dev_table, int64_t *chunks)
 {
     std::vector<Desc> host((size_t)ntensors);
     int64_t total = 0;
     for (int32_t i = 0; i < ntensors; ++i) {
-        const int64_t c = describe(list[i], mode, &host[(size_t)i]);
+        const int64_t c = describe(list[i], mode, chunk, &host[(size_t)i]);
         host[(size_t)i].chunk0 = total;
         total += c;
     }
@@ -662,7 +802,7 @@ pa_status table_for(const pa_tensor *list, int32_t ntensors, int mode, const Des
     std::lock_guard<std::mutex> lock(g_tab_mu);
     ++g_tick;
     for (Table &t : g_tables) {
-        if (t.device == dev && t.mode == mode && t.host.size() == host.size() &&
+        if (t.device == dev && t.mode == mode && t.chunk == chunk && t.host.size() == host.size() &&
             std::memcmp(t.host.data(), host.data(), host.size() * sizeof(Desc)) == 0) {
             t.last_use = g_tick;
             *dev_table = t.dev;
@@ -684,6 +824,7 @@ pa_status table_for(const pa_tensor *list, int32_t ntensors, int mode, const Des
     Table t;
     t.device = dev;
     t.mode = mode;
+    t.chunk = chunk;
     t.chunks = total;
     t.last_use = g_tick;
     t.dev = nullptr;
@@ -733,8 +874,10 @@ pa_status step_multi(const pa_tensor *list, int32_t ntensors, int64_t step, doub
     if (total == 0)
         return ok();
     const Desc *table = nullptr;
-    int64_t chunks = 0;
-    if ((st = table_for(list, ntensors, MODE, &table, &chunks)) != PA_OK)
+    int64_t chunks = 0, chunk = 0;
+    if ((st = chunk_size(MODE + 3, total, &chunk)) != PA_OK)
+        return st;
+    if ((st = table_for(list, ntensors, MODE, chunk, &table, &chunks)) != PA_OK)
         return st;
     int grid = 0;
     if ((st = grid_for(MODE + 3, chunks, &grid)) != PA_OK)
@@ -743,10 +886,10 @@ pa_status step_multi(const pa_tensor *list, int32_t ntensors, int64_t step, doub
     std::memset(&none, 0, sizeof none);
     if (s.bc2 == 1.0f)
         pa::adamw_step_kernel<MODE, true, true><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
-            table, ntensors, chunks, none, s, nonfinite);
+            table, ntensors, chunks, chunk, none, s, nonfinite);
     else
         pa::adamw_step_kernel<MODE, true, false><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
-            table, ntensors, chunks, none, s, nonfinite);
+            table, ntensors, chunks, chunk, none, s, nonfinite);
     return check_launch("adamw_step_kernel (multi) launch");
 }
 
@@ -919,8 +1062,9 @@ pa_status pa_adamw_step_blockwise8(const float *p, const float *g, uint16_t *p_b
     int grid = 0;
     if ((st = grid_for(kSlotBlockwise, nblocks, &grid)) != PA_OK)
         return st;
+    const pa::BlockwiseArgs args = {p, g, p_bf16, m_code, m_absmax, v_code, v_absmax, n};
     pa::blockwise8_kernel<<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
-        p, g, p_bf16, m_code, m_absmax, v_code, v_absmax, qmap1, qmap2, n, nblocks, s, nonfinite);
+        args, qmap1, qmap2, nblocks, s, nonfinite);
     return check_launch("blockwise8_kernel launch");
 }
 
@@ -1010,17 +1154,21 @@ extern "C" pa_status pa_adamw_step_packed_e4_multi_noalloc(
         return fail(PA_ERR_NULL, "tensor list is NULL with ntensors = %d", ntensors);
     if ((st = check_counter(nonfinite)) != PA_OK)
         return st;
-    int64_t total = 0, chunks = 0;
+    int64_t total = 0, chunks = 0, chunk = 0;
     for (int32_t i = 0; i < ntensors; ++i) {
         if ((st = check_tensor(list[i], pa::kE4, i)) != PA_OK)
             return st;
         total += list[i].n;
-        const int64_t c = describe(list[i], pa::kE4, &g_noalloc_host[i]);
-        g_noalloc_host[i].chunk0 = chunks;
-        chunks += c;
     }
     if (total == 0)
         return ok();
+    if ((st = chunk_size(kSlotE4Multi, total, &chunk)) != PA_OK)
+        return st;
+    for (int32_t i = 0; i < ntensors; ++i) {
+        const int64_t c = describe(list[i], pa::kE4, chunk, &g_noalloc_host[i]);
+        g_noalloc_host[i].chunk0 = chunks;
+        chunks += c;
+    }
     pa::Desc *table = nullptr;
     if ((st = noalloc_table_address(&table)) != PA_OK)
         return st;
@@ -1037,9 +1185,9 @@ extern "C" pa_status pa_adamw_step_packed_e4_multi_noalloc(
     std::memset(&none, 0, sizeof none);
     if (s.bc2 == 1.0f)
         pa::adamw_step_kernel<pa::kE4, true, true><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
-            table, ntensors, chunks, none, s, nonfinite);
+            table, ntensors, chunks, chunk, none, s, nonfinite);
     else
         pa::adamw_step_kernel<pa::kE4, true, false><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
-            table, ntensors, chunks, none, s, nonfinite);
+            table, ntensors, chunks, chunk, none, s, nonfinite);
     return check_launch("adamw_step_kernel (no-alloc multi) launch");
 }

@@ -105,7 +105,7 @@ def traffic_per_param(mode):
         return None
     src = os.path.join(ROOT, "adamw_update_gb300", "csrc")
     h = hashlib.sha256()
-    for name in ("packedadam.cu", "codecs.cuh"):
+    for name in ("packedadam.cu", "codecs.cuh", "blockwise.cuh"):
         with open(os.path.join(src, name), "rb") as f:
             h.update(f.read())
     entry = d.get(mode)

@@ -1,0 +1,98 @@
+// GPU check of the blockwise requantiser's helpers (test code): the bucket
+// search against the plain 8-step binary search for every binary32 c in
+// [-1, 1], and the FMA division by the block scale against __fdiv_rn on
+// random (x, scale) pairs.  Kernels only add to counters and write the first
+// mismatch into a fixed 4-word slot claimed with atomicCAS.
+#include <cuda_runtime.h>
+#include <cstdint>
+#include "blockwise.cuh"
+
+using namespace pa;
+
+__device__ void note(unsigned long long *count, uint32_t *first, uint32_t a, uint32_t b, uint32_t got, uint32_t want)
+{
+    atomicAdd(count, 1ull);
+    if (atomicCAS(first, 0u, 1u) == 0u) {
+        first[1] = a; first[2] = b; first[3] = got ^ (want << 16);
+    }
+}
+
+// every c in [-1, 1]: ordered keys from ordered_bits(-1) to ordered_bits(1)
+__global__ void search_all(const float *qmap, unsigned long long *count, uint32_t *first)
+{
+    __shared__ float q[256], mid[512];
+    __shared__ uint16_t table[kBuckets];
+    __shared__ uint32_t red[32];
+    const int tid = threadIdx.x;
+    q[tid] = qmap[tid];
+    __syncthreads();
+    mid[tid] = tid < 255 ? __fmul_rn(__fadd_rn(q[tid], q[tid + 1]), 0.5f) : INFINITY;
+    mid[256 + tid] = INFINITY;
+    __syncthreads();
+    const int k = build_buckets(mid, table, red);
+    __syncthreads();
+    const uint32_t k_lo = ordered_bits(-1.0f), k_hi = ordered_bits(1.0f);
+    const uint64_t span = (uint64_t)(k_hi - k_lo) + 1;
+    for (uint64_t i = blockIdx.x * (uint64_t)blockDim.x + tid; i < span; i += (uint64_t)gridDim.x * blockDim.x) {
+        const float c = from_ordered_bits(k_lo + (uint32_t)i);
+        const uint32_t got = k <= 2 ? code_by_bucket<2>(mid, table, c, k) : code_by_bucket<0>(mid, table, c, k);
+        const uint32_t want = (uint32_t)count_below(mid, c);
+        if (got != want)
+            note(count, first, __float_as_uint(c), 0, got, want);
+    }
+}
+
+__device__ uint32_t mix32(uint64_t x)
+{
+    x ^= x >> 31; x *= 0x7fb5d329728ea185ull; x ^= x >> 27; x *= 0x81dadef4bc2dd44dull; x ^= x >> 33;
+    return (uint32_t)x;
+}
+
+__global__ void divide_random(uint64_t n, uint64_t seed, unsigned long long *count, uint32_t *first)
+{
+    for (uint64_t i = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; i < n; i += (uint64_t)gridDim.x * blockDim.x) {
+        const uint32_t r0 = mix32(3 * i + seed), r1 = mix32(3 * i + 1 + seed), r2 = mix32(3 * i + 2 + seed);
+        // scale: a normal number in [2^-100, 2^100)
+        const uint32_t sb = 0x0D800000u + r0 % 0x64000000u;
+        // x: |x| <= scale, exponent up to 160 binades below, some zeros, random sign
+        const uint32_t drop = (r1 >> 24) % 160u;
+        uint32_t xb = (r1 & 0x007FFFFFu) | ((sb & 0x7F800000u) - (drop << 23) * ((sb >> 23) > drop));
+        if ((sb >> 23) <= drop) xb = r1 & 0x007FFFFFu;  // subnormal x
+        if (xb > sb) xb = sb;
+        if ((r2 & 0xFFu) == 0u) xb = 0u;
+        xb |= r2 & 0x80000000u;
+        const float x = __uint_as_float(xb), s = __uint_as_float(sb);
+        const float got = needs_ieee_divide(x, fast_quotient_floor(sb)) ? __fdiv_rn(x, s)
+                                                                        : divide_by_scale_fma(x, s, __frcp_rn(s));
+        const float want = __fdiv_rn(x, s);
+        if (__float_as_uint(got) != __float_as_uint(want))
+            note(count, first, xb, sb, __float_as_uint(got), __float_as_uint(want));
+    }
+}
+
+extern "C" int run_search_all(const float *qmap_host, unsigned long long *count_host, uint32_t *first_host)
+{
+    float *q; unsigned long long *c; uint32_t *f;
+    if (cudaMalloc(&q, 256 * 4) || cudaMalloc(&c, 8) || cudaMalloc(&f, 16)) return -1;
+    cudaMemcpy(q, qmap_host, 256 * 4, cudaMemcpyHostToDevice);
+    cudaMemset(c, 0, 8); cudaMemset(f, 0, 16);
+    search_all<<<152 * 4, kThreadsPerBlockwiseCta>>>(q, c, f);
+    const int e = (int)cudaDeviceSynchronize();
+    cudaMemcpy(count_host, c, 8, cudaMemcpyDeviceToHost);
+    cudaMemcpy(first_host, f, 16, cudaMemcpyDeviceToHost);
+    cudaFree(q); cudaFree(c); cudaFree(f);
+    return e;
+}
+
+extern "C" int run_divide_random(uint64_t n, uint64_t seed, unsigned long long *count_host, uint32_t *first_host)
+{
+    unsigned long long *c; uint32_t *f;
+    if (cudaMalloc(&c, 8) || cudaMalloc(&f, 16)) return -1;
+    cudaMemset(c, 0, 8); cudaMemset(f, 0, 16);
+    divide_random<<<152 * 8, 256>>>(n, seed, c, f);
+    const int e = (int)cudaDeviceSynchronize();
+    cudaMemcpy(count_host, c, 8, cudaMemcpyDeviceToHost);
+    cudaMemcpy(first_host, f, 16, cudaMemcpyDeviceToHost);
+    cudaFree(c); cudaFree(f);
+    return e;
+}
