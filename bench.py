@@ -65,6 +65,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle sample")
     ap.add_argument("--fast", action="store_true", help="use libpackedadam_fast.so")
+    ap.add_argument("--params", type=int, default=None,
+                    help="override the parameter count of a one-tensor workload (flat-7e9, "
+                         "blockwise-1e9): the same distributions at another size, for profiling")
     return ap.parse_args()
 
 
@@ -175,12 +178,15 @@ class ClockSampler:
 # Workload construction (device buffers, seeded; outside every timed region)
 # ---------------------------------------------------------------------------
 
+PARAMS_OVERRIDE = {}
+
+
 def tensor_sizes(name):
     if name == "gpt-52":
         return [n for _, n in wl.GPT52_SHAPES]
     if name == "gpt2-148":
         return [n for _, n in wl.GPT2_148_SHAPES]
-    return [wl.WORKLOADS[name]["n"]]
+    return [PARAMS_OVERRIDE.get(name, wl.WORKLOADS[name]["n"])]
 
 
 def fill_gradient_(name, g, sizes, seed):
@@ -470,7 +476,8 @@ def run_ours(args):
             "dtype": "f32",
             "data": "synthetic",
             "config": {
-                "workload": w.name, "mode": w.mode, "params_per_gpu": w.n,
+                "workload": w.name if args.params is None else f"{w.name} at {w.n} params",
+                "mode": w.mode, "params_per_gpu": w.n,
                 "tensors": len(w.sizes), "bytes_per_param": bpp,
                 "l2": "flushed between steps (512 MB write)" if flush is not None
                       else f"inputs larger than L2 ({w.bytes_per_step() / 1e9:.1f} GB per step)",
@@ -554,7 +561,8 @@ def run_reference(args):
 
     mode = "blockwise" if args.workload == "blockwise-1e9" else args.mode
     cores = host_cores()
-    total = wl.WORKLOADS[args.workload]["n"]
+    total = tensor_sizes(args.workload)[0] if args.workload in ("flat-7e9", "blockwise-1e9") \
+        else wl.WORKLOADS[args.workload]["n"]
     budget = 150.0  # seconds for the whole run
     per_step = min(10.0, budget / max(1, args.steps + args.warmup))
     s = sample_size(mode, per_step, cores, total)
@@ -613,6 +621,10 @@ def run_reference(args):
 
 def main():
     args = parse()
+    if args.params is not None:
+        if args.workload not in ("flat-7e9", "blockwise-1e9"):
+            raise SystemExit("--params applies to the one-tensor workloads only")
+        PARAMS_OVERRIDE[args.workload] = args.params
     if args.impl == "reference":
         run_reference(args)
     else:
