@@ -26,7 +26,7 @@ __all__ = [
     "pa_adamw_step_packed_e4", "pa_adamw_step_packed_fp16", "pa_adamw_step_fp32",
     "pa_adamw_step_blockwise8", "pa_adamw_step_packed_e4_multi",
     "pa_adamw_step_packed_fp16_multi", "pa_adamw_step_fp32_multi", "pa_release_tables",
-    "shard_bounds", "pa_adamw_step_packed_e4_multi_noalloc",
+    "shard_bounds", "pa_adamw_step_packed_e4_multi_noalloc", "pa_adamw_step_packed_e4_host",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -288,3 +288,31 @@ def pa_adamw_step_packed_e4_multi_noalloc(entries, step, lr=1e-3, beta1=0.9, bet
     stream capture."""
     _multi(_lib.pa_adamw_step_packed_e4_multi_noalloc, entries, False, step, lr, beta1, beta2,
            eps, wd, nonfinite, stream)
+
+
+# ---- the packed-E4 step over host-resident tensors ------------------------------
+
+_lib.pa_adamw_step_packed_e4_host.restype = _i32
+_lib.pa_adamw_step_packed_e4_host.argtypes = [_vp, _vp, _vp, _i64, *_HYP, _vp, _i64, _vp, _vp]
+
+
+def _host_ptr(t, dtype):
+    if t.is_cuda:
+        raise ValueError("expected a host (CPU) tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"expected dtype {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def pa_adamw_step_packed_e4_host(p, g, state, workspace, step, lr=1e-3, beta1=0.9, beta2=0.999,
+                                 eps=1e-8, wd=0.0, nonfinite=None, stream=None):
+    """Packed-E4 step over host tensors (pinned for overlap), streamed through
+    the CUDA tensor `workspace` (uint8, >= 2.36 MB; larger means longer
+    chunks).  Synchronise `stream` before reading p or state."""
+    torch = _t()
+    _check(_lib.pa_adamw_step_packed_e4_host(
+        _host_ptr(p, torch.float32), _host_ptr(g, torch.float32), _host_ptr(state, torch.int32),
+        p.numel(), *_hyp(step, lr, beta1, beta2, eps, wd), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(nonfinite), _stream(stream)))

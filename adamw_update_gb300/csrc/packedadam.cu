@@ -1191,3 +1191,143 @@ extern "C" pa_status pa_adamw_step_packed_e4_multi_noalloc(
             table, ntensors, chunks, chunk, none, s, nonfinite);
     return check_launch("adamw_step_kernel (no-alloc multi) launch");
 }
+
+// ===========================================================================
+// Packed-E4 step over host-resident parameters, gradients and state
+// ===========================================================================
+// The tensors stay in (page-locked) host memory; the call streams them through
+// a caller-provided device workspace in chunks.  Three stages rotate: while
+// the step runs on chunk i (caller's stream), chunk i+1 is copied in (an
+// internal upload stream) and chunk i-1 is copied out (an internal download
+// stream); events order the three.  Each element crosses the host link as
+// 12 bytes in (p, g, word) and 8 bytes out (p, word).
+namespace {
+
+constexpr int kHostStages = 3;
+
+struct HostPipe {
+    bool ready = false;
+    cudaStream_t up = nullptr, down = nullptr;
+    cudaEvent_t entry = nullptr;
+    cudaEvent_t in_done[kHostStages] = {}, step_done[kHostStages] = {}, out_done[kHostStages] = {};
+};
+
+std::mutex g_pipe_mu;
+HostPipe g_pipe[64];
+
+pa_status host_pipe(int dev, HostPipe **out)
+{
+    HostPipe &hp = g_pipe[dev];
+    if (!hp.ready) {
+        cudaError_t e = cudaStreamCreateWithFlags(&hp.up, cudaStreamNonBlocking);
+        if (e == cudaSuccess)
+            e = cudaStreamCreateWithFlags(&hp.down, cudaStreamNonBlocking);
+        if (e == cudaSuccess)
+            e = cudaEventCreateWithFlags(&hp.entry, cudaEventDisableTiming);
+        for (int k = 0; k < kHostStages && e == cudaSuccess; ++k) {
+            e = cudaEventCreateWithFlags(&hp.in_done[k], cudaEventDisableTiming);
+            if (e == cudaSuccess)
+                e = cudaEventCreateWithFlags(&hp.step_done[k], cudaEventDisableTiming);
+            if (e == cudaSuccess)
+                e = cudaEventCreateWithFlags(&hp.out_done[k], cudaEventDisableTiming);
+        }
+        if (e != cudaSuccess)
+            return cuda_fail(e, "creating the host-step streams and events");
+        hp.ready = true;
+    }
+    *out = &hp;
+    return PA_OK;
+}
+
+}  // namespace
+
+extern "C" pa_status pa_adamw_step_packed_e4_host(float *p, const float *g, uint32_t *state,
+                                                  int64_t n, int64_t step, double lr,
+                                                  double beta1, double beta2, double eps,
+                                                  double wd, void *workspace,
+                                                  int64_t workspace_bytes,
+                                                  unsigned long long *nonfinite,
+                                                  pa_stream stream)
+{
+    Scalars s;
+    pa_status st = make_scalars(step, lr, beta1, beta2, eps, wd, &s);
+    if (st != PA_OK)
+        return st;
+    if (n < 0 || workspace_bytes < 0)
+        return fail(PA_ERR_ARG, "n and workspace_bytes must be >= 0");
+    if (n == 0)
+        return ok();
+    if (!p || !g || !state || !workspace)
+        return fail(PA_ERR_NULL, "NULL pointer with n = %lld", (long long)n);
+    if (!aligned(p, 4) || !aligned(g, 4) || !aligned(state, 4))
+        return fail(PA_ERR_ALIGN, "host arrays must be 4-byte aligned");
+    if (!aligned(workspace, 256))
+        return fail(PA_ERR_ALIGN, "workspace must be 256-byte aligned");
+    if ((st = check_counter(nonfinite)) != PA_OK)
+        return st;
+    // per stage: p, g, word arrays of `chunk` elements, each a multiple of 64
+    int64_t chunk = workspace_bytes / (kHostStages * 12) / 64 * 64;
+    if (chunk < 65536)
+        return fail(PA_ERR_ARG, "workspace of %lld bytes is below the minimum of %lld "
+                    "(3 stages x 12 bytes x 65536 elements)", (long long)workspace_bytes,
+                    (long long)(kHostStages * 12 * 65536));
+    if (chunk > n)
+        chunk = (n + 63) / 64 * 64;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64)
+        return fail(PA_ERR_CUDA, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_pipe_mu);  // one enqueue at a time per process
+    HostPipe *hp = nullptr;
+    if ((st = host_pipe(dev, &hp)) != PA_OK)
+        return st;
+    cudaStream_t cs = (cudaStream_t)stream;
+    char *ws = static_cast<char *>(workspace);
+    // uploads start after the work already queued on the caller's stream
+    if ((e = cudaEventRecord(hp->entry, cs)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(hp->up, hp->entry, 0)) != cudaSuccess)
+        return cuda_fail(e, "ordering the host step after the caller's stream");
+    const int64_t nchunks = (n + chunk - 1) / chunk;
+    for (int64_t i = 0; i < nchunks; ++i) {
+        const int k = (int)(i % kHostStages);
+        const int64_t off = i * chunk, len = (n - off < chunk) ? n - off : chunk;
+        float *sp = reinterpret_cast<float *>(ws + (size_t)k * 12 * chunk);
+        float *sg = sp + chunk;
+        uint32_t *sw = reinterpret_cast<uint32_t *>(sg + chunk);
+        // the stage is free once its previous download has finished
+        e = cudaStreamWaitEvent(hp->up, hp->out_done[k], 0);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(sp, p + off, (size_t)len * 4, cudaMemcpyHostToDevice, hp->up);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(sg, g + off, (size_t)len * 4, cudaMemcpyHostToDevice, hp->up);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(sw, state + off, (size_t)len * 4, cudaMemcpyHostToDevice, hp->up);
+        if (e == cudaSuccess)
+            e = cudaEventRecord(hp->in_done[k], hp->up);
+        if (e == cudaSuccess)
+            e = cudaStreamWaitEvent(cs, hp->in_done[k], 0);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "host step upload");
+        const pa_tensor t = {sp, sg, sw, nullptr, len};
+        if ((st = step_single<pa::kE4>(t, step, lr, beta1, beta2, eps, wd, nonfinite, stream)) != PA_OK)
+            return st;
+        e = cudaEventRecord(hp->step_done[k], cs);
+        if (e == cudaSuccess)
+            e = cudaStreamWaitEvent(hp->down, hp->step_done[k], 0);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(p + off, sp, (size_t)len * 4, cudaMemcpyDeviceToHost, hp->down);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(state + off, sw, (size_t)len * 4, cudaMemcpyDeviceToHost, hp->down);
+        if (e == cudaSuccess)
+            e = cudaEventRecord(hp->out_done[k], hp->down);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "host step download");
+    }
+    // the caller's stream resumes after the last downloads
+    for (int k = 0; k < kHostStages; ++k)
+        if ((e = cudaStreamWaitEvent(cs, hp->out_done[k], 0)) != cudaSuccess)
+            return cuda_fail(e, "ordering the caller's stream after the host step");
+    return ok();
+}

@@ -204,6 +204,32 @@ pa_status pa_adamw_step_packed_e4_multi_noalloc(const pa_tensor *list, int32_t n
                                                 unsigned long long *nonfinite,
                                                 pa_stream stream);
 
+/* ---------------------------------------------------------------------------
+ * pa_adamw_step_packed_e4_host -- the packed E4 step (as pa_adamw_step_packed_e4)
+ * over p, g and the state words held in HOST memory, for optimizer state kept
+ * off the device ("Packed AdamW Reference" README, "The canonical format": the
+ * state is 4 bytes per parameter instead of 8, which also shrinks the traffic
+ * over the host link: 12 bytes in and 8 bytes out per parameter).
+ * p, g, state: host arrays of n elements, 4-byte aligned; page-locked memory
+ * (cudaMallocHost or cudaHostRegister) lets the copies run asynchronously and
+ * overlap, pageable memory works but copies synchronously.
+ * workspace: caller-owned device memory, 256-byte aligned, of workspace_bytes
+ * >= 3 * 12 * 65536 bytes; the call streams the arrays through it in chunks of
+ * workspace_bytes / 36 elements (three rotating stages), overlapping uploads,
+ * the step and downloads on two internal streams (created on the first call on
+ * a device) and `stream`.  The call returns after queueing; `stream` is
+ * ordered after the last download, so synchronising `stream` makes the host
+ * arrays current.  Host enqueues are serialised by a process-wide lock; the
+ * workspace and host arrays must not be touched until `stream` has passed the
+ * call.  Errors as for the other steps; a workspace below the minimum is
+ * PA_ERR_ARG, a misaligned one PA_ERR_ALIGN.
+ * ------------------------------------------------------------------------- */
+pa_status pa_adamw_step_packed_e4_host(float *p, const float *g, uint32_t *state, int64_t n,
+                                       int64_t step, double lr, double beta1, double beta2,
+                                       double eps, double wd, void *workspace,
+                                       int64_t workspace_bytes, unsigned long long *nonfinite,
+                                       pa_stream stream);
+
 /* Frees every cached descriptor table on every device (synchronises them). */
 pa_status pa_release_tables(void);
 

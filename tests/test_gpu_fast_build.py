@@ -1,0 +1,102 @@
+"""The contracted-arithmetic build (libpackedadam_fast.so: FMA contraction,
+approximate divisions __fdividef) against the CPU oracle, one step from the
+same inputs: each state lane within 1 code step, blockwise absmax within 1e-6
+relative, codes and BF16 parameters within 1 step, and parameters within 16
+ulp of the largest of |p'|, |p*(1-lr*wd)| and |upd| (9 ulp measured on GB300).
+
+That parameter bound is not the 2 ulp one might hope for: p' = p*dk - upd is
+one FMA (0.5 ulp of p*dk from the unrounded product) and upd carries v'/bc2
+(__fdividef, 2 ulp), its square root (1.5 ulp), +eps and u (0.5 ulp each),
+u/den (__fdividef, 2 ulp) and m' = fma(b1, m, c1*g), whose single rounding
+differs from the two of the strict order by up to 1 ulp of b1*m -- many ulps
+of m' when the two terms nearly cancel.  When upd nearly cancels p*dk the
+difference is many ulps of the small result, so no bound in ulps of p' alone
+holds for this build.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as wl
+from gpu_helpers import dev, host_f32, host_u32
+
+pytestmark = pytest.mark.gpu
+HY = wl.HYPER
+
+
+@pytest.fixture(scope="module")
+def fast():
+    import adamw_update_gb300 as pa
+
+    return pa, pa.load_library(pa.library_path(fast=True))
+
+
+def _ulp(x):
+    x = np.abs(np.asarray(x, np.float32))
+    return np.spacing(np.maximum(x, np.float32(2.0 ** -126))).astype(np.float64)
+
+
+def _ordered_m(code):
+    code = code.astype(np.int64)
+    mag = code & 0x7FFF
+    return np.where(code & 0x8000, -mag, mag)
+
+
+def test_fast_build_packed_e4_within_tolerance(fast):
+    import torch
+
+    pa, lib = fast
+    n = 1 << 20
+    rng = np.random.default_rng(1)
+    p = rng.normal(0, 0.02, n).astype(np.float32)
+    g = (1e-3 * rng.standard_t(3, n)).astype(np.float32)
+    st, _ = oracle.encode_state(rng.normal(0, 1e-3, n), np.abs(rng.normal(0, 1e-3, n)))
+    for step in (1, 7, 100_000):
+        dp, ds = dev(p), dev(st)
+        rc = lib.pa_adamw_step_packed_e4(dp.data_ptr(), dev(g).data_ptr(), ds.data_ptr(), n, step,
+                                         HY["lr"], HY["beta1"], HY["beta2"], HY["eps"], HY["wd"],
+                                         None, torch.cuda.current_stream().cuda_stream)
+        assert rc == 0
+        torch.cuda.synchronize()
+        ep, ew, _ = oracle.step_packed(p, g, st, step, **HY)
+        gp, gw = host_f32(dp), host_u32(ds)
+        dm = np.abs(_ordered_m(gw & 0xFFFF) - _ordered_m(ew & 0xFFFF))
+        dr = np.abs((gw >> 16).astype(np.int64) - (ew >> 16).astype(np.int64))
+        assert dm.max() <= 1 and dr.max() <= 1, (step, dm.max(), dr.max())
+        pd = p * np.float32(1 - HY["lr"] * HY["wd"])
+        upd = pd.astype(np.float64) - ep.astype(np.float64)
+        scale = np.maximum(np.maximum(np.abs(ep), np.abs(pd)), np.abs(upd).astype(np.float32))
+        err = np.abs(gp.astype(np.float64) - ep.astype(np.float64)) / _ulp(scale)
+        assert err.max() <= 16.0, f"step {step}: params {err.max():.2f} ulp"
+
+
+def test_fast_build_blockwise_within_tolerance(fast):
+    import torch
+
+    pa, lib = fast
+    n = 64 * 2048 + 100
+    nb = -(-n // 2048)
+    rng = np.random.default_rng(2)
+    q1, q2 = wl.dynamic_qmap_signed(), wl.dynamic_qmap_unsigned()
+    p = rng.normal(0, 0.02, n).astype(np.float32)
+    g = rng.normal(0, 1e-3, n).astype(np.float32)
+    mc = rng.integers(0, 256, n).astype(np.uint8)
+    vc = rng.integers(0, 256, n).astype(np.uint8)
+    ma = np.abs(rng.normal(0, 1e-3, nb)).astype(np.float32)
+    va = np.abs(rng.normal(0, 1e-6, nb)).astype(np.float32)
+    d = [dev(x) for x in (p, g)] + [torch.empty(n, dtype=torch.bfloat16, device="cuda")]
+    d += [dev(mc), dev(ma), dev(vc), dev(va), dev(q1), dev(q2)]
+    rc = lib.pa_adamw_step_blockwise8(*[t.data_ptr() for t in d], n, 3, HY["lr"], HY["beta1"],
+                                      HY["beta2"], HY["eps"], HY["wd"], None,
+                                      torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    ob, emc, ema, evc, eva, _ = oracle.step_blockwise8(p, g, mc, ma, vc, va, q1, q2, 3, **HY)
+    gb = d[2].view(torch.int16).cpu().numpy().view(np.uint16).astype(np.int64)
+    assert np.abs(gb - ob.astype(np.int64)).max() <= 1  # BF16 within one step
+    np.testing.assert_allclose(host_f32(d[4]), ema, rtol=1e-6, atol=0)
+    np.testing.assert_allclose(host_f32(d[6]), eva, rtol=1e-6, atol=0)
+    assert np.abs(d[3].cpu().numpy().astype(np.int64) - emc.astype(np.int64)).max() <= 1
+    assert np.abs(d[5].cpu().numpy().astype(np.int64) - evc.astype(np.int64)).max() <= 1
