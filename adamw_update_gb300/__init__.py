@@ -27,6 +27,7 @@ __all__ = [
     "pa_adamw_step_blockwise8", "pa_adamw_step_packed_e4_multi",
     "pa_adamw_step_packed_fp16_multi", "pa_adamw_step_fp32_multi", "pa_release_tables",
     "shard_bounds", "pa_adamw_step_packed_e4_multi_noalloc", "pa_adamw_step_packed_e4_host",
+    "pa_hyper_table_fill", "pa_adamw_step_packed_e4_multi_graph",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -316,3 +317,41 @@ def pa_adamw_step_packed_e4_host(p, g, state, workspace, step, lr=1e-3, beta1=0.
         _host_ptr(p, torch.float32), _host_ptr(g, torch.float32), _host_ptr(state, torch.int32),
         p.numel(), *_hyp(step, lr, beta1, beta2, eps, wd), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(nonfinite), _stream(stream)))
+
+
+# ---- graph-replayable step: device table of per-step scalars ----------------------
+
+HYPER_ROW_FLOATS = 8  # pa_hyper: b1, b2, c1, c2, bc2, ss, dk, ef
+
+_lib.pa_hyper_table_fill.restype = _i32
+_lib.pa_hyper_table_fill.argtypes = [_vp, _i64, _i32, _vp, _d, _d, _d, _d, _d, _vp]
+_lib.pa_adamw_step_packed_e4_multi_graph.restype = _i32
+_lib.pa_adamw_step_packed_e4_multi_graph.argtypes = [
+    ctypes.POINTER(PaTensor), _i32, _vp, _i32, _vp, _vp, _vp, _vp]
+
+
+def pa_hyper_table_fill(rows, first_step, count, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8,
+                        wd=0.0, lr_per_step=None, stream=None):
+    """Fill `rows` (CUDA float32 tensor of >= count*8 floats) with the scalars of
+    steps first_step .. first_step+count-1; lr_per_step: optional schedule."""
+    torch = _t()
+    if rows.numel() < count * HYPER_ROW_FLOATS:
+        raise ValueError("rows holds fewer than count rows")
+    sched = None
+    if lr_per_step is not None:
+        sched = (ctypes.c_double * count)(*[float(x) for x in lr_per_step])
+    _check(_lib.pa_hyper_table_fill(_ptr(rows, torch.float32), int(first_step), int(count), sched,
+                                    float(lr), float(beta1), float(beta2), float(eps), float(wd),
+                                    _stream(stream)))
+
+
+def pa_adamw_step_packed_e4_multi_graph(entries, rows, nrows, index, status=None, nonfinite=None,
+                                        stream=None):
+    """Packed-E4 list step with the scalars of row index[0] of `rows`, then
+    index[0] += 1 on the device (capturable in a CUDA graph)."""
+    torch = _t()
+    arr = entries if isinstance(entries, ctypes.Array) else tensor_list(entries)
+    _check(_lib.pa_adamw_step_packed_e4_multi_graph(
+        arr, len(arr), _ptr(rows, torch.float32), int(nrows), _ptr(index, torch.int64),
+        _ptr(status, torch.int32) if status is not None else None, _ptr(nonfinite),
+        _stream(stream)))

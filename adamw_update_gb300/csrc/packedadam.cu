@@ -216,14 +216,14 @@ __device__ __forceinline__ void flush_nonfinite(uint32_t bad, unsigned long long
         atomicAdd(nonfinite, (unsigned long long)total);
 }
 
-// The persistent step kernel.  MULTI: walk the device descriptor table (each
+// The persistent step body.  MULTI: walk the device descriptor table (each
 // CTA visits chunks in increasing order, so the tensor index only moves
 // forward); otherwise the single descriptor passed by value.  U1: bc2 == 1.
 template <int MODE, bool MULTI, bool U1>
-__global__ void __launch_bounds__(kThreads, kMinBlocks)
-adamw_step_kernel(const Desc *__restrict__ table, int32_t ntensors, int64_t total_chunks,
-                  int64_t chunk, const Desc single, const Scalars s,
-                  unsigned long long *nonfinite)
+__device__ __forceinline__ void adamw_step_body(const Desc *__restrict__ table, int32_t ntensors,
+                                                int64_t total_chunks, int64_t chunk,
+                                                const Desc &single, const Scalars &s,
+                                                unsigned long long *nonfinite)
 {
     uint32_t bad = 0;
     int32_t t = 0;
@@ -248,6 +248,42 @@ adamw_step_kernel(const Desc *__restrict__ table, int32_t ntensors, int64_t tota
             scalar_chunk<MODE, U1>(d, k, chunk, s, bad);
     }
     flush_nonfinite(bad, nonfinite);
+}
+
+template <int MODE, bool MULTI, bool U1>
+__global__ void __launch_bounds__(kThreads, kMinBlocks)
+adamw_step_kernel(const Desc *__restrict__ table, int32_t ntensors, int64_t total_chunks,
+                  int64_t chunk, const Desc single, const Scalars s,
+                  unsigned long long *nonfinite)
+{
+    adamw_step_body<MODE, MULTI, U1>(table, ntensors, total_chunks, chunk, single, s, nonfinite);
+}
+
+// Graph-replayable variant: the scalars of the step are row *index of a
+// device table filled by the host ahead of time, so a captured launch needs no
+// host work per step.  An index outside [0, rows) sets *status to 1 and
+// skips the update (nothing is written).
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, kMinBlocks)
+adamw_step_table_kernel(const Desc *__restrict__ table, int32_t ntensors, int64_t total_chunks,
+                        int64_t chunk, const Scalars *__restrict__ rows, int32_t nrows,
+                        const int64_t *__restrict__ index, int32_t *status,
+                        unsigned long long *nonfinite)
+{
+    const int64_t i = *index;
+    if (i < 0 || i >= nrows) {
+        if (blockIdx.x == 0 && threadIdx.x == 0 && status != nullptr)
+            *status = 1;
+        return;
+    }
+    const Scalars s = rows[i];
+    Desc none = {};
+    adamw_step_body<MODE, true, false>(table, ntensors, total_chunks, chunk, none, s, nonfinite);
+}
+
+__global__ void advance_index_kernel(int64_t *index)
+{
+    *index += 1;
 }
 
 // ---- standalone codecs ("Packed AdamW Reference" README: inspect-formats) -------
@@ -1330,4 +1366,80 @@ extern "C" pa_status pa_adamw_step_packed_e4_host(float *p, const float *g, uint
         if ((e = cudaStreamWaitEvent(cs, hp->out_done[k], 0)) != cudaSuccess)
             return cuda_fail(e, "ordering the caller's stream after the host step");
     return ok();
+}
+
+// ===========================================================================
+// Graph-replayable packed-E4 tensor-list step
+// ===========================================================================
+static_assert(sizeof(pa_hyper) == sizeof(pa::Scalars), "pa_hyper mirrors the kernel scalars");
+
+extern "C" pa_status pa_hyper_table_fill(pa_hyper *rows, int64_t first_step, int32_t count,
+                                         const double *lr_per_step, double lr, double beta1,
+                                         double beta2, double eps, double wd, pa_stream stream)
+{
+    if (count < 0)
+        return fail(PA_ERR_ARG, "count must be >= 0 (got %d)", count);
+    if (count == 0)
+        return ok();
+    if (!rows)
+        return fail(PA_ERR_NULL, "rows is NULL with count = %d", count);
+    if (!aligned(rows, 16))
+        return fail(PA_ERR_ALIGN, "rows must be 16-byte aligned");
+    std::vector<Scalars> host((size_t)count);
+    for (int32_t k = 0; k < count; ++k) {
+        const double lrk = lr_per_step ? lr_per_step[k] : lr;
+        pa_status st = make_scalars(first_step + k, lrk, beta1, beta2, eps, wd, &host[(size_t)k]);
+        if (st != PA_OK)
+            return st;
+    }
+    // pageable source: the copy returns once the rows have been staged
+    cudaError_t e = cudaMemcpyAsync(rows, host.data(), (size_t)count * sizeof(Scalars),
+                                    cudaMemcpyHostToDevice, (cudaStream_t)stream);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "uploading the scalar rows");
+    return ok();
+}
+
+extern "C" pa_status pa_adamw_step_packed_e4_multi_graph(const pa_tensor *list, int32_t ntensors,
+                                                         const pa_hyper *rows, int32_t nrows,
+                                                         int64_t *index, int32_t *status,
+                                                         unsigned long long *nonfinite,
+                                                         pa_stream stream)
+{
+    if (ntensors < 0 || nrows < 0)
+        return fail(PA_ERR_ARG, "ntensors and nrows must be >= 0");
+    if (ntensors == 0)
+        return ok();
+    if (!list || !rows || !index)
+        return fail(PA_ERR_NULL, "list, rows and index must not be NULL");
+    if (!aligned(rows, 16) || !aligned(index, 8) || (status && !aligned(status, 4)))
+        return fail(PA_ERR_ALIGN, "rows must be 16-byte, index 8-byte, status 4-byte aligned");
+    pa_status st = check_counter(nonfinite);
+    if (st != PA_OK)
+        return st;
+    int64_t total = 0;
+    for (int32_t i = 0; i < ntensors; ++i) {
+        if ((st = check_tensor(list[i], pa::kE4, i)) != PA_OK)
+            return st;
+        total += list[i].n;
+    }
+    cudaStream_t cs = (cudaStream_t)stream;
+    if (total > 0) {
+        const Desc *table = nullptr;
+        int64_t chunks = 0, chunk = 0;
+        if ((st = chunk_size(kSlotE4Multi, total, &chunk)) != PA_OK)
+            return st;
+        if ((st = table_for(list, ntensors, pa::kE4, chunk, &table, &chunks)) != PA_OK)
+            return st;
+        int grid = 0;
+        if ((st = grid_for(kSlotE4Multi, chunks, &grid)) != PA_OK)
+            return st;
+        pa::adamw_step_table_kernel<pa::kE4><<<grid, pa::kThreads, 0, cs>>>(
+            table, ntensors, chunks, chunk, reinterpret_cast<const Scalars *>(rows), nrows,
+            index, status, nonfinite);
+        if ((st = check_launch("adamw_step_table_kernel launch")) != PA_OK)
+            return st;
+    }
+    pa::advance_index_kernel<<<1, 1, 0, cs>>>(index);
+    return check_launch("advance_index_kernel launch");
 }

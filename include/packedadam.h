@@ -230,6 +230,42 @@ pa_status pa_adamw_step_packed_e4_host(float *p, const float *g, uint32_t *state
                                        int64_t workspace_bytes, unsigned long long *nonfinite,
                                        pa_stream stream);
 
+/* ---------------------------------------------------------------------------
+ * Graph-replayable step.  pa_adamw_step_packed_e4_multi computes the step's
+ * scalars on the host at every call, so a CUDA graph that captured it would
+ * replay one step number forever.  Here the scalars come from a device table
+ * of rows filled ahead of time and a device-side row index that the call
+ * advances, so a captured call replays as consecutive steps with no host work.
+ *
+ * pa_hyper: the eight binary32 scalars of one step (formed as described at the
+ * top of this header): beta1, beta2, 1-beta1, 1-beta2, 1-beta2^step,
+ * lr/(1-beta1^step), 1-lr*wd, eps.
+ * pa_hyper_table_fill: compute rows for steps first_step .. first_step+count-1
+ *   and copy them to `rows` (device, 16-byte aligned, count entries) on
+ *   `stream`; lr_per_step (host, count doubles, nullable) gives a schedule,
+ *   otherwise `lr` is used for every row.  The host array is read during the
+ *   call only.
+ * pa_adamw_step_packed_e4_multi_graph: the packed E4 tensor-list step with the
+ *   scalars of row *index (index: device int64), then *index += 1 (a second,
+ *   one-thread launch on `stream`).  When *index is outside [0, nrows) nothing
+ *   is updated and *status (device int32, nullable) is set to 1; the index
+ *   still advances.  The list's descriptor table is made on the first call
+ *   with that list (a cudaMalloc); make that first call before capturing, so a
+ *   captured call finds it.  Results equal pa_adamw_step_packed_e4_multi at the
+ *   same step and hyperparameters, bit for bit.
+ * ------------------------------------------------------------------------- */
+typedef struct pa_hyper {
+    float b1, b2, c1, c2, bc2, ss, dk, ef;
+} pa_hyper;
+
+pa_status pa_hyper_table_fill(pa_hyper *rows, int64_t first_step, int32_t count,
+                              const double *lr_per_step, double lr, double beta1, double beta2,
+                              double eps, double wd, pa_stream stream);
+pa_status pa_adamw_step_packed_e4_multi_graph(const pa_tensor *list, int32_t ntensors,
+                                              const pa_hyper *rows, int32_t nrows, int64_t *index,
+                                              int32_t *status, unsigned long long *nonfinite,
+                                              pa_stream stream);
+
 /* Frees every cached descriptor table on every device (synchronises them). */
 pa_status pa_release_tables(void);
 
