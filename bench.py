@@ -65,6 +65,9 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle sample")
     ap.add_argument("--fast", action="store_true", help="use libpackedadam_fast.so")
+    ap.add_argument("--graph", action="store_true",
+                    help="packed E4: capture the step (device-indexed scalar rows) in a CUDA "
+                         "graph and time its replays")
     ap.add_argument("--params", type=int, default=None,
                     help="override the parameter count of a one-tensor workload (flat-7e9, "
                          "blockwise-1e9): the same distributions at another size, for profiling")
@@ -272,6 +275,33 @@ def step_fn(pa, w, hy, nonfinite):
     return run
 
 
+def graph_step_fn(pa, w, hy, nonfinite, nsteps):
+    """One step = one replay of a CUDA graph holding the device-indexed packed
+    E4 list step; the scalar rows of steps 1..nsteps are filled beforehand."""
+    import torch
+
+    if w.mode != "e4" or w.fresh_g is not None:
+        raise SystemExit("--graph applies to the packed-E4 workloads with a fixed gradient")
+    rows = torch.empty(nsteps * pa.HYPER_ROW_FLOATS, dtype=torch.float32, device=w.p.device)
+    pa.pa_hyper_table_fill(rows, 1, nsteps, **hy)
+    index = torch.zeros(1, dtype=torch.int64, device=w.p.device)
+    status = torch.zeros(1, dtype=torch.int32, device=w.p.device)
+    arr = w.tensor_array(pa)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # makes the descriptor table before capture
+        pa.pa_adamw_step_packed_e4_multi_graph(arr, rows, nsteps, index, status, nonfinite)
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        pa.pa_adamw_step_packed_e4_multi_graph(arr, rows, nsteps, index, status, nonfinite)
+    index.zero_()  # replays start again at step 1
+
+    def run(t):
+        graph.replay()
+    return run
+
+
 # ---------------------------------------------------------------------------
 # CPU oracle on a bounded sample of the workload
 # ---------------------------------------------------------------------------
@@ -402,6 +432,8 @@ def run_ours(args):
     hy = wl.HYPER
     nonfinite = torch.zeros(1, dtype=torch.int64, device=device)
     run = step_fn(lib, w, hy, nonfinite)
+    if args.graph:
+        run = graph_step_fn(lib, w, hy, nonfinite, args.warmup + args.steps + 2)
     stream = torch.cuda.current_stream()
     flush = None
     if w.bytes_per_step() < 4 * L2_BYTES:
@@ -483,6 +515,7 @@ def run_ours(args):
                       else f"inputs larger than L2 ({w.bytes_per_step() / 1e9:.1f} GB per step)",
                 "parallelism": f"{world} independent shards, no data-path collective",
                 "library": "libpackedadam_fast.so" if args.fast else "libpackedadam.so",
+                "launch": "CUDA graph replay" if args.graph else "C-ABI call per step",
             },
             "roofline": {
                 "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -492,7 +525,7 @@ def run_ours(args):
             },
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": args.steps,
+            "gpu_launches": args.steps * (2 if args.graph else 1),
             "clocks": clocks,
             "nonfinite": int(nonfinite.item()),
         }
