@@ -28,6 +28,7 @@ __all__ = [
     "pa_adamw_step_packed_fp16_multi", "pa_adamw_step_fp32_multi", "pa_release_tables",
     "shard_bounds", "pa_adamw_step_packed_e4_multi_noalloc", "pa_adamw_step_packed_e4_host",
     "pa_hyper_table_fill", "pa_adamw_step_packed_e4_multi_graph",
+    "pa_adamw_step_packed_e4_bf16g", "pa_adamw_step_packed_e4_multi_bf16g",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -206,18 +207,20 @@ def pa_adamw_step_blockwise8(p, g, p_bf16, m_code, m_absmax, v_code, v_absmax, q
 
 # ---- multi-tensor steps --------------------------------------------------------
 
-def tensor_list(entries, fp32: bool = False):
-    """ctypes pa_tensor array from (p, g, state) or (p, g, m, v) tuples."""
+def tensor_list(entries, fp32: bool = False, grad_dtype=None):
+    """ctypes pa_tensor array from (p, g, state) or (p, g, m, v) tuples;
+    grad_dtype: torch.float32 (default) or torch.bfloat16 for the *_bf16g calls."""
     torch = _t()
+    gd = torch.float32 if grad_dtype is None else grad_dtype
     arr = (PaTensor * len(entries))()
     for k, e in enumerate(entries):
         if fp32:
             p, g, m, v = e
-            arr[k] = PaTensor(_ptr(p, torch.float32), _ptr(g, torch.float32),
+            arr[k] = PaTensor(_ptr(p, torch.float32), _ptr(g, gd),
                               _ptr(m, torch.float32), _ptr(v, torch.float32), p.numel())
         else:
             p, g, s = e
-            arr[k] = PaTensor(_ptr(p, torch.float32), _ptr(g, torch.float32),
+            arr[k] = PaTensor(_ptr(p, torch.float32), _ptr(g, gd),
                               _ptr(s, torch.int32), None, p.numel())
     return arr
 
@@ -355,3 +358,33 @@ def pa_adamw_step_packed_e4_multi_graph(entries, rows, nrows, index, status=None
         arr, len(arr), _ptr(rows, torch.float32), int(nrows), _ptr(index, torch.int64),
         _ptr(status, torch.int32) if status is not None else None, _ptr(nonfinite),
         _stream(stream)))
+
+
+# ---- packed-E4 steps with bfloat16 gradients --------------------------------------
+
+_lib.pa_adamw_step_packed_e4_bf16g.restype = _i32
+_lib.pa_adamw_step_packed_e4_bf16g.argtypes = [_vp, _vp, _vp, _i64, *_HYP, _vp, _vp]
+_lib.pa_adamw_step_packed_e4_multi_bf16g.restype = _i32
+_lib.pa_adamw_step_packed_e4_multi_bf16g.argtypes = [ctypes.POINTER(PaTensor), _i32, *_HYP, _vp, _vp]
+
+
+def pa_adamw_step_packed_e4_bf16g(p, g, state, step, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8,
+                                  wd=0.0, nonfinite=None, stream=None):
+    """Packed-E4 step with a torch.bfloat16 gradient (widened exactly)."""
+    torch = _t()
+    _check(_lib.pa_adamw_step_packed_e4_bf16g(_ptr(p, torch.float32), _ptr(g, torch.bfloat16),
+                                              _ptr(state, torch.int32), p.numel(),
+                                              *_hyp(step, lr, beta1, beta2, eps, wd),
+                                              _ptr(nonfinite), _stream(stream)))
+
+
+def pa_adamw_step_packed_e4_multi_bf16g(entries, step, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8,
+                                        wd=0.0, nonfinite=None, stream=None):
+    """One launch over (p, g_bf16, state) tuples (or a tensor_list array made
+    with grad_dtype=torch.bfloat16)."""
+    torch = _t()
+    arr = entries if isinstance(entries, ctypes.Array) else \
+        tensor_list(entries, grad_dtype=torch.bfloat16)
+    _check(_lib.pa_adamw_step_packed_e4_multi_bf16g(arr, len(arr),
+                                                    *_hyp(step, lr, beta1, beta2, eps, wd),
+                                                    _ptr(nonfinite), _stream(stream)))

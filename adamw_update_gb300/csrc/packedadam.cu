@@ -72,6 +72,18 @@ struct Desc {
 __device__ __forceinline__ float4 load_stream(const float *a) { return __ldcs(reinterpret_cast<const float4 *>(a)); }
 __device__ __forceinline__ uint4 load_stream(const uint32_t *a) { return __ldcs(reinterpret_cast<const uint4 *>(a)); }
 __device__ __forceinline__ float4 load_readonly(const float *a) { return __ldg(reinterpret_cast<const float4 *>(a)); }
+// four bfloat16 gradients (8 bytes) widened exactly to binary32
+__device__ __forceinline__ float4 load_readonly(const __nv_bfloat16 *a)
+{
+    const uint2 r = __ldg(reinterpret_cast<const uint2 *>(a));
+    return make_float4(__uint_as_float(r.x << 16), __uint_as_float(r.x & 0xFFFF0000u),
+                       __uint_as_float(r.y << 16), __uint_as_float(r.y & 0xFFFF0000u));
+}
+__device__ __forceinline__ float load_grad(const float *g, int64_t i) { return __ldg(g + i); }
+__device__ __forceinline__ float load_grad(const __nv_bfloat16 *g, int64_t i)
+{
+    return __uint_as_float((uint32_t)__ldg(reinterpret_cast<const unsigned short *>(g) + i) << 16);
+}
 __device__ __forceinline__ void store_stream(float *a, float4 x) { __stcs(reinterpret_cast<float4 *>(a), x); }
 __device__ __forceinline__ void store_stream(uint32_t *a, uint4 x) { __stcs(reinterpret_cast<uint4 *>(a), x); }
 
@@ -94,12 +106,12 @@ __device__ __forceinline__ uint32_t packed_element(float &p, float g, uint32_t w
 }
 
 // Element i of tensor d with 4-byte accesses (heads, tails, unaligned tensors).
-template <int MODE, bool U1>
+template <int MODE, bool U1, typename GT = float>
 __device__ __forceinline__ void scalar_element(const Desc &d, int64_t i, const Scalars &s,
                                                uint32_t &bad)
 {
     float p = d.p[i];
-    const float g = __ldg(d.g + i);
+    const float g = load_grad(reinterpret_cast<const GT *>(d.g), i);
     if constexpr (MODE == kF32) {
         float *m = static_cast<float *>(d.s1);
         float *v = static_cast<float *>(d.s2);
@@ -121,7 +133,7 @@ __device__ __forceinline__ void scalar_element(const Desc &d, int64_t i, const S
 // thread issues all of its 16-byte loads (kUnroll vectors of p, g and the
 // state) before any arithmetic; the per-thread pointers are set up once per
 // chunk and advanced by a constant per wave.
-template <int MODE, bool U1>
+template <int MODE, bool U1, typename GT = float>
 __device__ __forceinline__ void vector_chunk(const Desc &d, int64_t k, int64_t chunk,
                                              const Scalars &s, uint32_t &bad)
 {
@@ -129,11 +141,11 @@ __device__ __forceinline__ void vector_chunk(const Desc &d, int64_t k, int64_t c
     const int64_t nb = d.n - d.head;
     int64_t base = k * chunk;
     if (k == 0 && tid < d.head)
-        scalar_element<MODE, U1>(d, tid, s, bad);
+        scalar_element<MODE, U1, GT>(d, tid, s, bad);
     const int64_t end = base + chunk < nb ? base + chunk : nb;
     const int64_t off = d.head + base + 4 * tid;
     float *P = d.p + off;
-    const float *G = d.g + off;
+    const GT *G = reinterpret_cast<const GT *>(d.g) + off;
     uint32_t *W = static_cast<uint32_t *>(d.s1) + off;   // packed modes
     float *M = static_cast<float *>(d.s1) + off;         // FP32 mode
     float *V = static_cast<float *>(d.s2) + off;
@@ -189,14 +201,14 @@ __device__ __forceinline__ void vector_chunk(const Desc &d, int64_t k, int64_t c
                 // the one vector that straddles the end of the tensor
                 const int64_t e = base + 4 * ((int64_t)u * kThreads + tid);
                 for (int64_t i = e; i < nb; ++i)
-                    scalar_element<MODE, U1>(d, d.head + i, s, bad);
+                    scalar_element<MODE, U1, GT>(d, d.head + i, s, bad);
             }
         }
     }
 }
 
 // Chunk k of a 4-byte-path tensor: elements [k*chunk, (k+1)*chunk).
-template <int MODE, bool U1>
+template <int MODE, bool U1, typename GT = float>
 __device__ __forceinline__ void scalar_chunk(const Desc &d, int64_t k, int64_t chunk,
                                              const Scalars &s, uint32_t &bad)
 {
@@ -204,7 +216,7 @@ __device__ __forceinline__ void scalar_chunk(const Desc &d, int64_t k, int64_t c
     const int64_t end = base + chunk < d.n ? base + chunk : d.n;
 #pragma unroll 4
     for (int64_t i = base + threadIdx.x; i < end; i += kThreads)
-        scalar_element<MODE, U1>(d, i, s, bad);
+        scalar_element<MODE, U1, GT>(d, i, s, bad);
 }
 
 __device__ __forceinline__ void flush_nonfinite(uint32_t bad, unsigned long long *nonfinite)
@@ -219,7 +231,7 @@ __device__ __forceinline__ void flush_nonfinite(uint32_t bad, unsigned long long
 // The persistent step body.  MULTI: walk the device descriptor table (each
 // CTA visits chunks in increasing order, so the tensor index only moves
 // forward); otherwise the single descriptor passed by value.  U1: bc2 == 1.
-template <int MODE, bool MULTI, bool U1>
+template <int MODE, bool MULTI, bool U1, typename GT = float>
 __device__ __forceinline__ void adamw_step_body(const Desc *__restrict__ table, int32_t ntensors,
                                                 int64_t total_chunks, int64_t chunk,
                                                 const Desc &single, const Scalars &s,
@@ -243,20 +255,21 @@ __device__ __forceinline__ void adamw_step_body(const Desc *__restrict__ table, 
         }
         const int64_t k = c - d.chunk0;
         if (d.vec)
-            vector_chunk<MODE, U1>(d, k, chunk, s, bad);
+            vector_chunk<MODE, U1, GT>(d, k, chunk, s, bad);
         else
-            scalar_chunk<MODE, U1>(d, k, chunk, s, bad);
+            scalar_chunk<MODE, U1, GT>(d, k, chunk, s, bad);
     }
     flush_nonfinite(bad, nonfinite);
 }
 
-template <int MODE, bool MULTI, bool U1>
+template <int MODE, bool MULTI, bool U1, typename GT = float>
 __global__ void __launch_bounds__(kThreads, kMinBlocks)
 adamw_step_kernel(const Desc *__restrict__ table, int32_t ntensors, int64_t total_chunks,
                   int64_t chunk, const Desc single, const Scalars s,
                   unsigned long long *nonfinite)
 {
-    adamw_step_body<MODE, MULTI, U1>(table, ntensors, total_chunks, chunk, single, s, nonfinite);
+    adamw_step_body<MODE, MULTI, U1, GT>(table, ntensors, total_chunks, chunk, single, s,
+                                         nonfinite);
 }
 
 // Graph-replayable variant: the scalars of the step are row *index of a
@@ -726,20 +739,26 @@ pa_status check_launch(const char *what)
 // Fill d for one tensor; returns its chunk count.  The 16-byte path needs p, g
 // and the state (and v in FP32 mode) to share their address modulo 16; the
 // head peels the elements before the first 16-byte boundary.
-int64_t describe(const pa_tensor &t, int mode, int64_t chunk, Desc *d)
+int64_t describe(const pa_tensor &t, int mode, int64_t chunk, Desc *d, int grad_bytes = 4)
 {
     d->p = t.p;
     d->g = t.g;
     d->s1 = t.state;
     d->s2 = t.state2;
     d->n = t.n;
-    const uintptr_t ph = reinterpret_cast<uintptr_t>(t.p) & 15u;
-    bool same = (reinterpret_cast<uintptr_t>(t.g) & 15u) == ph &&
-                (reinterpret_cast<uintptr_t>(t.state) & 15u) == ph;
+    // element phase within a 4-element vector: all streams must agree for the
+    // vector path (p and the state are 4-byte elements, g 4 or 2 bytes)
+    const uintptr_t ph = (reinterpret_cast<uintptr_t>(t.p) >> 2) & 3u;
+    const uintptr_t gph = (reinterpret_cast<uintptr_t>(t.g) / (uintptr_t)grad_bytes) & 3u;
+    bool same = gph == ph && (reinterpret_cast<uintptr_t>(t.p) & 3u) == 0 &&
+                (reinterpret_cast<uintptr_t>(t.p) & 15u) == 4 * ph &&
+                (reinterpret_cast<uintptr_t>(t.g) & (uintptr_t)(4 * grad_bytes - 1)) ==
+                    (uintptr_t)grad_bytes * gph &&
+                (reinterpret_cast<uintptr_t>(t.state) & 15u) == 4 * ph;
     if (mode == pa::kF32)
-        same = same && (reinterpret_cast<uintptr_t>(t.state2) & 15u) == ph;
+        same = same && (reinterpret_cast<uintptr_t>(t.state2) & 15u) == 4 * ph;
     d->vec = same ? 1 : 0;
-    int64_t head = same ? (int64_t)(((16u - ph) & 15u) / 4u) : 0;
+    int64_t head = same ? (int64_t)((4u - ph) & 3u) : 0;
     if (head > t.n)
         head = t.n;
     d->head = (int32_t)head;
@@ -750,7 +769,7 @@ int64_t describe(const pa_tensor &t, int mode, int64_t chunk, Desc *d)
     return chunks > 0 ? chunks : 1;
 }
 
-pa_status check_tensor(const pa_tensor &t, int mode, int index)
+pa_status check_tensor(const pa_tensor &t, int mode, int index, uintptr_t grad_align = 4)
 {
     if (t.n < 0)
         return fail(PA_ERR_ARG, "tensor %d: n must be >= 0 (got %lld)", index, (long long)t.n);
@@ -758,9 +777,10 @@ pa_status check_tensor(const pa_tensor &t, int mode, int index)
         return PA_OK;
     if (!t.p || !t.g || !t.state || (mode == pa::kF32 && !t.state2))
         return fail(PA_ERR_NULL, "tensor %d: NULL pointer with n = %lld", index, (long long)t.n);
-    if (!aligned(t.p, 4) || !aligned(t.g, 4) || !aligned(t.state, 4) ||
+    if (!aligned(t.p, 4) || !aligned(t.g, grad_align) || !aligned(t.state, 4) ||
         (mode == pa::kF32 && !aligned(t.state2, 4)))
-        return fail(PA_ERR_ALIGN, "tensor %d: pointers must be 4-byte aligned", index);
+        return fail(PA_ERR_ALIGN, "tensor %d: pointers must be aligned to their element size",
+                    index);
     return PA_OK;
 }
 
@@ -771,7 +791,7 @@ pa_status check_counter(const unsigned long long *nonfinite)
     return PA_OK;
 }
 
-template <int MODE>
+template <int MODE, typename GT = float>
 pa_status step_single(const pa_tensor &t, int64_t step, double lr, double beta1, double beta2,
                       double eps, double wd, unsigned long long *nonfinite, pa_stream stream)
 {
@@ -779,7 +799,8 @@ pa_status step_single(const pa_tensor &t, int64_t step, double lr, double beta1,
     pa_status st = make_scalars(step, lr, beta1, beta2, eps, wd, &s);
     if (st != PA_OK)
         return st;
-    if ((st = check_tensor(t, MODE, 0)) != PA_OK || (st = check_counter(nonfinite)) != PA_OK)
+    if ((st = check_tensor(t, MODE, 0, sizeof(GT))) != PA_OK ||
+        (st = check_counter(nonfinite)) != PA_OK)
         return st;
     if (t.n == 0)
         return ok();
@@ -787,16 +808,16 @@ pa_status step_single(const pa_tensor &t, int64_t step, double lr, double beta1,
     int64_t chunk = 0;
     if ((st = chunk_size(MODE, t.n, &chunk)) != PA_OK)
         return st;
-    const int64_t chunks = describe(t, MODE, chunk, &d);
+    const int64_t chunks = describe(t, MODE, chunk, &d, (int)sizeof(GT));
     d.chunk0 = 0;
     int grid = 0;
     if ((st = grid_for(MODE, chunks, &grid)) != PA_OK)
         return st;
     if (s.bc2 == 1.0f)
-        pa::adamw_step_kernel<MODE, false, true><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
+        pa::adamw_step_kernel<MODE, false, true, GT><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
             nullptr, 1, chunks, chunk, d, s, nonfinite);
     else
-        pa::adamw_step_kernel<MODE, false, false><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
+        pa::adamw_step_kernel<MODE, false, false, GT><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
             nullptr, 1, chunks, chunk, d, s, nonfinite);
     return check_launch("adamw_step_kernel launch");
 }
@@ -809,6 +830,7 @@ pa_status step_single(const pa_tensor &t, int64_t step, double lr, double beta1,
 struct Table {
     int device;
     int mode;
+    int grad_bytes;
     int64_t chunk;
     std::vector<Desc> host;
     Desc *dev;
@@ -822,12 +844,12 @@ uint64_t g_tick = 0;
 constexpr size_t kMaxTables = 64;
 
 pa_status table_for(const pa_tensor *list, int32_t ntensors, int mode, int64_t chunk,
-                    const Desc **dev_table, int64_t *chunks)
+                    const Desc **dev_table, int64_t *chunks, int grad_bytes = 4)
 {
     std::vector<Desc> host((size_t)ntensors);
     int64_t total = 0;
     for (int32_t i = 0; i < ntensors; ++i) {
-        const int64_t c = describe(list[i], mode, chunk, &host[(size_t)i]);
+        const int64_t c = describe(list[i], mode, chunk, &host[(size_t)i], grad_bytes);
         host[(size_t)i].chunk0 = total;
         total += c;
     }
@@ -838,7 +860,8 @@ pa_status table_for(const pa_tensor *list, int32_t ntensors, int mode, int64_t c
     std::lock_guard<std::mutex> lock(g_tab_mu);
     ++g_tick;
     for (Table &t : g_tables) {
-        if (t.device == dev && t.mode == mode && t.chunk == chunk && t.host.size() == host.size() &&
+        if (t.device == dev && t.mode == mode && t.grad_bytes == grad_bytes && t.chunk == chunk &&
+            t.host.size() == host.size() &&
             std::memcmp(t.host.data(), host.data(), host.size() * sizeof(Desc)) == 0) {
             t.last_use = g_tick;
             *dev_table = t.dev;
@@ -860,6 +883,7 @@ pa_status table_for(const pa_tensor *list, int32_t ntensors, int mode, int64_t c
     Table t;
     t.device = dev;
     t.mode = mode;
+    t.grad_bytes = grad_bytes;
     t.chunk = chunk;
     t.chunks = total;
     t.last_use = g_tick;
@@ -884,7 +908,7 @@ pa_status table_for(const pa_tensor *list, int32_t ntensors, int mode, int64_t c
     return PA_OK;
 }
 
-template <int MODE>
+template <int MODE, typename GT = float>
 pa_status step_multi(const pa_tensor *list, int32_t ntensors, int64_t step, double lr,
                      double beta1, double beta2, double eps, double wd,
                      unsigned long long *nonfinite, pa_stream stream)
@@ -903,7 +927,7 @@ pa_status step_multi(const pa_tensor *list, int32_t ntensors, int64_t step, doub
         return st;
     int64_t total = 0;
     for (int32_t i = 0; i < ntensors; ++i) {
-        if ((st = check_tensor(list[i], MODE, i)) != PA_OK)
+        if ((st = check_tensor(list[i], MODE, i, sizeof(GT))) != PA_OK)
             return st;
         total += list[i].n;
     }
@@ -913,7 +937,7 @@ pa_status step_multi(const pa_tensor *list, int32_t ntensors, int64_t step, doub
     int64_t chunks = 0, chunk = 0;
     if ((st = chunk_size(MODE + 3, total, &chunk)) != PA_OK)
         return st;
-    if ((st = table_for(list, ntensors, MODE, chunk, &table, &chunks)) != PA_OK)
+    if ((st = table_for(list, ntensors, MODE, chunk, &table, &chunks, (int)sizeof(GT))) != PA_OK)
         return st;
     int grid = 0;
     if ((st = grid_for(MODE + 3, chunks, &grid)) != PA_OK)
@@ -921,10 +945,10 @@ pa_status step_multi(const pa_tensor *list, int32_t ntensors, int64_t step, doub
     Desc none;
     std::memset(&none, 0, sizeof none);
     if (s.bc2 == 1.0f)
-        pa::adamw_step_kernel<MODE, true, true><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
+        pa::adamw_step_kernel<MODE, true, true, GT><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
             table, ntensors, chunks, chunk, none, s, nonfinite);
     else
-        pa::adamw_step_kernel<MODE, true, false><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
+        pa::adamw_step_kernel<MODE, true, false, GT><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
             table, ntensors, chunks, chunk, none, s, nonfinite);
     return check_launch("adamw_step_kernel (multi) launch");
 }
@@ -1442,4 +1466,28 @@ extern "C" pa_status pa_adamw_step_packed_e4_multi_graph(const pa_tensor *list, 
     }
     pa::advance_index_kernel<<<1, 1, 0, cs>>>(index);
     return check_launch("advance_index_kernel launch");
+}
+
+// ===========================================================================
+// Packed-E4 steps that read bfloat16 gradients
+// ===========================================================================
+extern "C" pa_status pa_adamw_step_packed_e4_bf16g(float *p, const uint16_t *g, uint32_t *state,
+                                                   int64_t n, int64_t step, double lr,
+                                                   double beta1, double beta2, double eps,
+                                                   double wd, unsigned long long *nonfinite,
+                                                   pa_stream stream)
+{
+    const pa_tensor t = {p, reinterpret_cast<const float *>(g), state, nullptr, n};
+    return step_single<pa::kE4, __nv_bfloat16>(t, step, lr, beta1, beta2, eps, wd, nonfinite,
+                                                stream);
+}
+
+extern "C" pa_status pa_adamw_step_packed_e4_multi_bf16g(const pa_tensor *list, int32_t ntensors,
+                                                         int64_t step, double lr, double beta1,
+                                                         double beta2, double eps, double wd,
+                                                         unsigned long long *nonfinite,
+                                                         pa_stream stream)
+{
+    return step_multi<pa::kE4, __nv_bfloat16>(list, ntensors, step, lr, beta1, beta2, eps, wd,
+                                              nonfinite, stream);
 }

@@ -65,6 +65,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle sample")
     ap.add_argument("--fast", action="store_true", help="use libpackedadam_fast.so")
+    ap.add_argument("--grad", default="fp32", choices=["fp32", "bf16"],
+                    help="gradient dtype of the packed-E4 step (bf16: 18 bytes per parameter)")
     ap.add_argument("--graph", action="store_true",
                     help="packed E4: capture the step (device-indexed scalar rows) in a CUDA "
                          "graph and time its replays")
@@ -235,11 +237,15 @@ class Workload:
         else:
             self.s = [torch.zeros(n, dtype=torch.int32, device=device)]
         self.fresh_g = None
+        self.grad_bf16 = False
         if name == "single-4096":  # the workload draws g afresh every step
             self.fresh_g = []
 
+    def bytes_per_param(self):
+        return BYTES_PER_PARAM[self.mode] - (2 if self.grad_bf16 else 0)
+
     def bytes_per_step(self):
-        return BYTES_PER_PARAM[self.mode] * self.n
+        return self.bytes_per_param() * self.n
 
     def tensor_array(self, pa, g=None):
         g = self.g if g is None else g
@@ -247,7 +253,10 @@ class Workload:
         ents = []
         for a, b in zip(offs[:-1], offs[1:]):
             ents.append((self.p[a:b], g[a:b], *[s[a:b] for s in self.s]))
-        return pa.tensor_list(ents, fp32=self.mode == "fp32")
+        import torch
+
+        return pa.tensor_list(ents, fp32=self.mode == "fp32",
+                              grad_dtype=torch.bfloat16 if self.grad_bf16 else None)
 
 
 def step_fn(pa, w, hy, nonfinite):
@@ -261,6 +270,8 @@ def step_fn(pa, w, hy, nonfinite):
         return run
     fn = {"e4": pa.pa_adamw_step_packed_e4_multi, "fp16": pa.pa_adamw_step_packed_fp16_multi,
           "fp32": pa.pa_adamw_step_fp32_multi}[w.mode]
+    if w.grad_bf16:
+        fn = pa.pa_adamw_step_packed_e4_multi_bf16g
     arrays = [w.tensor_array(pa)]
     if w.fresh_g is not None:
         arrays = []
@@ -280,8 +291,8 @@ def graph_step_fn(pa, w, hy, nonfinite, nsteps):
     E4 list step; the scalar rows of steps 1..nsteps are filled beforehand."""
     import torch
 
-    if w.mode != "e4" or w.fresh_g is not None:
-        raise SystemExit("--graph applies to the packed-E4 workloads with a fixed gradient")
+    if w.mode != "e4" or w.fresh_g is not None or w.grad_bf16:
+        raise SystemExit("--graph applies to the packed-E4 workloads with a fixed FP32 gradient")
     rows = torch.empty(nsteps * pa.HYPER_ROW_FLOATS, dtype=torch.float32, device=w.p.device)
     pa.pa_hyper_table_fill(rows, 1, nsteps, **hy)
     index = torch.zeros(1, dtype=torch.int64, device=w.p.device)
@@ -384,7 +395,7 @@ def host_sample(w, s):
                   w.m_absmax[:nb].cpu().numpy(), w.v_code[:s].cpu().numpy(),
                   w.v_absmax[:nb].cpu().numpy()]
         return arrays, (w.q1.cpu().numpy(), w.q2.cpu().numpy())
-    arrays = [w.p[:s].cpu().numpy(), w.g[:s].cpu().numpy()]
+    arrays = [w.p[:s].cpu().numpy(), w.g[:s].float().cpu().numpy()]  # bf16 widens exactly
     for st in w.s:
         a = st[:s].cpu().numpy()
         arrays.append(a.view(np.uint32) if a.dtype == np.int32 else a)
@@ -431,6 +442,11 @@ def run_ours(args):
     w = Workload(args.workload, args.mode, device, seed=1234 + rank)
     hy = wl.HYPER
     nonfinite = torch.zeros(1, dtype=torch.int64, device=device)
+    if args.grad == "bf16":
+        if w.mode != "e4":
+            raise SystemExit("--grad bf16 applies to the packed-E4 mode")
+        w.g = w.g.to(torch.bfloat16)
+        w.grad_bf16 = True
     run = step_fn(lib, w, hy, nonfinite)
     if args.graph:
         run = graph_step_fn(lib, w, hy, nonfinite, args.warmup + args.steps + 2)
@@ -490,9 +506,9 @@ def run_ours(args):
 
     if rank == 0:
         peak, peak_kind = measured_peak()
-        bpp = BYTES_PER_PARAM[w.mode]
+        bpp = w.bytes_per_param()
         achieved = bpp * w.n / (kernel_ms / 1e3) / 1e9
-        traffic = traffic_per_param(w.mode)
+        traffic = None if w.grad_bf16 else traffic_per_param(w.mode)
         line = {
             "metric": "packed-E4 AdamW step: params/s and HBM GB/s as % of GB300 peak, 1 GPU"
                       if w.mode == "e4" else f"{w.mode} AdamW step: params/s and HBM GB/s",
@@ -515,6 +531,7 @@ def run_ours(args):
                       else f"inputs larger than L2 ({w.bytes_per_step() / 1e9:.1f} GB per step)",
                 "parallelism": f"{world} independent shards, no data-path collective",
                 "library": "libpackedadam_fast.so" if args.fast else "libpackedadam.so",
+                "grad": args.grad,
                 "launch": "CUDA graph replay" if args.graph else "C-ABI call per step",
             },
             "roofline": {
@@ -561,7 +578,7 @@ def measure_e2e(pa, w, hy, args, stream, nonfinite):
         host[id(t)].copy_(t)
     h2d = sum(t.numel() * t.element_size() for t in dev_in)
     d2h = sum(t.numel() * t.element_size() for t in dev_out)
-    if w.mode == "e4" and len(w.sizes) == 1:
+    if w.mode == "e4" and len(w.sizes) == 1 and not w.grad_bf16:
         ws = torch.empty(3 * 12 * (1 << 26), dtype=torch.uint8, device=w.p.device)
         hp, hg, hs = host[id(w.p)], host[id(w.g)], host[id(w.s[0])]
         api = "pa_adamw_step_packed_e4_host (pinned host tensors, 2.4 GB workspace)"

@@ -231,6 +231,22 @@ pa_status pa_adamw_step_packed_e4_host(float *p, const float *g, uint32_t *state
                                        pa_stream stream);
 
 /* ---------------------------------------------------------------------------
+ * Packed-E4 steps whose gradient is bfloat16 (uint16 bit patterns, 2-byte
+ * aligned), as produced by mixed-precision backward passes: each gradient is
+ * widened exactly to binary32 and the step is the packed E4 step above, bit for
+ * bit.  The gradient costs 2 bytes instead of 4: 18 bytes per parameter.
+ * pa_adamw_step_packed_e4_multi_bf16g reads list[t].g as a uint16 pointer.
+ * ------------------------------------------------------------------------- */
+pa_status pa_adamw_step_packed_e4_bf16g(float *p, const uint16_t *g, uint32_t *state, int64_t n,
+                                        int64_t step, double lr, double beta1, double beta2,
+                                        double eps, double wd, unsigned long long *nonfinite,
+                                        pa_stream stream);
+pa_status pa_adamw_step_packed_e4_multi_bf16g(const pa_tensor *list, int32_t ntensors,
+                                              int64_t step, double lr, double beta1, double beta2,
+                                              double eps, double wd, unsigned long long *nonfinite,
+                                              pa_stream stream);
+
+/* ---------------------------------------------------------------------------
  * Graph-replayable step.  pa_adamw_step_packed_e4_multi computes the step's
  * scalars on the host at every call, so a CUDA graph that captured it would
  * replay one step number forever.  Here the scalars come from a device table
