@@ -347,13 +347,12 @@ decode_state_kernel(const uint32_t *__restrict__ word, float *__restrict__ m,
 //    reciprocal and nothing under- or overflows; here |x| <= scale, so that
 //    holds for |x| >= 2^-100; zeros keep their sign by an OR of the sign bit;
 //    other |x| < 2^-100 use the IEEE divide.
-//  * Search.  A per-CTA table splits [-2, 2) into 4096 buckets on the
-//    order-preserving integer image of a binary32 (sign-magnitude flipped),
-//    2^19 consecutive values each; an entry holds the number of midpoints
-//    below the bucket's first value and how many midpoints fall inside the
-//    bucket.  The code is that count plus one comparison per midpoint inside
-//    c's bucket -- exact for any ascending map; for the log-linear maps a
-//    bucket rarely holds more than one midpoint.
+//  * Search.  A per-CTA table indexed by the top 14 bits of c's binary32
+//    pattern (32 buckets per binade, either sign) holds the number of
+//    midpoints below every value of the bucket; the code is that count plus K
+//    comparisons with the following midpoints, K the largest number of
+//    midpoints in one bucket (uniform over the CTA, so no divergence) -- exact
+//    for any ascending map; K = 1 for the log-linear maps.
 //  * A block whose scale is NaN, infinite or outside [2^-100, 2^100) takes
 //    the IEEE divide and an 8-step binary search over the midpoints.
 // Rare path: requantise a thread's 8 values with the IEEE divide and the
@@ -386,7 +385,7 @@ struct BlockwiseArgs {
 
 struct BlockwiseShared {
     float q1[256], q2[256], mid1[512], mid2[512];  // midpoints padded with +Inf
-    uint16_t bucket1[kBuckets], bucket2[kBuckets];
+    uint8_t bucket1[kBuckets], bucket2[kBuckets];
     uint32_t warp_max[2][2][kThreads / 32];  // [iteration parity][m, v][warp]
     uint32_t red[2][32];
 };
@@ -417,7 +416,7 @@ __device__ __noinline__ uint2 requantise_fixup(float x0, float x1, float x2, flo
 // redone in a fix-up pass that is rarely entered.
 template <int K>
 __device__ __forceinline__ uint2 requantise_fast(const float *x, uint32_t sb, const float *mid,
-                                                 const uint16_t *table, int k)
+                                                 const uint8_t *table, int k)
 {
     const float scale = __uint_as_float(sb), y = __frcp_rn(scale);
     const uint32_t floor = fast_quotient_floor(sb);

@@ -210,6 +210,7 @@ class Workload:
         import torch
 
         self.name, self.mode = name, mode
+        self.grad_bf16 = False
         self.sizes = tensor_sizes(name)
         self.n = sum(self.sizes)
         n = self.n
@@ -237,7 +238,6 @@ class Workload:
         else:
             self.s = [torch.zeros(n, dtype=torch.int32, device=device)]
         self.fresh_g = None
-        self.grad_bf16 = False
         if name == "single-4096":  # the workload draws g afresh every step
             self.fresh_g = []
 

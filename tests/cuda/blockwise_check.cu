@@ -17,11 +17,11 @@ __device__ void note(unsigned long long *count, uint32_t *first, uint32_t a, uin
     }
 }
 
-// every c in [-1, 1]: ordered keys from ordered_bits(-1) to ordered_bits(1)
+// every c in [-1, 1]: both signs, every binary32 pattern of magnitude <= 1
 __global__ void search_all(const float *qmap, unsigned long long *count, uint32_t *first)
 {
     __shared__ float q[256], mid[512];
-    __shared__ uint16_t table[kBuckets];
+    __shared__ uint8_t table[kBuckets];
     __shared__ uint32_t red[32];
     const int tid = threadIdx.x;
     q[tid] = qmap[tid];
@@ -31,10 +31,10 @@ __global__ void search_all(const float *qmap, unsigned long long *count, uint32_
     __syncthreads();
     const int k = build_buckets(mid, table, red);
     __syncthreads();
-    const uint32_t k_lo = ordered_bits(-1.0f), k_hi = ordered_bits(1.0f);
-    const uint64_t span = (uint64_t)(k_hi - k_lo) + 1;
-    for (uint64_t i = blockIdx.x * (uint64_t)blockDim.x + tid; i < span; i += (uint64_t)gridDim.x * blockDim.x) {
-        const float c = from_ordered_bits(k_lo + (uint32_t)i);
+    const uint64_t half = (uint64_t)0x3F800000u + 1;  // magnitudes 0 .. 1.0
+    for (uint64_t i = blockIdx.x * (uint64_t)blockDim.x + tid; i < 2 * half; i += (uint64_t)gridDim.x * blockDim.x) {
+        const uint32_t bits = i < half ? (uint32_t)i : 0x80000000u | (uint32_t)(i - half);
+        const float c = __uint_as_float(bits);
         const uint32_t got = k <= 2 ? code_by_bucket<2>(mid, table, c, k) : code_by_bucket<0>(mid, table, c, k);
         const uint32_t want = (uint32_t)count_below(mid, c);
         if (got != want)
