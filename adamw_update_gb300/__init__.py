@@ -28,7 +28,7 @@ __all__ = [
     "pa_adamw_step_packed_fp16_multi", "pa_adamw_step_fp32_multi", "pa_release_tables",
     "shard_bounds", "pa_adamw_step_packed_e4_multi_noalloc", "pa_adamw_step_packed_e4_host",
     "pa_hyper_table_fill", "pa_adamw_step_packed_e4_multi_graph",
-    "pa_adamw_step_packed_e4_bf16g", "pa_adamw_step_packed_e4_multi_bf16g",
+    "pa_adamw_step_packed_e4_bf16g", "pa_adamw_step_packed_e4_multi_bf16g", "pa_shutdown",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -253,6 +253,14 @@ def pa_adamw_step_fp32_multi(entries, step, lr=1e-3, beta1=0.9, beta2=0.999, eps
 
 def pa_release_tables():
     _check(_lib.pa_release_tables())
+
+
+_lib.pa_shutdown.restype = _i32
+_lib.pa_shutdown.argtypes = []
+
+
+def pa_shutdown():
+    _check(_lib.pa_shutdown())
 
 
 # ---- sharding of a flattened parameter space ------------------------------------

@@ -1127,6 +1127,12 @@ pa_status pa_adamw_step_blockwise8(const float *p, const float *g, uint16_t *p_b
     return check_launch("blockwise8_kernel launch");
 }
 
+pa_status pa_shutdown(void)
+{
+    // the cached descriptor tables; the host-step streams and events live until exit
+    return pa_release_tables();
+}
+
 pa_status pa_release_tables(void)
 {
     std::lock_guard<std::mutex> lock(g_tab_mu);

@@ -285,6 +285,11 @@ pa_status pa_adamw_step_packed_e4_multi_graph(const pa_tensor *list, int32_t nte
 /* Frees every cached descriptor table on every device (synchronises them). */
 pa_status pa_release_tables(void);
 
+/* Releases what the library holds on the devices (the cached descriptor
+ * tables); call it before unloading the library.  Later calls recreate what
+ * they need. */
+pa_status pa_shutdown(void);
+
 #ifdef __cplusplus
 }
 #endif
