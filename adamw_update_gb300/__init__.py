@@ -29,6 +29,7 @@ __all__ = [
     "shard_bounds", "pa_adamw_step_packed_e4_multi_noalloc", "pa_adamw_step_packed_e4_host",
     "pa_hyper_table_fill", "pa_adamw_step_packed_e4_multi_graph",
     "pa_adamw_step_packed_e4_bf16g", "pa_adamw_step_packed_e4_multi_bf16g", "pa_shutdown",
+    "pa_adamw_step_blockwise8_multi",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -396,3 +397,41 @@ def pa_adamw_step_packed_e4_multi_bf16g(entries, step, lr=1e-3, beta1=0.9, beta2
     _check(_lib.pa_adamw_step_packed_e4_multi_bf16g(arr, len(arr),
                                                     *_hyp(step, lr, beta1, beta2, eps, wd),
                                                     _ptr(nonfinite), _stream(stream)))
+
+
+# ---- blockwise tensor-list step ----------------------------------------------------
+
+class PaBlockwiseTensor(ctypes.Structure):
+    """pa_blockwise_tensor: p, g, p_bf16, m_code, m_absmax, v_code, v_absmax, n."""
+    _fields_ = [("p", ctypes.c_void_p), ("g", ctypes.c_void_p), ("p_bf16", ctypes.c_void_p),
+                ("m_code", ctypes.c_void_p), ("m_absmax", ctypes.c_void_p),
+                ("v_code", ctypes.c_void_p), ("v_absmax", ctypes.c_void_p), ("n", ctypes.c_int64)]
+
+
+_lib.pa_adamw_step_blockwise8_multi.restype = _i32
+_lib.pa_adamw_step_blockwise8_multi.argtypes = [ctypes.POINTER(PaBlockwiseTensor), _i32, _vp, _vp,
+                                                *_HYP, _vp, _vp]
+
+
+def blockwise_list(entries):
+    """ctypes pa_blockwise_tensor array from (p, g, p_bf16, m_code, m_absmax,
+    v_code, v_absmax) tuples of CUDA tensors."""
+    torch = _t()
+    arr = (PaBlockwiseTensor * len(entries))()
+    for k, (p, g, pb, mc, ma, vc, va) in enumerate(entries):
+        arr[k] = PaBlockwiseTensor(_ptr(p, torch.float32), _ptr(g, torch.float32),
+                                   _ptr(pb, torch.bfloat16), _ptr(mc, torch.uint8),
+                                   _ptr(ma, torch.float32), _ptr(vc, torch.uint8),
+                                   _ptr(va, torch.float32), p.numel())
+    return arr
+
+
+def pa_adamw_step_blockwise8_multi(entries, qmap1, qmap2, step, lr=1e-3, beta1=0.9, beta2=0.999,
+                                   eps=1e-8, wd=0.01, nonfinite=None, stream=None):
+    """One launch of the blockwise step over a list of tensors."""
+    torch = _t()
+    arr = entries if isinstance(entries, ctypes.Array) else blockwise_list(entries)
+    _check(_lib.pa_adamw_step_blockwise8_multi(arr, len(arr), _ptr(qmap1, torch.float32),
+                                               _ptr(qmap2, torch.float32),
+                                               *_hyp(step, lr, beta1, beta2, eps, wd),
+                                               _ptr(nonfinite), _stream(stream)))

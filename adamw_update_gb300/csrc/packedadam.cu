@@ -557,12 +557,11 @@ __device__ __forceinline__ void blockwise_block(const BlockwiseArgs &a, Blockwis
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 4)
-blockwise8_kernel(const BlockwiseArgs a, const float *__restrict__ qmap1,
-                  const float *__restrict__ qmap2, int64_t nblocks, const Scalars s,
-                  unsigned long long *nonfinite)
+// Per-CTA set-up: maps, midpoints (+Inf padded) and the two bucket tables;
+// returns the largest bucket population of each map.
+__device__ __forceinline__ void blockwise_setup(BlockwiseShared &sh, const float *__restrict__ qmap1,
+                                                const float *__restrict__ qmap2, int &k1, int &k2)
 {
-    __shared__ BlockwiseShared sh;
     const int tid = threadIdx.x;
     sh.q1[tid] = __ldg(qmap1 + tid);
     sh.q2[tid] = __ldg(qmap2 + tid);
@@ -572,22 +571,74 @@ blockwise8_kernel(const BlockwiseArgs a, const float *__restrict__ qmap1,
     sh.mid1[256 + tid] = INFINITY;
     sh.mid2[256 + tid] = INFINITY;
     __syncthreads();
-    const int k1 = build_buckets(sh.mid1, sh.bucket1, sh.red[0]);
-    const int k2 = build_buckets(sh.mid2, sh.bucket2, sh.red[1]);
+    k1 = build_buckets(sh.mid1, sh.bucket1, sh.red[0]);
+    k2 = build_buckets(sh.mid2, sh.bucket2, sh.red[1]);
     __syncthreads();
-    const int64_t whole_blocks = a.n / kBlock;
+}
+
+// Block b of one tensor: the comparison count is fixed at compile time when
+// every bucket of both maps holds at most one (or two) midpoints.
+__device__ __forceinline__ void blockwise_dispatch(const BlockwiseArgs &a, BlockwiseShared &sh,
+                                                   int64_t b, int parity, const Scalars &s,
+                                                   int k1, int k2, uint32_t &bad)
+{
+    const int k = k1 > k2 ? k1 : k2;
+    if (b < a.n / kBlock) {
+        if (k <= 1)
+            blockwise_block<true, 1>(a, sh, b, parity, s, k1, k2, bad);
+        else if (k <= 2)
+            blockwise_block<true, 2>(a, sh, b, parity, s, k1, k2, bad);
+        else
+            blockwise_block<true, 0>(a, sh, b, parity, s, k1, k2, bad);
+    } else {
+        blockwise_block<false, 0>(a, sh, b, parity, s, k1, k2, bad);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 4)
+blockwise8_kernel(const BlockwiseArgs a, const float *__restrict__ qmap1,
+                  const float *__restrict__ qmap2, int64_t nblocks, const Scalars s,
+                  unsigned long long *nonfinite)
+{
+    __shared__ BlockwiseShared sh;
+    int k1, k2;
+    blockwise_setup(sh, qmap1, qmap2, k1, k2);
     uint32_t bad = 0;
     int parity = 0;
-    const bool two = k1 <= 2 && k2 <= 2;  // every bucket holds at most two midpoints
-    for (int64_t b = blockIdx.x; b < nblocks; b += gridDim.x, parity ^= 1) {
-        if (b < whole_blocks) {
-            if (two)
-                blockwise_block<true, 2>(a, sh, b, parity, s, k1, k2, bad);
-            else
-                blockwise_block<true, 0>(a, sh, b, parity, s, k1, k2, bad);
-        } else {
-            blockwise_block<false, 0>(a, sh, b, parity, s, k1, k2, bad);
+    for (int64_t b = blockIdx.x; b < nblocks; b += gridDim.x, parity ^= 1)
+        blockwise_dispatch(a, sh, b, parity, s, k1, k2, bad);
+    flush_nonfinite(bad, nonfinite);
+}
+
+// One tensor of a blockwise list; block0 = its first block in the list's
+// concatenated block index.
+struct BwDesc {
+    BlockwiseArgs a;
+    int64_t block0;
+};
+
+// Tensor-list form: a persistent grid over the concatenated blocks of every
+// tensor; each CTA walks the descriptor table forward.
+__global__ void __launch_bounds__(kThreads, 4)
+blockwise8_multi_kernel(const BwDesc *__restrict__ table, int32_t ntensors, int64_t total_blocks,
+                        const float *__restrict__ qmap1, const float *__restrict__ qmap2,
+                        const Scalars s, unsigned long long *nonfinite)
+{
+    __shared__ BlockwiseShared sh;
+    int k1, k2;
+    blockwise_setup(sh, qmap1, qmap2, k1, k2);
+    uint32_t bad = 0;
+    int parity = 0;
+    int32_t t = 0;
+    BwDesc d = table[0];
+    int64_t next = ntensors > 1 ? table[1].block0 : total_blocks;
+    for (int64_t b = blockIdx.x; b < total_blocks; b += gridDim.x, parity ^= 1) {
+        while (b >= next) {
+            ++t;
+            d = table[t];
+            next = t + 1 < ntensors ? table[t + 1].block0 : total_blocks;
         }
+        blockwise_dispatch(d.a, sh, b - d.block0, parity, s, k1, k2, bad);
     }
     flush_nonfinite(bad, nonfinite);
 }
@@ -1133,8 +1184,11 @@ pa_status pa_shutdown(void)
     return pa_release_tables();
 }
 
+pa_status release_blockwise_tables();
+
 pa_status pa_release_tables(void)
 {
+    release_blockwise_tables();
     std::lock_guard<std::mutex> lock(g_tab_mu);
     int cur = 0;
     cudaGetDevice(&cur);
@@ -1495,4 +1549,152 @@ extern "C" pa_status pa_adamw_step_packed_e4_multi_bf16g(const pa_tensor *list, 
 {
     return step_multi<pa::kE4, __nv_bfloat16>(list, ntensors, step, lr, beta1, beta2, eps, wd,
                                               nonfinite, stream);
+}
+
+// ===========================================================================
+// Blockwise tensor-list step
+// ===========================================================================
+namespace {
+
+struct BwTable {
+    int device;
+    std::vector<pa::BwDesc> host;
+    pa::BwDesc *dev;
+    int64_t blocks;
+    uint64_t last_use;
+};
+
+std::mutex g_bw_mu;
+std::vector<BwTable> g_bw_tables;
+uint64_t g_bw_tick = 0;
+
+pa_status check_blockwise_tensor(const pa_blockwise_tensor &t, int index)
+{
+    if (t.n < 0)
+        return fail(PA_ERR_ARG, "tensor %d: n must be >= 0 (got %lld)", index, (long long)t.n);
+    if (t.n == 0)
+        return PA_OK;
+    if (!t.p || !t.g || !t.p_bf16 || !t.m_code || !t.m_absmax || !t.v_code || !t.v_absmax)
+        return fail(PA_ERR_NULL, "tensor %d: NULL pointer with n = %lld", index, (long long)t.n);
+    if (!aligned(t.p, 16) || !aligned(t.g, 16) || !aligned(t.p_bf16, 8) ||
+        !aligned(t.m_code, 4) || !aligned(t.v_code, 4) || !aligned(t.m_absmax, 4) ||
+        !aligned(t.v_absmax, 4))
+        return fail(PA_ERR_ALIGN, "tensor %d: p, g 16-byte, p_bf16 8-byte, codes and absmax "
+                    "4-byte alignment required", index);
+    return PA_OK;
+}
+
+pa_status bw_table_for(const pa_blockwise_tensor *list, int32_t ntensors, const pa::BwDesc **out,
+                       int64_t *blocks)
+{
+    std::vector<pa::BwDesc> host((size_t)ntensors);
+    int64_t total = 0;
+    for (int32_t i = 0; i < ntensors; ++i) {
+        const pa_blockwise_tensor &t = list[i];
+        host[(size_t)i].a = {t.p, t.g, t.p_bf16, t.m_code, t.m_absmax, t.v_code, t.v_absmax, t.n};
+        host[(size_t)i].block0 = total;
+        total += (t.n + pa::kBlock - 1) / pa::kBlock;
+    }
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lock(g_bw_mu);
+    ++g_bw_tick;
+    for (BwTable &t : g_bw_tables)
+        if (t.device == dev && t.host.size() == host.size() &&
+            std::memcmp(t.host.data(), host.data(), host.size() * sizeof(pa::BwDesc)) == 0) {
+            t.last_use = g_bw_tick;
+            *out = t.dev;
+            *blocks = t.blocks;
+            return PA_OK;
+        }
+    if (g_bw_tables.size() >= kMaxTables) {
+        size_t old = 0;
+        for (size_t k = 1; k < g_bw_tables.size(); ++k)
+            if (g_bw_tables[k].last_use < g_bw_tables[old].last_use)
+                old = k;
+        int cur = dev;
+        cudaSetDevice(g_bw_tables[old].device);
+        cudaFree(g_bw_tables[old].dev);  // synchronises that device
+        cudaSetDevice(cur);
+        g_bw_tables.erase(g_bw_tables.begin() + (long)old);
+    }
+    BwTable t;
+    t.device = dev;
+    t.blocks = total;
+    t.last_use = g_bw_tick;
+    t.dev = nullptr;
+    const size_t bytes = host.size() * sizeof(pa::BwDesc);
+    if ((e = cudaMalloc((void **)&t.dev, bytes)) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(PA_ERR_NOMEM, "cudaMalloc of a %zu-byte descriptor table: %s", bytes,
+                    cudaGetErrorString(e));
+    }
+    if ((e = cudaMemcpy(t.dev, host.data(), bytes, cudaMemcpyHostToDevice)) != cudaSuccess) {
+        cudaFree(t.dev);
+        return cuda_fail(e, "descriptor table upload");
+    }
+    t.host = std::move(host);
+    g_bw_tables.push_back(std::move(t));
+    *out = g_bw_tables.back().dev;
+    *blocks = g_bw_tables.back().blocks;
+    return PA_OK;
+}
+
+}  // namespace
+
+extern "C" pa_status pa_adamw_step_blockwise8_multi(const pa_blockwise_tensor *list,
+                                                    int32_t ntensors, const float *qmap1,
+                                                    const float *qmap2, int64_t step, double lr,
+                                                    double beta1, double beta2, double eps,
+                                                    double wd, unsigned long long *nonfinite,
+                                                    pa_stream stream)
+{
+    Scalars s;
+    pa_status st = make_scalars(step, lr, beta1, beta2, eps, wd, &s);
+    if (st != PA_OK)
+        return st;
+    if (ntensors < 0)
+        return fail(PA_ERR_ARG, "ntensors must be >= 0 (got %d)", ntensors);
+    if (ntensors == 0)
+        return ok();
+    if (!list || !qmap1 || !qmap2)
+        return fail(PA_ERR_NULL, "list and maps must not be NULL");
+    if (!aligned(qmap1, 4) || !aligned(qmap2, 4))
+        return fail(PA_ERR_ALIGN, "maps must be 4-byte aligned");
+    if ((st = check_counter(nonfinite)) != PA_OK)
+        return st;
+    int64_t total = 0;
+    for (int32_t i = 0; i < ntensors; ++i) {
+        if ((st = check_blockwise_tensor(list[i], i)) != PA_OK)
+            return st;
+        total += list[i].n;
+    }
+    if (total == 0)
+        return ok();
+    const pa::BwDesc *table = nullptr;
+    int64_t blocks = 0;
+    if ((st = bw_table_for(list, ntensors, &table, &blocks)) != PA_OK)
+        return st;
+    int grid = 0;
+    if ((st = grid_for(kSlotBlockwise, blocks, &grid)) != PA_OK)
+        return st;
+    pa::blockwise8_multi_kernel<<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
+        table, ntensors, blocks, qmap1, qmap2, s, nonfinite);
+    return check_launch("blockwise8_multi_kernel launch");
+}
+
+pa_status release_blockwise_tables()
+{
+    std::lock_guard<std::mutex> lock(g_bw_mu);
+    int cur = 0;
+    cudaGetDevice(&cur);
+    for (BwTable &t : g_bw_tables) {
+        cudaSetDevice(t.device);
+        cudaFree(t.dev);
+    }
+    g_bw_tables.clear();
+    cudaSetDevice(cur);
+    return PA_OK;
 }

@@ -141,6 +141,28 @@ pa_status pa_adamw_step_blockwise8(const float *p, const float *g, uint16_t *p_b
                                    double beta2, double eps, double wd,
                                    unsigned long long *nonfinite, pa_stream stream);
 
+/* Blockwise tensor-list step: pa_adamw_step_blockwise8 over every tensor of a
+ * list in one persistent launch (blocks never span tensors: each tensor's
+ * blocks start at its element 0).  list[t] (host, read during the call):
+ * arrays as for pa_adamw_step_blockwise8 with n = list[t].n; both maps are
+ * shared by the list.  The descriptor table is cached like the other lists'. */
+typedef struct pa_blockwise_tensor {
+    const float *p;
+    const float *g;
+    uint16_t *p_bf16;
+    uint8_t *m_code;
+    float *m_absmax;
+    uint8_t *v_code;
+    float *v_absmax;
+    int64_t n;
+} pa_blockwise_tensor;
+
+pa_status pa_adamw_step_blockwise8_multi(const pa_blockwise_tensor *list, int32_t ntensors,
+                                         const float *qmap1, const float *qmap2, int64_t step,
+                                         double lr, double beta1, double beta2, double eps,
+                                         double wd, unsigned long long *nonfinite,
+                                         pa_stream stream);
+
 /* ---------------------------------------------------------------------------
  * Multi-tensor steps: one persistent grid-stride launch over every tensor of
  * a list ("Packed AdamW / Reference / v1.0.0", "Execution contract", lists one

@@ -97,3 +97,47 @@ def test_blockwise_alignment_errors(pa):
     with pytest.raises(pa.PackedAdamError):
         pa.pa_adamw_step_blockwise8(x[1:4097], x[:4096], b[:4096], c[:4096], x[:2], c[:4096],
                                     x[:2], q, q, 1)
+
+
+def test_blockwise_tensor_list_equals_single_calls(pa):
+    """One launch over a list (short, whole and ragged tensors, an empty one)
+    gives the bits of one single-tensor call per tensor, and of the oracle."""
+    import torch
+
+    q1, q2 = _maps("dynamic")
+    sizes = [1, 2048, 2049, 0, 5000, 3 * 2048 + 7]
+    rng = np.random.default_rng(12)
+    lists, singles, host = [], [], []
+    for n in sizes:
+        nb = -(-n // 2048)
+        p = rng.normal(0, 0.02, n).astype(np.float32)
+        g = rng.normal(0, 1e-3, n).astype(np.float32)
+        mc = np.full(n, wl.nearest_zero_code(q1), np.uint8)
+        vc = np.full(n, wl.nearest_zero_code(q2), np.uint8)
+        z = np.zeros(nb, np.float32)
+        mk = lambda: (dev(p), dev(g), torch.empty(n, dtype=torch.bfloat16, device="cuda"),  # noqa: E731
+                      dev(mc), dev(z), dev(vc), dev(z))
+        lists.append(mk())
+        singles.append(mk())
+        host.append([p, g, mc, z.copy(), vc, z.copy()])
+    d1, d2 = dev(q1), dev(q2)
+    for t in (1, 2):
+        pa.pa_adamw_step_blockwise8_multi(lists, d1, d2, t, **HY)
+        for e in singles:
+            if e[0].numel():
+                pa.pa_adamw_step_blockwise8(*e, d1, d2, t, **HY)
+        torch.cuda.synchronize()
+        for k, (a, b) in enumerate(zip(lists, singles)):
+            for x, y in zip(a[2:], b[2:]):
+                xb = x.cpu().numpy().view(np.uint8) if x.dtype != torch.bfloat16 else \
+                    x.view(torch.int16).cpu().numpy().view(np.uint8)
+                yb = y.cpu().numpy().view(np.uint8) if y.dtype != torch.bfloat16 else \
+                    y.view(torch.int16).cpu().numpy().view(np.uint8)
+                assert np.array_equal(xb, yb), (k, t)
+            if sizes[k]:
+                p, g, mc, ma, vc, va = host[k]
+                ob, mc, ma, vc, va, _ = oracle.step_blockwise8(p, g, mc, ma, vc, va, q1, q2, t, **HY)
+                host[k] = [p, g, mc, ma, vc, va]
+                got = a[2].view(torch.int16).cpu().numpy().view(np.uint16)
+                assert np.array_equal(got, ob) and np.array_equal(a[3].cpu().numpy(), mc)
+                assert np.array_equal(a[5].cpu().numpy(), vc)
