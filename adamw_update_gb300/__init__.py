@@ -29,7 +29,7 @@ __all__ = [
     "shard_bounds", "pa_adamw_step_packed_e4_multi_noalloc", "pa_adamw_step_packed_e4_host",
     "pa_hyper_table_fill", "pa_adamw_step_packed_e4_multi_graph",
     "pa_adamw_step_packed_e4_bf16g", "pa_adamw_step_packed_e4_multi_bf16g", "pa_shutdown",
-    "pa_adamw_step_blockwise8_multi",
+    "pa_adamw_step_blockwise8_multi", "pa_device_fault",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -435,3 +435,17 @@ def pa_adamw_step_blockwise8_multi(entries, qmap1, qmap2, step, lr=1e-3, beta1=0
                                                _ptr(qmap2, torch.float32),
                                                *_hyp(step, lr, beta1, beta2, eps, wd),
                                                _ptr(nonfinite), _stream(stream)))
+
+
+# ---- fault flag of the staged step kernels ------------------------------------------
+
+_lib.pa_device_fault.restype = _i32
+_lib.pa_device_fault.argtypes = [ctypes.POINTER(ctypes.c_uint32), _i32]
+
+
+def pa_device_fault(clear: bool = False) -> int:
+    """0 if no bounded wait of a staged step kernel has run out on the current
+    device since the flag was last cleared, else its fault code (1-3)."""
+    code = ctypes.c_uint32(0)
+    _check(_lib.pa_device_fault(ctypes.byref(code), 1 if clear else 0))
+    return int(code.value)

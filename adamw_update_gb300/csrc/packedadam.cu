@@ -25,11 +25,13 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <type_traits>
 #include <vector>
 
 #include "blockwise.cuh"
 #include "codecs.cuh"
 #include "packedadam.h"
+#include "pipeline.cuh"
 
 namespace pa {
 
@@ -272,14 +274,256 @@ adamw_step_kernel(const Desc *__restrict__ table, int32_t ntensors, int64_t tota
                                          nonfinite);
 }
 
+// ---- the staged step (FP32 gradients) -----------------------------------------
+// One CTA per SM: a producer warp whose lane 0 streams tiles of p, g and the
+// state (p, g, m, v in the FP32 mode) into a two-stage shared-memory ring
+// with bulk (TMA) copies, and 24 consumer warps that update a staged tile
+// from shared memory and store p' and the new state straight to global memory
+// with streaming hints.  The copies of the next tile are in flight while the
+// consumers work on the current one, so HBM sees a steady stream of large
+// reads without the registers that register-staged loads would hold, and the
+// 768 consumer threads have enough independent elements (8 each per tile) to
+// hide the latency of the division and square-root chains.  Measured on
+// GB300 (10^9 parameters, packed E4): 6144-element tiles with 24 consumer
+// warps and two stages ran at 1.13x the register-staged kernel; 8 consumer
+// warps could not keep up with the copies.
+//
+// A tile covers kTile elements of one tensor's 16-byte body (from d.head on);
+// the last tile of a tensor may be shorter: its largest multiple of four
+// elements is copied and the remaining <= 3, like the <= 3 head elements, are
+// updated from global memory by single consumer threads.  A tensor on the
+// 4-byte path (streams not sharing their address modulo 16) is cut into
+// tiles the same way but updated from global memory, with no copies.
+constexpr int kTile = 6144;
+constexpr int kStages = 2;
+constexpr int kConsumerWarps = 24;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kPipeThreads = kConsumers + 32;  // + the producer warp
+constexpr int kTileVecs = kTile / (4 * kConsumers);
+static_assert(kTile % (4 * kConsumers) == 0, "a tile is whole 16-byte vectors per consumer");
+
+template <int MODE>
+struct PipeLayout {
+    static constexpr int kStreams = MODE == kF32 ? 4 : 3;  // p, g, word | p, g, m, v
+    static constexpr size_t kStageBytes = (size_t)kStreams * kTile * 4;
+    static constexpr size_t kBytes = kStages * kStageBytes + 2 * kStages * sizeof(uint64_t);
+};
+
+// Set (first code wins) when a bounded wait of a staged kernel gives up; the
+// launch's results are then incomplete.  Read and cleared by pa_device_fault.
+enum PipeFault : uint32_t {
+    kFaultEmptyWait = 1,  // the producer waited > 2 s for consumers to free a stage
+    kFaultCopyWait = 2,   // the producer waited > 2 s for its last copies to land
+    kFaultFullWait = 3,   // a consumer waited > 2 s for a stage's copies
+};
+static __device__ uint32_t g_pipe_fault;
+
+__device__ __forceinline__ void pipe_fault(uint32_t code)
+{
+    atomicCAS(&g_pipe_fault, 0u, code);
+}
+
+// Elements [base, base + len) of the tensor form tile k; the first len4 of
+// them (a multiple of 4) are staged by bulk copies (0 on the 4-byte path).
+struct Span {
+    int64_t base;
+    int32_t len, len4;
+};
+
+__device__ __forceinline__ Span tile_span(const Desc &d, int64_t k)
+{
+    const int64_t b = k * kTile;
+    int64_t len = (d.vec ? d.n - d.head : d.n) - b;
+    len = len < 0 ? 0 : (len > kTile ? kTile : len);
+    Span sp;
+    sp.base = d.vec ? d.head + b : b;
+    sp.len = (int32_t)len;
+    sp.len4 = d.vec ? (int32_t)(len & ~(int64_t)3) : 0;
+    return sp;
+}
+
+// Walks the descriptor table forward to the tensor of global tile c.
+template <bool MULTI>
+struct TableCursor {
+    const Desc *table;
+    int32_t ntensors, t;
+    int64_t next;
+    Desc d;
+    __device__ __forceinline__ TableCursor(const Desc *tab, int32_t nt, int64_t total,
+                                           const Desc &single)
+        : table(tab), ntensors(nt), t(0), next(total), d(single)
+    {
+        if (MULTI) {
+            d = table[0];
+            next = ntensors > 1 ? table[1].chunk0 : total;
+        }
+    }
+    __device__ __forceinline__ void seek(int64_t c, int64_t total)
+    {
+        if (MULTI)
+            while (c >= next) {
+                ++t;
+                d = table[t];
+                next = t + 1 < ntensors ? table[t + 1].chunk0 : total;
+            }
+    }
+};
+
+template <int MODE, bool MULTI>
+__device__ __forceinline__ void pipe_produce(unsigned char *smem, uint64_t *full, uint64_t *empty,
+                                             const Desc *table, int32_t ntensors, int64_t total,
+                                             const Desc &single)
+{
+    using L = PipeLayout<MODE>;
+    TableCursor<MULTI> cur(table, ntensors, total, single);
+    int64_t k = 0;  // fills issued
+    for (int64_t c = blockIdx.x; c < total; c += gridDim.x, ++k) {
+        cur.seek(c, total);
+        const int st = (int)(k % kStages);
+        const uint32_t use = (uint32_t)(k / kStages);
+        if (!mbar_wait(&empty[st], (use & 1u) ^ 1u)) {  // the first use passes at once
+            pipe_fault(kFaultEmptyWait);
+            break;
+        }
+        const Span sp = tile_span(cur.d, c - cur.d.chunk0);
+        const uint32_t bytes = (uint32_t)sp.len4 * 4u;
+        mbar_arrive_expect(&full[st], bytes * (uint32_t)L::kStreams);
+        if (bytes != 0) {
+            unsigned char *buf = smem + (size_t)st * L::kStageBytes;
+            bulk_load(buf, cur.d.p + sp.base, bytes, &full[st]);
+            bulk_load(buf + kTile * 4, cur.d.g + sp.base, bytes, &full[st]);
+            bulk_load(buf + 2 * kTile * 4, static_cast<const uint32_t *>(cur.d.s1) + sp.base, bytes,
+                      &full[st]);
+            if (MODE == kF32)
+                bulk_load(buf + 3 * kTile * 4, static_cast<const float *>(cur.d.s2) + sp.base,
+                          bytes, &full[st]);
+        }
+    }
+    // The CTA's shared memory must outlive its copies: wait for the last fill
+    // of every stage before leaving.
+    for (int64_t j = k > kStages ? k - kStages : 0; j < k; ++j)
+        if (!mbar_wait(&full[j % kStages], (uint32_t)((j / kStages) & 1)))
+            pipe_fault(kFaultCopyWait);
+}
+
+template <int MODE, bool MULTI, bool U1>
+__device__ __forceinline__ void pipe_consume(const unsigned char *smem, uint64_t *full,
+                                             uint64_t *empty, const Desc *table, int32_t ntensors,
+                                             int64_t total, const Desc &single, const Scalars &s,
+                                             uint32_t &bad)
+{
+    using L = PipeLayout<MODE>;
+    const int ct = threadIdx.x;  // consumer thread, 0 .. kConsumers-1
+    TableCursor<MULTI> cur(table, ntensors, total, single);
+    int64_t k = 0;
+    for (int64_t c = blockIdx.x; c < total; c += gridDim.x, ++k) {
+        cur.seek(c, total);
+        const int st = (int)(k % kStages);
+        if (!mbar_wait(&full[st], (uint32_t)((k / kStages) & 1))) {
+            pipe_fault(kFaultFullWait);
+            break;
+        }
+        const Desc &d = cur.d;
+        const int64_t kt = c - d.chunk0;
+        const Span sp = tile_span(d, kt);
+        if (d.vec) {
+            const unsigned char *buf = smem + (size_t)st * L::kStageBytes;
+#pragma unroll
+            for (int v = 0; v < kTileVecs; ++v) {
+                const int e = 4 * (ct + v * kConsumers);
+                if (e < sp.len4) {
+                    const float4 pv = *reinterpret_cast<const float4 *>(buf + 4 * e);
+                    const float4 gv = *reinterpret_cast<const float4 *>(buf + kTile * 4 + 4 * e);
+                    float pp[4] = {pv.x, pv.y, pv.z, pv.w};
+                    const float gg[4] = {gv.x, gv.y, gv.z, gv.w};
+                    float *P = d.p + sp.base + e;
+                    if constexpr (MODE == kF32) {
+                        const float4 mv = *reinterpret_cast<const float4 *>(buf + 2 * kTile * 4 + 4 * e);
+                        const float4 vv = *reinterpret_cast<const float4 *>(buf + 3 * kTile * 4 + 4 * e);
+                        float mm[4] = {mv.x, mv.y, mv.z, mv.w};
+                        float vq[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const Moments o = adamw_element<U1>(pp[j], gg[j], mm[j], vq[j], s);
+                            bad += any_nonfinite(o);
+                            pp[j] = o.p;
+                            mm[j] = o.m;
+                            vq[j] = o.v;
+                        }
+                        store_stream(static_cast<float *>(d.s1) + sp.base + e,
+                                     make_float4(mm[0], mm[1], mm[2], mm[3]));
+                        store_stream(static_cast<float *>(d.s2) + sp.base + e,
+                                     make_float4(vq[0], vq[1], vq[2], vq[3]));
+                    } else {
+                        const uint4 wv = *reinterpret_cast<const uint4 *>(buf + 2 * kTile * 4 + 4 * e);
+                        uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            ww[j] = packed_element<MODE, U1>(pp[j], gg[j], ww[j], s, bad);
+                        store_stream(static_cast<uint32_t *>(d.s1) + sp.base + e,
+                                     make_uint4(ww[0], ww[1], ww[2], ww[3]));
+                    }
+                    store_stream(P, make_float4(pp[0], pp[1], pp[2], pp[3]));
+                }
+            }
+            if (kt == 0 && ct < d.head)  // the <= 3 elements before the 16-byte body
+                scalar_element<MODE, U1>(d, ct, s, bad);
+            if (ct < sp.len - sp.len4)  // the <= 3 elements after the staged part
+                scalar_element<MODE, U1>(d, sp.base + sp.len4 + ct, s, bad);
+        } else {
+            for (int j = ct; j < sp.len; j += kConsumers)
+                scalar_element<MODE, U1>(d, sp.base + j, s, bad);
+        }
+        __syncwarp();
+        if ((ct & 31) == 0)
+            mbar_arrive(&empty[st]);
+    }
+}
+
+template <int MODE, bool MULTI, bool U1>
+__device__ __forceinline__ void pipe_body(const Desc *__restrict__ table, int32_t ntensors,
+                                          int64_t total_tiles, const Desc &single,
+                                          const Scalars &s, unsigned long long *nonfinite)
+{
+    using L = PipeLayout<MODE>;
+    extern __shared__ __align__(128) unsigned char pipe_smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(pipe_smem + kStages * L::kStageBytes);
+    uint64_t *empty = full + kStages;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kConsumerWarps);
+        }
+        mbar_init_fence();
+    }
+    __syncthreads();
+    if (threadIdx.x >= kConsumers) {
+        if (threadIdx.x == kConsumers)
+            pipe_produce<MODE, MULTI>(pipe_smem, full, empty, table, ntensors, total_tiles, single);
+        return;
+    }
+    uint32_t bad = 0;
+    pipe_consume<MODE, MULTI, U1>(pipe_smem, full, empty, table, ntensors, total_tiles, single, s,
+                                  bad);
+    flush_nonfinite(bad, nonfinite);
+}
+
+template <int MODE, bool MULTI, bool U1>
+__global__ void __launch_bounds__(kPipeThreads, 1)
+adamw_step_pipe_kernel(const Desc *__restrict__ table, int32_t ntensors, int64_t total_tiles,
+                       const Desc single, const Scalars s, unsigned long long *nonfinite)
+{
+    pipe_body<MODE, MULTI, U1>(table, ntensors, total_tiles, single, s, nonfinite);
+}
+
 // Graph-replayable variant: the scalars of the step are row *index of a
 // device table filled by the host ahead of time, so a captured launch needs no
 // host work per step.  An index outside [0, rows) sets *status to 1 and
 // skips the update (nothing is written).
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, kMinBlocks)
-adamw_step_table_kernel(const Desc *__restrict__ table, int32_t ntensors, int64_t total_chunks,
-                        int64_t chunk, const Scalars *__restrict__ rows, int32_t nrows,
+__global__ void __launch_bounds__(kPipeThreads, 1)
+adamw_step_table_kernel(const Desc *__restrict__ table, int32_t ntensors, int64_t total_tiles,
+                        const Scalars *__restrict__ rows, int32_t nrows,
                         const int64_t *__restrict__ index, int32_t *status,
                         unsigned long long *nonfinite)
 {
@@ -291,7 +535,7 @@ adamw_step_table_kernel(const Desc *__restrict__ table, int32_t ntensors, int64_
     }
     const Scalars s = rows[i];
     Desc none = {};
-    adamw_step_body<MODE, true, false>(table, ntensors, total_chunks, chunk, none, s, nonfinite);
+    pipe_body<MODE, true, false>(table, ntensors, total_tiles, none, s, nonfinite);
 }
 
 __global__ void advance_index_kernel(int64_t *index)
@@ -706,26 +950,24 @@ pa_status make_scalars(int64_t step, double lr, double beta1, double beta2, doub
 }
 
 // ---- per-device launch geometry --------------------------------------------
+// Kernels launched with kThreads threads and no dynamic shared memory: the
+// register-staged step (bfloat16 gradients), the blockwise step, the codecs.
+enum KernelSlot { kSlotBf16, kSlotBf16Multi, kSlotBlockwise, kSlotCodec, kNumSlots };
+
 struct DeviceInfo {
     bool ready = false;
     int sms = 0;
-    int occ[8] = {0};  // resident CTAs per SM, by kernel slot
+    int occ[kNumSlots] = {0};  // resident CTAs per SM, by kernel slot
 };
 
 std::mutex g_dev_mu;
 DeviceInfo g_dev[64];
 
-enum KernelSlot { kSlotE4, kSlotFP16, kSlotF32, kSlotE4Multi, kSlotFP16Multi, kSlotF32Multi, kSlotBlockwise, kSlotCodec };
-
 const void *kernel_of(int slot)
 {
     switch (slot) {
-    case kSlotE4: return (const void *)pa::adamw_step_kernel<pa::kE4, false, false>;
-    case kSlotFP16: return (const void *)pa::adamw_step_kernel<pa::kFP16, false, false>;
-    case kSlotF32: return (const void *)pa::adamw_step_kernel<pa::kF32, false, false>;
-    case kSlotE4Multi: return (const void *)pa::adamw_step_kernel<pa::kE4, true, false>;
-    case kSlotFP16Multi: return (const void *)pa::adamw_step_kernel<pa::kFP16, true, false>;
-    case kSlotF32Multi: return (const void *)pa::adamw_step_kernel<pa::kF32, true, false>;
+    case kSlotBf16: return (const void *)pa::adamw_step_kernel<pa::kE4, false, false, __nv_bfloat16>;
+    case kSlotBf16Multi: return (const void *)pa::adamw_step_kernel<pa::kE4, true, false, __nv_bfloat16>;
     case kSlotBlockwise: return (const void *)pa::blockwise8_kernel;
     default: return (const void *)pa::encode_state_kernel<pa::kE4>;
     }
@@ -747,7 +989,7 @@ pa_status grid_for(int slot, int64_t work, int *grid)
         e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess)
             return cuda_fail(e, "cudaDeviceGetAttribute");
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < kNumSlots; ++k) {
             e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&di.occ[k], kernel_of(k), pa::kThreads, 0);
             if (e != cudaSuccess)
                 return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
@@ -774,6 +1016,45 @@ pa_status chunk_size(int slot, int64_t elements, int64_t *chunk)
     int64_t waves = elements / (pa::kWave * (int64_t)full * 32);
     waves = waves < 1 ? 1 : (waves > pa::kMaxWaves ? pa::kMaxWaves : waves);
     *chunk = waves * pa::kWave;
+    return PA_OK;
+}
+
+// Grid of a staged kernel: one CTA per SM (its shared-memory ring takes most
+// of the SM), capped by the tiles.  The first launch of each kernel on a device
+// raises its dynamic shared-memory limit.
+pa_status pipe_grid(const void *kernel, size_t smem, int64_t tiles, int *grid)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64)
+        return fail(PA_ERR_CUDA, "device ordinal %d out of range", dev);
+    static std::mutex mu;
+    static std::vector<std::pair<const void *, int>> ready;  // (kernel, device) set up
+    static int sms[64] = {0};
+    std::lock_guard<std::mutex> lock(mu);
+    bool done = false;
+    for (const auto &r : ready)
+        done = done || (r.first == kernel && r.second == dev);
+    if (!done) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "raising the shared-memory limit of the staged step");
+        int occ = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, pa::kPipeThreads, smem);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+        if (occ < 1)
+            return fail(PA_ERR_CUDA, "the staged step (%zu bytes of shared memory) does not fit an SM",
+                        smem);
+        if (sms[dev] == 0 &&
+            (e = cudaDeviceGetAttribute(&sms[dev], cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        ready.emplace_back(kernel, dev);
+    }
+    const int64_t full = sms[dev];
+    *grid = (int)(tiles < full ? (tiles > 0 ? tiles : 1) : full);
     return PA_OK;
 }
 
@@ -855,13 +1136,30 @@ pa_status step_single(const pa_tensor &t, int64_t step, double lr, double beta1,
     if (t.n == 0)
         return ok();
     Desc d;
+    if constexpr (std::is_same<GT, float>::value) {
+        const int64_t tiles = describe(t, MODE, pa::kTile, &d);
+        d.chunk0 = 0;
+        const size_t smem = pa::PipeLayout<MODE>::kBytes;
+        const void *kern = s.bc2 == 1.0f ? (const void *)pa::adamw_step_pipe_kernel<MODE, false, true>
+                                         : (const void *)pa::adamw_step_pipe_kernel<MODE, false, false>;
+        int grid = 0;
+        if ((st = pipe_grid(kern, smem, tiles, &grid)) != PA_OK)
+            return st;
+        if (s.bc2 == 1.0f)
+            pa::adamw_step_pipe_kernel<MODE, false, true><<<grid, pa::kPipeThreads, smem, (cudaStream_t)stream>>>(
+                nullptr, 1, tiles, d, s, nonfinite);
+        else
+            pa::adamw_step_pipe_kernel<MODE, false, false><<<grid, pa::kPipeThreads, smem, (cudaStream_t)stream>>>(
+                nullptr, 1, tiles, d, s, nonfinite);
+        return check_launch("adamw_step_pipe_kernel launch");
+    }
     int64_t chunk = 0;
-    if ((st = chunk_size(MODE, t.n, &chunk)) != PA_OK)
+    if ((st = chunk_size(kSlotBf16, t.n, &chunk)) != PA_OK)
         return st;
     const int64_t chunks = describe(t, MODE, chunk, &d, (int)sizeof(GT));
     d.chunk0 = 0;
     int grid = 0;
-    if ((st = grid_for(MODE, chunks, &grid)) != PA_OK)
+    if ((st = grid_for(kSlotBf16, chunks, &grid)) != PA_OK)
         return st;
     if (s.bc2 == 1.0f)
         pa::adamw_step_kernel<MODE, false, true, GT><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
@@ -984,16 +1282,34 @@ pa_status step_multi(const pa_tensor *list, int32_t ntensors, int64_t step, doub
     if (total == 0)
         return ok();
     const Desc *table = nullptr;
+    Desc none;
+    std::memset(&none, 0, sizeof none);
+    if constexpr (std::is_same<GT, float>::value) {
+        int64_t tiles = 0;
+        if ((st = table_for(list, ntensors, MODE, pa::kTile, &table, &tiles)) != PA_OK)
+            return st;
+        const size_t smem = pa::PipeLayout<MODE>::kBytes;
+        const void *kern = s.bc2 == 1.0f ? (const void *)pa::adamw_step_pipe_kernel<MODE, true, true>
+                                         : (const void *)pa::adamw_step_pipe_kernel<MODE, true, false>;
+        int grid = 0;
+        if ((st = pipe_grid(kern, smem, tiles, &grid)) != PA_OK)
+            return st;
+        if (s.bc2 == 1.0f)
+            pa::adamw_step_pipe_kernel<MODE, true, true><<<grid, pa::kPipeThreads, smem, (cudaStream_t)stream>>>(
+                table, ntensors, tiles, none, s, nonfinite);
+        else
+            pa::adamw_step_pipe_kernel<MODE, true, false><<<grid, pa::kPipeThreads, smem, (cudaStream_t)stream>>>(
+                table, ntensors, tiles, none, s, nonfinite);
+        return check_launch("adamw_step_pipe_kernel (multi) launch");
+    }
     int64_t chunks = 0, chunk = 0;
-    if ((st = chunk_size(MODE + 3, total, &chunk)) != PA_OK)
+    if ((st = chunk_size(kSlotBf16Multi, total, &chunk)) != PA_OK)
         return st;
     if ((st = table_for(list, ntensors, MODE, chunk, &table, &chunks, (int)sizeof(GT))) != PA_OK)
         return st;
     int grid = 0;
-    if ((st = grid_for(MODE + 3, chunks, &grid)) != PA_OK)
+    if ((st = grid_for(kSlotBf16Multi, chunks, &grid)) != PA_OK)
         return st;
-    Desc none;
-    std::memset(&none, 0, sizeof none);
     if (s.bc2 == 1.0f)
         pa::adamw_step_kernel<MODE, true, true, GT><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
             table, ntensors, chunks, chunk, none, s, nonfinite);
@@ -1184,6 +1500,21 @@ pa_status pa_shutdown(void)
     return pa_release_tables();
 }
 
+pa_status pa_device_fault(uint32_t *code, int32_t clear)
+{
+    if (!code)
+        return fail(PA_ERR_NULL, "code is NULL");
+    cudaError_t e = cudaMemcpyFromSymbol(code, pa::g_pipe_fault, sizeof(uint32_t));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "reading the device fault flag");
+    if (clear && *code != 0) {
+        const uint32_t zero = 0;
+        if ((e = cudaMemcpyToSymbol(pa::g_pipe_fault, &zero, sizeof zero)) != cudaSuccess)
+            return cuda_fail(e, "clearing the device fault flag");
+    }
+    return ok();
+}
+
 pa_status release_blockwise_tables();
 
 pa_status pa_release_tables(void)
@@ -1273,7 +1604,7 @@ extern "C" pa_status pa_adamw_step_packed_e4_multi_noalloc(
         return fail(PA_ERR_NULL, "tensor list is NULL with ntensors = %d", ntensors);
     if ((st = check_counter(nonfinite)) != PA_OK)
         return st;
-    int64_t total = 0, chunks = 0, chunk = 0;
+    int64_t total = 0, tiles = 0;
     for (int32_t i = 0; i < ntensors; ++i) {
         if ((st = check_tensor(list[i], pa::kE4, i)) != PA_OK)
             return st;
@@ -1281,12 +1612,10 @@ extern "C" pa_status pa_adamw_step_packed_e4_multi_noalloc(
     }
     if (total == 0)
         return ok();
-    if ((st = chunk_size(kSlotE4Multi, total, &chunk)) != PA_OK)
-        return st;
     for (int32_t i = 0; i < ntensors; ++i) {
-        const int64_t c = describe(list[i], pa::kE4, chunk, &g_noalloc_host[i]);
-        g_noalloc_host[i].chunk0 = chunks;
-        chunks += c;
+        const int64_t c = describe(list[i], pa::kE4, pa::kTile, &g_noalloc_host[i]);
+        g_noalloc_host[i].chunk0 = tiles;
+        tiles += c;
     }
     pa::Desc *table = nullptr;
     if ((st = noalloc_table_address(&table)) != PA_OK)
@@ -1297,18 +1626,21 @@ extern "C" pa_status pa_adamw_step_packed_e4_multi_noalloc(
                                     cudaMemcpyHostToDevice, (cudaStream_t)stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "descriptor upload to the fixed device array");
+    const size_t smem = pa::PipeLayout<pa::kE4>::kBytes;
+    const void *kern = s.bc2 == 1.0f ? (const void *)pa::adamw_step_pipe_kernel<pa::kE4, true, true>
+                                     : (const void *)pa::adamw_step_pipe_kernel<pa::kE4, true, false>;
     int grid = 0;
-    if ((st = grid_for(kSlotE4Multi, chunks, &grid)) != PA_OK)
+    if ((st = pipe_grid(kern, smem, tiles, &grid)) != PA_OK)
         return st;
     pa::Desc none;
     std::memset(&none, 0, sizeof none);
     if (s.bc2 == 1.0f)
-        pa::adamw_step_kernel<pa::kE4, true, true><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
-            table, ntensors, chunks, chunk, none, s, nonfinite);
+        pa::adamw_step_pipe_kernel<pa::kE4, true, true><<<grid, pa::kPipeThreads, smem, (cudaStream_t)stream>>>(
+            table, ntensors, tiles, none, s, nonfinite);
     else
-        pa::adamw_step_kernel<pa::kE4, true, false><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
-            table, ntensors, chunks, chunk, none, s, nonfinite);
-    return check_launch("adamw_step_kernel (no-alloc multi) launch");
+        pa::adamw_step_pipe_kernel<pa::kE4, true, false><<<grid, pa::kPipeThreads, smem, (cudaStream_t)stream>>>(
+            table, ntensors, tiles, none, s, nonfinite);
+    return check_launch("adamw_step_pipe_kernel (no-alloc multi) launch");
 }
 
 // ===========================================================================
@@ -1509,17 +1841,17 @@ extern "C" pa_status pa_adamw_step_packed_e4_multi_graph(const pa_tensor *list, 
     cudaStream_t cs = (cudaStream_t)stream;
     if (total > 0) {
         const Desc *table = nullptr;
-        int64_t chunks = 0, chunk = 0;
-        if ((st = chunk_size(kSlotE4Multi, total, &chunk)) != PA_OK)
+        int64_t tiles = 0;
+        if ((st = table_for(list, ntensors, pa::kE4, pa::kTile, &table, &tiles)) != PA_OK)
             return st;
-        if ((st = table_for(list, ntensors, pa::kE4, chunk, &table, &chunks)) != PA_OK)
-            return st;
+        const size_t smem = pa::PipeLayout<pa::kE4>::kBytes;
         int grid = 0;
-        if ((st = grid_for(kSlotE4Multi, chunks, &grid)) != PA_OK)
+        if ((st = pipe_grid((const void *)pa::adamw_step_table_kernel<pa::kE4>, smem, tiles, &grid)) !=
+            PA_OK)
             return st;
-        pa::adamw_step_table_kernel<pa::kE4><<<grid, pa::kThreads, 0, cs>>>(
-            table, ntensors, chunks, chunk, reinterpret_cast<const Scalars *>(rows), nrows,
-            index, status, nonfinite);
+        pa::adamw_step_table_kernel<pa::kE4><<<grid, pa::kPipeThreads, smem, cs>>>(
+            table, ntensors, tiles, reinterpret_cast<const Scalars *>(rows), nrows, index, status,
+            nonfinite);
         if ((st = check_launch("adamw_step_table_kernel launch")) != PA_OK)
             return st;
     }

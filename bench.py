@@ -46,8 +46,8 @@ sys.path.insert(0, ROOT)
 import workloads as wl  # noqa: E402
 
 BYTES_PER_PARAM = {"e4": 20, "fp16": 20, "fp32": 28, "blockwise": 14 + 16 / 2048}
-KERNEL_NAME = {"e4": "adamw_step_kernel<0,true>", "fp16": "adamw_step_kernel<1,true>",
-               "fp32": "adamw_step_kernel<2,true>", "blockwise": "blockwise8_kernel"}
+KERNEL_NAME = {"e4": "adamw_step_pipe_kernel<0,true>", "fp16": "adamw_step_pipe_kernel<1,true>",
+               "fp32": "adamw_step_pipe_kernel<2,true>", "blockwise": "blockwise8_kernel"}
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_HBM_GBS = 6800.0
 
@@ -113,7 +113,7 @@ def traffic_per_param(mode):
         return None
     src = os.path.join(ROOT, "adamw_update_gb300", "csrc")
     h = hashlib.sha256()
-    for name in ("packedadam.cu", "codecs.cuh", "blockwise.cuh"):
+    for name in ("packedadam.cu", "codecs.cuh", "blockwise.cuh", "pipeline.cuh"):
         with open(os.path.join(src, name), "rb") as f:
             h.update(f.read())
     entry = d.get(mode)
@@ -538,7 +538,10 @@ def run_ours(args):
                 "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_source": peak_kind,
                 "traffic": None if traffic is None else traffic * w.n,
-                "kernel": KERNEL_NAME[w.mode], "kernel_ms": kernel_ms,
+                "kernel": ("adamw_step_kernel<0,true,bfloat16>" if args.grad == "bf16"
+                           else "adamw_step_table_kernel<0>" if args.graph
+                           else KERNEL_NAME[w.mode]),
+                "kernel_ms": kernel_ms,
             },
             "cpu_baseline": cpu,
             "e2e": e2e,

@@ -97,9 +97,13 @@ pa_status pa_decode_state_fp16(const uint32_t *word, float *m, float *rms, int64
 /* ---------------------------------------------------------------------------
  * Single-tensor AdamW steps.  p (float[n]) and the state are updated in place;
  * g (float[n]) is read.  step is the 1-based global step.  All arrays 4-byte
- * aligned; when p, g and the state share their address modulo 16 the kernel
- * uses 16-byte accesses after peeling up to 3 leading elements, otherwise
- * 4-byte accesses.
+ * aligned; when p, g and the state share their address modulo 16, the part
+ * after up to 3 leading elements is staged through shared memory by bulk
+ * copies (6144-element tiles, one CTA per SM, about 144 KB of shared memory;
+ * 192 KB in the FP32 mode), otherwise elements are read with 4-byte accesses.
+ * The staged kernels wait on their own copies with a 2-second limit; a wait
+ * that runs out leaves that launch's results incomplete and is reported by
+ * pa_device_fault (below), never by a hang.
  *
  * pa_adamw_step_packed_e4 -- the packed E4 step ("Packed AdamW / Reference /
  *   v1.0.0", "Release scope"): decode m and r from state[i], v = r*r, the FP32
@@ -303,6 +307,15 @@ pa_status pa_adamw_step_packed_e4_multi_graph(const pa_tensor *list, int32_t nte
                                               const pa_hyper *rows, int32_t nrows, int64_t *index,
                                               int32_t *status, unsigned long long *nonfinite,
                                               pa_stream stream);
+
+/* Device fault flag of the staged step kernels (current device): *code = 0
+ * when no bounded wait has run out since the flag was last cleared, else 1 (the
+ * copying warp found a stage still in use after 2 s), 2 (a copy had not landed
+ * 2 s after the last tile) or 3 (a computing warp waited 2 s for a stage's
+ * copies); the first fault is kept.  clear != 0 resets it to 0.  Synchronous:
+ * the read waits for the work already queued on the legacy default stream.
+ * PA_ERR_NULL if code is NULL. */
+pa_status pa_device_fault(uint32_t *code, int32_t clear);
 
 /* Frees every cached descriptor table on every device (synchronises them). */
 pa_status pa_release_tables(void);

@@ -41,7 +41,7 @@ def _f32(n, seed, std):
     return torch.from_numpy(np.random.default_rng(seed).normal(0, std, n).astype(np.float32))
 
 
-@pytest.mark.parametrize("n", [1, 2, 3, 5, 17, 4095, 4097, 9001])
+@pytest.mark.parametrize("n", [1, 2, 3, 5, 17, 4095, 4097, 6143, 6145, 9001, 12291])
 @pytest.mark.parametrize("off", [0, 1, 2, 3])
 def test_single_steps_and_codecs_stay_in_bounds(n, off):
     import torch

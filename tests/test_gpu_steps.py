@@ -17,7 +17,7 @@ from gpu_helpers import assert_same_bits, dev, host_f32, host_u32
 pytestmark = pytest.mark.gpu
 
 HY = wl.HYPER
-SIZES = [1, 3, 4, 5, 255, 4095, 4096, 4097, 3 * 4096 + 7, 100_003]
+SIZES = [1, 3, 4, 5, 255, 4095, 4096, 4097, 3 * 4096 + 7, 6143, 6144, 6147, 2 * 6144 + 5, 100_003]
 
 
 @pytest.fixture(scope="module")
@@ -298,3 +298,8 @@ def test_late_steps_unit_bias_correction(pa, mode):
     assert_same_bits(gp, ep, f"{mode} p")
     assert_same_bits(gw, ew, f"{mode} state")
     assert gb == eb
+
+
+def test_no_pipeline_fault_after_the_steps(pa):
+    """The staged kernels' bounded waits never ran out during this module."""
+    assert pa.pa_device_fault(clear=True) == 0
