@@ -92,14 +92,15 @@ __device__ __forceinline__ void store_stream(uint32_t *a, uint4 x) { __stcs(rein
 // ---- one element of a packed step -------------------------------------------
 // Decode the prior state, v = r*r, FP32 update, encode m' and sqrt(v') into the
 // next word ("Release scope": the state is stored only after the update).
-template <int MODE, bool UNIT_BC2>
+template <int MODE, bool UNIT_BC2, bool ZS = false>
 __device__ __forceinline__ uint32_t packed_element(float &p, float g, uint32_t w,
-                                                   const Scalars &s, uint32_t &bad)
+                                                   const Scalars &s, uint32_t &bad,
+                                                   const ZeroSafe *zs = nullptr)
 {
     const float m = MODE == kE4 ? decode_m_lane(w) : decode_fp16_low(w);
     const float r = MODE == kE4 ? decode_rms_lane(w) : decode_fp16_high(w);
     float rn = 0.0f;
-    const Moments o = adamw_element<UNIT_BC2>(p, g, m, __fmul_rn(r, r), s, &rn);
+    const Moments o = adamw_element<UNIT_BC2, ZS>(p, g, m, __fmul_rn(r, r), s, &rn, zs);
     bad += any_nonfinite(o);
     p = o.p;
     if (!UNIT_BC2)
@@ -406,6 +407,76 @@ __device__ __forceinline__ void pipe_produce(unsigned char *smem, uint64_t *full
             pipe_fault(kFaultCopyWait);
 }
 
+// One staged 16-byte vector: elements e..e+3 of the stage buffer, which are
+// elements base+e.. of the tensor.  A warp with an exactly-zero gradient among
+// its lanes' elements takes the zero-safe arithmetic (same results).
+template <int MODE, bool U1, bool ZS>
+__device__ __forceinline__ void pipe_vector_math(const unsigned char *buf, int e, const Desc &d,
+                                                 int64_t base, float pp[4], const float gg[4],
+                                                 const Scalars &s, const ZeroSafe &zs,
+                                                 uint32_t &bad)
+{
+    if constexpr (MODE == kF32) {
+        const float4 mv = *reinterpret_cast<const float4 *>(buf + 2 * kTile * 4 + 4 * e);
+        const float4 vv = *reinterpret_cast<const float4 *>(buf + 3 * kTile * 4 + 4 * e);
+        float mm[4] = {mv.x, mv.y, mv.z, mv.w};
+        float vq[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const Moments o = adamw_element<U1, ZS>(pp[j], gg[j], mm[j], vq[j], s, nullptr, &zs);
+            bad += any_nonfinite(o);
+            pp[j] = o.p;
+            mm[j] = o.m;
+            vq[j] = o.v;
+        }
+        store_stream(static_cast<float *>(d.s1) + base + e, make_float4(mm[0], mm[1], mm[2], mm[3]));
+        store_stream(static_cast<float *>(d.s2) + base + e, make_float4(vq[0], vq[1], vq[2], vq[3]));
+    } else {
+        const uint4 wv = *reinterpret_cast<const uint4 *>(buf + 2 * kTile * 4 + 4 * e);
+        uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            ww[j] = packed_element<MODE, U1, ZS>(pp[j], gg[j], ww[j], s, bad, &zs);
+        store_stream(static_cast<uint32_t *>(d.s1) + base + e, make_uint4(ww[0], ww[1], ww[2], ww[3]));
+    }
+}
+
+// One staged vector whose gradients gv are already loaded.
+template <int MODE, bool U1, bool ZS>
+__device__ __forceinline__ void pipe_vector_g(const unsigned char *buf, int e, const Desc &d,
+                                              int64_t base, const float4 gv, const Scalars &s,
+                                              const ZeroSafe &zs, uint32_t &bad)
+{
+    const float4 pv = *reinterpret_cast<const float4 *>(buf + 4 * e);
+    float pp[4] = {pv.x, pv.y, pv.z, pv.w};
+    const float gg[4] = {gv.x, gv.y, gv.z, gv.w};
+    pipe_vector_math<MODE, U1, ZS>(buf, e, d, base, pp, gg, s, zs, bad);
+    store_stream(d.p + base + e, make_float4(pp[0], pp[1], pp[2], pp[3]));
+}
+
+__device__ __forceinline__ bool has_zero(const float4 g)
+{
+    return g.x == 0.0f || g.y == 0.0f || g.z == 0.0f || g.w == 0.0f;
+}
+
+__device__ __forceinline__ float4 staged_grad(const unsigned char *buf, int e)
+{
+    return *reinterpret_cast<const float4 *>(buf + kTile * 4 + 4 * e);
+}
+
+// Elements first, first+stride, ... below end, from global memory (head,
+// ragged tail, 4-byte-path tensors).  (Inlined: as an out-of-line call it
+// cost 2-9 % on GB300, the descriptor then living on the stack.)
+template <int MODE, bool U1>
+__device__ __forceinline__ uint32_t pipe_scalar_run(const Desc &d, int64_t first, int64_t end,
+                                                 int32_t stride, const Scalars &s)
+{
+    uint32_t bad = 0;
+    for (int64_t i = first; i < end; i += stride)
+        scalar_element<MODE, U1>(d, i, s, bad);
+    return bad;
+}
+
 template <int MODE, bool MULTI, bool U1>
 __device__ __forceinline__ void pipe_consume(const unsigned char *smem, uint64_t *full,
                                              uint64_t *empty, const Desc *table, int32_t ntensors,
@@ -414,6 +485,7 @@ __device__ __forceinline__ void pipe_consume(const unsigned char *smem, uint64_t
 {
     using L = PipeLayout<MODE>;
     const int ct = threadIdx.x;  // consumer thread, 0 .. kConsumers-1
+    const ZeroSafe zs = zero_safe_of(s);
     TableCursor<MULTI> cur(table, ntensors, total, single);
     int64_t k = 0;
     for (int64_t c = blockIdx.x; c < total; c += gridDim.x, ++k) {
@@ -428,51 +500,51 @@ __device__ __forceinline__ void pipe_consume(const unsigned char *smem, uint64_t
         const Span sp = tile_span(d, kt);
         if (d.vec) {
             const unsigned char *buf = smem + (size_t)st * L::kStageBytes;
+            // Whole tile without a zero gradient in this warp: every vector
+            // on the plain path, unrolled.  Otherwise one vector at a time,
+            // each warp-vector choosing the plain or the zero-safe arithmetic
+            // (one copy of each: the E4 element is large, and more inlined
+            // copies missed in the instruction cache on GB300).
+            bool fast = sp.len4 == kTile;  // uniform over the CTA
+            float4 gv[kTileVecs];
+            if (fast) {
+                bool z = false;
 #pragma unroll
-            for (int v = 0; v < kTileVecs; ++v) {
-                const int e = 4 * (ct + v * kConsumers);
-                if (e < sp.len4) {
-                    const float4 pv = *reinterpret_cast<const float4 *>(buf + 4 * e);
-                    const float4 gv = *reinterpret_cast<const float4 *>(buf + kTile * 4 + 4 * e);
-                    float pp[4] = {pv.x, pv.y, pv.z, pv.w};
-                    const float gg[4] = {gv.x, gv.y, gv.z, gv.w};
-                    float *P = d.p + sp.base + e;
-                    if constexpr (MODE == kF32) {
-                        const float4 mv = *reinterpret_cast<const float4 *>(buf + 2 * kTile * 4 + 4 * e);
-                        const float4 vv = *reinterpret_cast<const float4 *>(buf + 3 * kTile * 4 + 4 * e);
-                        float mm[4] = {mv.x, mv.y, mv.z, mv.w};
-                        float vq[4] = {vv.x, vv.y, vv.z, vv.w};
+                for (int v = 0; v < kTileVecs; ++v) {
+                    gv[v] = staged_grad(buf, 4 * (ct + v * kConsumers));
+                    z = z || has_zero(gv[v]);
+                }
+                fast = !__any_sync(0xFFFFFFFFu, z);
+            }
+            if (fast) {
 #pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const Moments o = adamw_element<U1>(pp[j], gg[j], mm[j], vq[j], s);
-                            bad += any_nonfinite(o);
-                            pp[j] = o.p;
-                            mm[j] = o.m;
-                            vq[j] = o.v;
-                        }
-                        store_stream(static_cast<float *>(d.s1) + sp.base + e,
-                                     make_float4(mm[0], mm[1], mm[2], mm[3]));
-                        store_stream(static_cast<float *>(d.s2) + sp.base + e,
-                                     make_float4(vq[0], vq[1], vq[2], vq[3]));
-                    } else {
-                        const uint4 wv = *reinterpret_cast<const uint4 *>(buf + 2 * kTile * 4 + 4 * e);
-                        uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            ww[j] = packed_element<MODE, U1>(pp[j], gg[j], ww[j], s, bad);
-                        store_stream(static_cast<uint32_t *>(d.s1) + sp.base + e,
-                                     make_uint4(ww[0], ww[1], ww[2], ww[3]));
+                for (int v = 0; v < kTileVecs; ++v)
+                    pipe_vector_g<MODE, U1, false>(buf, 4 * (ct + v * kConsumers), d, sp.base, gv[v],
+                                                   s, zs, bad);
+            } else {
+#pragma unroll 1
+                for (int v = 0; v < kTileVecs; ++v) {
+                    const int e = 4 * (ct + v * kConsumers);
+                    if (e < sp.len4) {
+                        const float4 g = staged_grad(buf, e);
+                        if (__any_sync(__activemask(), has_zero(g)))
+                            pipe_vector_g<MODE, U1, true>(buf, e, d, sp.base, g, s, zs, bad);
+                        else
+                            pipe_vector_g<MODE, U1, false>(buf, e, d, sp.base, g, s, zs, bad);
                     }
-                    store_stream(P, make_float4(pp[0], pp[1], pp[2], pp[3]));
                 }
             }
-            if (kt == 0 && ct < d.head)  // the <= 3 elements before the 16-byte body
-                scalar_element<MODE, U1>(d, ct, s, bad);
-            if (ct < sp.len - sp.len4)  // the <= 3 elements after the staged part
-                scalar_element<MODE, U1>(d, sp.base + sp.len4 + ct, s, bad);
+            // the <= 3 elements before the 16-byte body (first tile) and the
+            // <= 3 after the staged part (last tile), one per thread
+            const bool head = kt == 0 && ct < d.head, tail = ct < sp.len - sp.len4;
+            if (head || tail) {
+#pragma unroll 1
+                for (int r = head ? 0 : 1; r < (tail ? 2 : 1); ++r)
+                    bad += pipe_scalar_run<MODE, U1>(d, r == 0 ? ct : sp.base + sp.len4 + ct,
+                                                     (r == 0 ? ct : sp.base + sp.len4 + ct) + 1, 1, s);
+            }
         } else {
-            for (int j = ct; j < sp.len; j += kConsumers)
-                scalar_element<MODE, U1>(d, sp.base + j, s, bad);
+            bad += pipe_scalar_run<MODE, U1>(d, sp.base + ct, sp.base + sp.len, kConsumers, s);
         }
         __syncwarp();
         if ((ct & 31) == 0)
