@@ -699,15 +699,23 @@ struct BlockwiseArgs {
     int64_t n;
 };
 
+// Staged blockwise kernel: one CTA per SM; a tile is kBwGroups consecutive
+// 2048-element blocks of one tensor, and consumer group j (8 warps, 256
+// threads) updates block j of a tile.
+constexpr int kBwGroups = kConsumerWarps / 8;  // 3
+constexpr int kBwTile = kBwGroups * kBlock;    // 6144 elements
+constexpr int kBwStages = 2;
+constexpr size_t kBwStageBytes = (size_t)kBwTile * (4 + 4 + 1 + 1);  // p, g, m_code, v_code
+
 struct BlockwiseShared {
     float q1[256], q2[256], mid1[512], mid2[512];  // midpoints padded with +Inf
     uint8_t bucket1[kBuckets], bucket2[kBuckets];
-    uint32_t warp_max[2][2][kThreads / 32];  // [iteration parity][m, v][warp]
+    uint32_t warp_max[kBwGroups][2][2][8];  // [group][block parity][m, v][warp of the group]
     uint32_t red[2][32];
 };
+constexpr size_t kBwSmemBytes = kBwStages * kBwStageBytes + sizeof(BlockwiseShared) +
+                                2 * kBwStages * sizeof(uint64_t);
 
-// One 2048-element block.  WHOLE: every element is in range (all blocks but
-// a short last one), so no per-element bound logic is compiled in.
 // Redo, with the IEEE divide, the codes of the values that need it.
 __device__ __noinline__ uint2 requantise_fixup(float x0, float x1, float x2, float x3, float x4,
                                                float x5, float x6, float x7, float scale,
@@ -728,19 +736,21 @@ __device__ __noinline__ uint2 requantise_fixup(float x0, float x1, float x2, flo
 }
 
 // Codes of a thread's 8 values of one moment, block scale bits sb in the
-// FMA-division range.  Values that need the IEEE divide (tiny nonzero x) are
-// redone in a fix-up pass that is rarely entered.
+// FMA-division range.  Values that may need the IEEE divide (|x| below the
+// floor: tiny x, and zeros, whose fast code is right anyway) send the thread
+// through a fix-up pass that is rarely entered; one compare per value.
 template <int K>
 __device__ __forceinline__ uint2 requantise_fast(const float *x, uint32_t sb, const float *mid,
                                                  const uint8_t *table, int k)
 {
     const float scale = __uint_as_float(sb), y = __frcp_rn(scale);
     const uint32_t floor = fast_quotient_floor(sb);
+    const float floorf = __uint_as_float(floor);
     uint2 code = make_uint2(0u, 0u);
     bool fix = false;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        fix |= needs_ieee_divide(x[j], floor);
+        fix = fix || fabsf(x[j]) < floorf;
         const uint32_t cj = code_by_bucket<K>(mid, table, divide_by_scale_fma(x[j], scale, y), k);
         if (j < 4)
             code.x |= cj << (8 * j);
@@ -753,45 +763,36 @@ __device__ __forceinline__ uint2 requantise_fast(const float *x, uint32_t sb, co
     return code;
 }
 
+// One 2048-element block b, by one group of 256 threads (thread gt of the
+// group holds elements 4gt..4gt+3 and 1024+4gt..1024+4gt+3: pv, gv, and the
+// codes mc, vc packed four to a word).  WHOLE: every element is in range (all
+// blocks but a short last one), so no per-element bound logic is compiled in.
+// The block absmax is a warp max (redux.sync on the binary32 bits of |x|,
+// which orders non-negative floats and lets a NaN win) and a max over the
+// group's 8 warps through shared memory, between which the group meets at
+// its named barrier; `gpar` alternates the shared slots between consecutive
+// blocks of the group.
 template <bool WHOLE, int K>
 __device__ __forceinline__ void blockwise_block(const BlockwiseArgs &a, BlockwiseShared &sh,
-                                                int64_t b, int parity, const Scalars &s,
-                                                int k1, int k2, uint32_t &bad)
+                                                int64_t b, int group, int gt, uint32_t gpar,
+                                                const float pv[8], const float gv[8],
+                                                const uint32_t mc[2], const uint32_t vc[2],
+                                                const Scalars &s, int k1, int k2, uint32_t &bad)
 {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int lane = gt & 31, warp = gt >> 5;
     const int64_t base = b * kBlock;
     const float am = a.m_absmax[b], av = a.v_absmax[b];
     float mn[8], vn[8];
     uint32_t um = 0, uv = 0;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-        const int64_t e0 = base + 1024 * h + 4 * tid;
-        float pv[4], gv[4];
-        uint32_t mc, vc;
-        if (WHOLE) {
-            const float4 x = __ldg(reinterpret_cast<const float4 *>(a.p + e0));
-            const float4 y = __ldg(reinterpret_cast<const float4 *>(a.g + e0));
-            pv[0] = x.x; pv[1] = x.y; pv[2] = x.z; pv[3] = x.w;
-            gv[0] = y.x; gv[1] = y.y; gv[2] = y.z; gv[3] = y.w;
-            mc = *reinterpret_cast<const uint32_t *>(a.m_code + e0);
-            vc = *reinterpret_cast<const uint32_t *>(a.v_code + e0);
-        } else {
-            mc = vc = 0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const bool in = e0 + j < a.n;
-                pv[j] = in ? a.p[e0 + j] : 0.0f;
-                gv[j] = in ? a.g[e0 + j] : 0.0f;
-                mc |= (in ? (uint32_t)a.m_code[e0 + j] : 0u) << (8 * j);
-                vc |= (in ? (uint32_t)a.v_code[e0 + j] : 0u) << (8 * j);
-            }
-        }
+        const int64_t e0 = base + 1024 * h + 4 * gt;
         float po[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const float m = __fmul_rn(sh.q1[__byte_perm(mc, 0u, 0x4440u + j)], am);
-            const float v = __fmul_rn(sh.q2[__byte_perm(vc, 0u, 0x4440u + j)], av);
-            const Moments o = adamw_element(pv[j], gv[j], m, v, s);
+            const float m = __fmul_rn(sh.q1[__byte_perm(mc[h], 0u, 0x4440u + j)], am);
+            const float v = __fmul_rn(sh.q2[__byte_perm(vc[h], 0u, 0x4440u + j)], av);
+            const Moments o = adamw_element(pv[4 * h + j], gv[4 * h + j], m, v, s);
             po[j] = o.p;
             if (WHOLE || e0 + j < a.n) {
                 bad += any_nonfinite(o);
@@ -823,20 +824,20 @@ __device__ __forceinline__ void blockwise_block(const BlockwiseArgs &a, Blockwis
     um = __reduce_max_sync(0xFFFFFFFFu, um);
     uv = __reduce_max_sync(0xFFFFFFFFu, uv);
     if (lane == 0) {
-        sh.warp_max[parity][0][warp] = um;
-        sh.warp_max[parity][1][warp] = uv;
+        sh.warp_max[group][gpar][0][warp] = um;
+        sh.warp_max[group][gpar][1][warp] = uv;
     }
-    __syncthreads();
-    um = __reduce_max_sync(0xFFFFFFFFu, lane < kThreads / 32 ? sh.warp_max[parity][0][lane] : 0u);
-    uv = __reduce_max_sync(0xFFFFFFFFu, lane < kThreads / 32 ? sh.warp_max[parity][1][lane] : 0u);
-    if (tid == 0) {
+    asm volatile("bar.sync %0, 256;" ::"r"(1 + group) : "memory");
+    um = __reduce_max_sync(0xFFFFFFFFu, lane < 8 ? sh.warp_max[group][gpar][0][lane] : 0u);
+    uv = __reduce_max_sync(0xFFFFFFFFu, lane < 8 ? sh.warp_max[group][gpar][1][lane] : 0u);
+    if (gt == 0) {
         a.m_absmax[b] = __uint_as_float(um);
         a.v_absmax[b] = __uint_as_float(uv);
     }
     const uint32_t floor_bits = __float_as_uint(1e-30f);
     const uint32_t smb = max(um, floor_bits), svb = max(uv, floor_bits);  // NaN bits stay NaN
     uint32_t mcode[2], vcode[2];
-    if (scale_in_fast_range(smb)) {  // uniform over the CTA
+    if (scale_in_fast_range(smb)) {  // uniform over the group
         const uint2 cm = requantise_fast<K>(mn, smb, sh.mid1, sh.bucket1, k1);
         mcode[0] = cm.x;
         mcode[1] = cm.y;
@@ -858,7 +859,7 @@ __device__ __forceinline__ void blockwise_block(const BlockwiseArgs &a, Blockwis
     }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-        const int64_t e0 = base + 1024 * h + 4 * tid;
+        const int64_t e0 = base + 1024 * h + 4 * gt;
         if (WHOLE) {
             *reinterpret_cast<uint32_t *>(a.m_code + e0) = mcode[h];
             *reinterpret_cast<uint32_t *>(a.v_code + e0) = vcode[h];
@@ -874,88 +875,221 @@ __device__ __forceinline__ void blockwise_block(const BlockwiseArgs &a, Blockwis
 }
 
 // Per-CTA set-up: maps, midpoints (+Inf padded) and the two bucket tables;
-// returns the largest bucket population of each map.
+// returns the largest bucket population of each map.  Every thread of the CTA
+// takes part.
 __device__ __forceinline__ void blockwise_setup(BlockwiseShared &sh, const float *__restrict__ qmap1,
                                                 const float *__restrict__ qmap2, int &k1, int &k2)
 {
     const int tid = threadIdx.x;
-    sh.q1[tid] = __ldg(qmap1 + tid);
-    sh.q2[tid] = __ldg(qmap2 + tid);
+    if (tid < 256) {
+        sh.q1[tid] = __ldg(qmap1 + tid);
+        sh.q2[tid] = __ldg(qmap2 + tid);
+    }
     __syncthreads();
-    sh.mid1[tid] = tid < 255 ? __fmul_rn(__fadd_rn(sh.q1[tid], sh.q1[tid + 1]), 0.5f) : INFINITY;
-    sh.mid2[tid] = tid < 255 ? __fmul_rn(__fadd_rn(sh.q2[tid], sh.q2[tid + 1]), 0.5f) : INFINITY;
-    sh.mid1[256 + tid] = INFINITY;
-    sh.mid2[256 + tid] = INFINITY;
+    if (tid < 256) {
+        sh.mid1[tid] = tid < 255 ? __fmul_rn(__fadd_rn(sh.q1[tid], sh.q1[tid + 1]), 0.5f) : INFINITY;
+        sh.mid2[tid] = tid < 255 ? __fmul_rn(__fadd_rn(sh.q2[tid], sh.q2[tid + 1]), 0.5f) : INFINITY;
+        sh.mid1[256 + tid] = INFINITY;
+        sh.mid2[256 + tid] = INFINITY;
+    }
     __syncthreads();
     k1 = build_buckets(sh.mid1, sh.bucket1, sh.red[0]);
     k2 = build_buckets(sh.mid2, sh.bucket2, sh.red[1]);
     __syncthreads();
 }
 
-// Block b of one tensor: the comparison count is fixed at compile time when
-// every bucket of both maps holds at most one (or two) midpoints.
-__device__ __forceinline__ void blockwise_dispatch(const BlockwiseArgs &a, BlockwiseShared &sh,
-                                                   int64_t b, int parity, const Scalars &s,
-                                                   int k1, int k2, uint32_t &bad)
-{
-    const int k = k1 > k2 ? k1 : k2;
-    if (b < a.n / kBlock) {
-        if (k <= 1)
-            blockwise_block<true, 1>(a, sh, b, parity, s, k1, k2, bad);
-        else if (k <= 2)
-            blockwise_block<true, 2>(a, sh, b, parity, s, k1, k2, bad);
-        else
-            blockwise_block<true, 0>(a, sh, b, parity, s, k1, k2, bad);
-    } else {
-        blockwise_block<false, 0>(a, sh, b, parity, s, k1, k2, bad);
-    }
-}
-
-__global__ void __launch_bounds__(kThreads, 4)
-blockwise8_kernel(const BlockwiseArgs a, const float *__restrict__ qmap1,
-                  const float *__restrict__ qmap2, int64_t nblocks, const Scalars s,
-                  unsigned long long *nonfinite)
-{
-    __shared__ BlockwiseShared sh;
-    int k1, k2;
-    blockwise_setup(sh, qmap1, qmap2, k1, k2);
-    uint32_t bad = 0;
-    int parity = 0;
-    for (int64_t b = blockIdx.x; b < nblocks; b += gridDim.x, parity ^= 1)
-        blockwise_dispatch(a, sh, b, parity, s, k1, k2, bad);
-    flush_nonfinite(bad, nonfinite);
-}
-
-// One tensor of a blockwise list; block0 = its first block in the list's
-// concatenated block index.
+// One tensor of a blockwise list; item0 = its first work item in the list.
+// A tensor's work items are its tiles of kBwGroups whole blocks (the last
+// tile may hold fewer) and, when n is not a multiple of 2048, one more item:
+// the short last block.
 struct BwDesc {
     BlockwiseArgs a;
-    int64_t block0;
+    int64_t item0;
 };
 
-// Tensor-list form: a persistent grid over the concatenated blocks of every
-// tensor; each CTA walks the descriptor table forward.
-__global__ void __launch_bounds__(kThreads, 4)
-blockwise8_multi_kernel(const BwDesc *__restrict__ table, int32_t ntensors, int64_t total_blocks,
-                        const float *__restrict__ qmap1, const float *__restrict__ qmap2,
-                        const Scalars s, unsigned long long *nonfinite)
+__host__ __device__ __forceinline__ int64_t bw_full_tiles(int64_t n)
 {
-    __shared__ BlockwiseShared sh;
-    int k1, k2;
-    blockwise_setup(sh, qmap1, qmap2, k1, k2);
-    uint32_t bad = 0;
-    int parity = 0;
-    int32_t t = 0;
-    BwDesc d = table[0];
-    int64_t next = ntensors > 1 ? table[1].block0 : total_blocks;
-    for (int64_t b = blockIdx.x; b < total_blocks; b += gridDim.x, parity ^= 1) {
-        while (b >= next) {
-            ++t;
-            d = table[t];
-            next = t + 1 < ntensors ? table[t + 1].block0 : total_blocks;
+    return (n / kBlock + kBwGroups - 1) / kBwGroups;
+}
+
+template <bool MULTI>
+struct BwCursor {
+    const BwDesc *table;
+    int32_t ntensors, t;
+    int64_t next;
+    BwDesc d;
+    __device__ __forceinline__ BwCursor(const BwDesc *tab, int32_t nt, int64_t total, const BwDesc &single)
+        : table(tab), ntensors(nt), t(0), next(total), d(single)
+    {
+        if (MULTI) {
+            d = table[0];
+            next = ntensors > 1 ? table[1].item0 : total;
         }
-        blockwise_dispatch(d.a, sh, b - d.block0, parity, s, k1, k2, bad);
     }
+    __device__ __forceinline__ void seek(int64_t c, int64_t total)
+    {
+        if (MULTI)
+            while (c >= next) {
+                ++t;
+                d = table[t];
+                next = t + 1 < ntensors ? table[t + 1].item0 : total;
+            }
+    }
+};
+
+__device__ __forceinline__ bool codes_staged(const BlockwiseArgs &a)
+{
+    return ((reinterpret_cast<uintptr_t>(a.m_code) | reinterpret_cast<uintptr_t>(a.v_code)) & 15u) == 0;
+}
+
+template <bool MULTI>
+__device__ __forceinline__ void bw_produce(unsigned char *smem, uint64_t *full, uint64_t *empty,
+                                           const BwDesc *table, int32_t ntensors, int64_t total,
+                                           const BwDesc &single)
+{
+    BwCursor<MULTI> cur(table, ntensors, total, single);
+    int64_t k = 0;
+    for (int64_t c = blockIdx.x; c < total; c += gridDim.x, ++k) {
+        cur.seek(c, total);
+        const int st = (int)(k % kBwStages);
+        const uint32_t use = (uint32_t)(k / kBwStages);
+        if (!mbar_wait(&empty[st], (use & 1u) ^ 1u)) {
+            pipe_fault(kFaultEmptyWait);
+            break;
+        }
+        const BlockwiseArgs &a = cur.d.a;
+        const int64_t kt = c - cur.d.item0;
+        const int64_t nf = a.n / kBlock;
+        if (kt < bw_full_tiles(a.n)) {
+            const int64_t b0 = kt * kBwGroups;
+            const int64_t nb = nf - b0 < kBwGroups ? nf - b0 : kBwGroups;
+            const uint32_t elems = (uint32_t)(nb * kBlock);
+            const int64_t e0 = b0 * kBlock;
+            const bool codes = codes_staged(a);
+            mbar_arrive_expect(&full[st], elems * (codes ? 10u : 8u));
+            unsigned char *buf = smem + (size_t)st * kBwStageBytes;
+            bulk_load(buf, a.p + e0, elems * 4u, &full[st]);
+            bulk_load(buf + kBwTile * 4, a.g + e0, elems * 4u, &full[st]);
+            if (codes) {
+                bulk_load(buf + kBwTile * 8, a.m_code + e0, elems, &full[st]);
+                bulk_load(buf + kBwTile * 9, a.v_code + e0, elems, &full[st]);
+            }
+        } else {
+            mbar_arrive_expect(&full[st], 0u);  // the short last block: read from global memory
+        }
+    }
+    for (int64_t j = k > kBwStages ? k - kBwStages : 0; j < k; ++j)
+        if (!mbar_wait(&full[j % kBwStages], (uint32_t)((j / kBwStages) & 1)))
+            pipe_fault(kFaultCopyWait);
+}
+
+template <bool MULTI>
+__device__ __forceinline__ void bw_consume(const unsigned char *smem, uint64_t *full, uint64_t *empty,
+                                           BlockwiseShared &sh, const BwDesc *table,
+                                           int32_t ntensors, int64_t total, const BwDesc &single,
+                                           const Scalars &s, int k1, int k2, uint32_t &bad)
+{
+    const int group = threadIdx.x >> 8, gt = threadIdx.x & 255;
+    const int kmax = k1 > k2 ? k1 : k2;
+    uint32_t gpar = 0;
+    BwCursor<MULTI> cur(table, ntensors, total, single);
+    int64_t k = 0;
+    for (int64_t c = blockIdx.x; c < total; c += gridDim.x, ++k) {
+        cur.seek(c, total);
+        const int st = (int)(k % kBwStages);
+        if (!mbar_wait(&full[st], (uint32_t)((k / kBwStages) & 1))) {
+            pipe_fault(kFaultFullWait);
+            break;
+        }
+        const BlockwiseArgs &a = cur.d.a;
+        const int64_t kt = c - cur.d.item0;
+        const int64_t nf = a.n / kBlock;
+        const bool tile = kt < bw_full_tiles(a.n);
+        const int64_t b = tile ? kt * kBwGroups + group : nf;
+        const bool mine = tile ? b < nf : group == 0;
+        // this thread's elements and codes, into registers
+        float pv[8], gv[8];
+        uint32_t mc[2] = {0u, 0u}, vc[2] = {0u, 0u};
+        if (tile && mine) {
+            const unsigned char *buf = smem + (size_t)st * kBwStageBytes;
+            const int o = group * kBlock + 4 * gt;
+            const bool codes = codes_staged(a);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const float4 x = *reinterpret_cast<const float4 *>(buf + 4 * (o + 1024 * h));
+                const float4 y = *reinterpret_cast<const float4 *>(buf + kBwTile * 4 + 4 * (o + 1024 * h));
+                pv[4 * h] = x.x; pv[4 * h + 1] = x.y; pv[4 * h + 2] = x.z; pv[4 * h + 3] = x.w;
+                gv[4 * h] = y.x; gv[4 * h + 1] = y.y; gv[4 * h + 2] = y.z; gv[4 * h + 3] = y.w;
+                if (codes) {
+                    mc[h] = *reinterpret_cast<const uint32_t *>(buf + kBwTile * 8 + o + 1024 * h);
+                    vc[h] = *reinterpret_cast<const uint32_t *>(buf + kBwTile * 9 + o + 1024 * h);
+                } else {
+                    const int64_t e = b * kBlock + 1024 * h + 4 * gt;
+                    mc[h] = *reinterpret_cast<const uint32_t *>(a.m_code + e);
+                    vc[h] = *reinterpret_cast<const uint32_t *>(a.v_code + e);
+                }
+            }
+        } else if (mine) {  // the short last block, from global memory
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int64_t e0 = b * kBlock + 1024 * h + 4 * gt;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const bool in = e0 + j < a.n;
+                    pv[4 * h + j] = in ? a.p[e0 + j] : 0.0f;
+                    gv[4 * h + j] = in ? a.g[e0 + j] : 0.0f;
+                    mc[h] |= (in ? (uint32_t)a.m_code[e0 + j] : 0u) << (8 * j);
+                    vc[h] |= (in ? (uint32_t)a.v_code[e0 + j] : 0u) << (8 * j);
+                }
+            }
+        }
+        // the stage is no longer read: hand it back before computing
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0)
+            mbar_arrive(&empty[st]);
+        if (mine) {
+            // whole blocks with at most one midpoint per bucket (the log-linear
+            // maps): the specialised body; anything else: the generic one
+            if (tile && kmax <= 1)
+                blockwise_block<true, 1>(a, sh, b, group, gt, gpar, pv, gv, mc, vc, s, k1, k2, bad);
+            else
+                blockwise_block<false, 0>(a, sh, b, group, gt, gpar, pv, gv, mc, vc, s, k1, k2, bad);
+            gpar ^= 1u;
+        }
+    }
+}
+
+// The blockwise step over a tensor list (MULTI) or one tensor.  One CTA per
+// SM: the producer warp stages p, g and (when both code arrays are 16-byte
+// aligned) the two code arrays of a tile of kBwGroups blocks; three groups of
+// 8 consumer warps update one block each.
+template <bool MULTI>
+__global__ void __launch_bounds__(kPipeThreads, 1)
+blockwise8_pipe_kernel(const BwDesc *__restrict__ table, int32_t ntensors, int64_t total_items,
+                       const BwDesc single, const float *__restrict__ qmap1,
+                       const float *__restrict__ qmap2, const Scalars s,
+                       unsigned long long *nonfinite)
+{
+    extern __shared__ __align__(128) unsigned char bw_smem[];
+    BlockwiseShared &sh = *reinterpret_cast<BlockwiseShared *>(bw_smem + kBwStages * kBwStageBytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(bw_smem + kBwStages * kBwStageBytes + sizeof(BlockwiseShared));
+    uint64_t *empty = full + kBwStages;
+    int k1, k2;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kBwStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kConsumerWarps);
+        }
+        mbar_init_fence();
+    }
+    blockwise_setup(sh, qmap1, qmap2, k1, k2);  // ends with __syncthreads
+    if (threadIdx.x >= kConsumers) {
+        if (threadIdx.x == kConsumers)
+            bw_produce<MULTI>(bw_smem, full, empty, table, ntensors, total_items, single);
+        return;
+    }
+    uint32_t bad = 0;
+    bw_consume<MULTI>(bw_smem, full, empty, sh, table, ntensors, total_items, single, s, k1, k2, bad);
     flush_nonfinite(bad, nonfinite);
 }
 
@@ -1023,8 +1157,8 @@ pa_status make_scalars(int64_t step, double lr, double beta1, double beta2, doub
 
 // ---- per-device launch geometry --------------------------------------------
 // Kernels launched with kThreads threads and no dynamic shared memory: the
-// register-staged step (bfloat16 gradients), the blockwise step, the codecs.
-enum KernelSlot { kSlotBf16, kSlotBf16Multi, kSlotBlockwise, kSlotCodec, kNumSlots };
+// register-staged step (bfloat16 gradients) and the codecs.
+enum KernelSlot { kSlotBf16, kSlotBf16Multi, kSlotCodec, kNumSlots };
 
 struct DeviceInfo {
     bool ready = false;
@@ -1040,7 +1174,6 @@ const void *kernel_of(int slot)
     switch (slot) {
     case kSlotBf16: return (const void *)pa::adamw_step_kernel<pa::kE4, false, false, __nv_bfloat16>;
     case kSlotBf16Multi: return (const void *)pa::adamw_step_kernel<pa::kE4, true, false, __nv_bfloat16>;
-    case kSlotBlockwise: return (const void *)pa::blockwise8_kernel;
     default: return (const void *)pa::encode_state_kernel<pa::kE4>;
     }
 }
@@ -1556,14 +1689,17 @@ pa_status pa_adamw_step_blockwise8(const float *p, const float *g, uint16_t *p_b
         return fail(PA_ERR_ALIGN, "absmax arrays and maps must be 4-byte aligned");
     if ((st = check_counter(nonfinite)) != PA_OK)
         return st;
-    const int64_t nblocks = (n + pa::kBlock - 1) / pa::kBlock;
+    pa::BwDesc d;
+    d.a = {p, g, p_bf16, m_code, m_absmax, v_code, v_absmax, n};
+    d.item0 = 0;
+    const int64_t items = pa::bw_full_tiles(n) + (n % pa::kBlock != 0 ? 1 : 0);
     int grid = 0;
-    if ((st = grid_for(kSlotBlockwise, nblocks, &grid)) != PA_OK)
+    if ((st = pipe_grid((const void *)pa::blockwise8_pipe_kernel<false>, pa::kBwSmemBytes, items,
+                        &grid)) != PA_OK)
         return st;
-    const pa::BlockwiseArgs args = {p, g, p_bf16, m_code, m_absmax, v_code, v_absmax, n};
-    pa::blockwise8_kernel<<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
-        args, qmap1, qmap2, nblocks, s, nonfinite);
-    return check_launch("blockwise8_kernel launch");
+    pa::blockwise8_pipe_kernel<false><<<grid, pa::kPipeThreads, pa::kBwSmemBytes, (cudaStream_t)stream>>>(
+        nullptr, 1, items, d, qmap1, qmap2, s, nonfinite);
+    return check_launch("blockwise8_pipe_kernel launch");
 }
 
 pa_status pa_shutdown(void)
@@ -1964,7 +2100,7 @@ struct BwTable {
     int device;
     std::vector<pa::BwDesc> host;
     pa::BwDesc *dev;
-    int64_t blocks;
+    int64_t items;  // work items of the staged kernel
     uint64_t last_use;
 };
 
@@ -1989,15 +2125,15 @@ pa_status check_blockwise_tensor(const pa_blockwise_tensor &t, int index)
 }
 
 pa_status bw_table_for(const pa_blockwise_tensor *list, int32_t ntensors, const pa::BwDesc **out,
-                       int64_t *blocks)
+                       int64_t *items)
 {
     std::vector<pa::BwDesc> host((size_t)ntensors);
     int64_t total = 0;
     for (int32_t i = 0; i < ntensors; ++i) {
         const pa_blockwise_tensor &t = list[i];
         host[(size_t)i].a = {t.p, t.g, t.p_bf16, t.m_code, t.m_absmax, t.v_code, t.v_absmax, t.n};
-        host[(size_t)i].block0 = total;
-        total += (t.n + pa::kBlock - 1) / pa::kBlock;
+        host[(size_t)i].item0 = total;
+        total += pa::bw_full_tiles(t.n) + (t.n % pa::kBlock != 0 ? 1 : 0);
     }
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -2010,7 +2146,7 @@ pa_status bw_table_for(const pa_blockwise_tensor *list, int32_t ntensors, const 
             std::memcmp(t.host.data(), host.data(), host.size() * sizeof(pa::BwDesc)) == 0) {
             t.last_use = g_bw_tick;
             *out = t.dev;
-            *blocks = t.blocks;
+            *items = t.items;
             return PA_OK;
         }
     if (g_bw_tables.size() >= kMaxTables) {
@@ -2026,7 +2162,7 @@ pa_status bw_table_for(const pa_blockwise_tensor *list, int32_t ntensors, const 
     }
     BwTable t;
     t.device = dev;
-    t.blocks = total;
+    t.items = total;
     t.last_use = g_bw_tick;
     t.dev = nullptr;
     const size_t bytes = host.size() * sizeof(pa::BwDesc);
@@ -2042,7 +2178,7 @@ pa_status bw_table_for(const pa_blockwise_tensor *list, int32_t ntensors, const 
     t.host = std::move(host);
     g_bw_tables.push_back(std::move(t));
     *out = g_bw_tables.back().dev;
-    *blocks = g_bw_tables.back().blocks;
+    *items = g_bw_tables.back().items;
     return PA_OK;
 }
 
@@ -2078,15 +2214,18 @@ extern "C" pa_status pa_adamw_step_blockwise8_multi(const pa_blockwise_tensor *l
     if (total == 0)
         return ok();
     const pa::BwDesc *table = nullptr;
-    int64_t blocks = 0;
-    if ((st = bw_table_for(list, ntensors, &table, &blocks)) != PA_OK)
+    int64_t items = 0;
+    if ((st = bw_table_for(list, ntensors, &table, &items)) != PA_OK)
         return st;
     int grid = 0;
-    if ((st = grid_for(kSlotBlockwise, blocks, &grid)) != PA_OK)
+    if ((st = pipe_grid((const void *)pa::blockwise8_pipe_kernel<true>, pa::kBwSmemBytes, items,
+                        &grid)) != PA_OK)
         return st;
-    pa::blockwise8_multi_kernel<<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
-        table, ntensors, blocks, qmap1, qmap2, s, nonfinite);
-    return check_launch("blockwise8_multi_kernel launch");
+    pa::BwDesc none;
+    std::memset(&none, 0, sizeof none);
+    pa::blockwise8_pipe_kernel<true><<<grid, pa::kPipeThreads, pa::kBwSmemBytes, (cudaStream_t)stream>>>(
+        table, ntensors, items, none, qmap1, qmap2, s, nonfinite);
+    return check_launch("blockwise8_pipe_kernel (multi) launch");
 }
 
 pa_status release_blockwise_tables()

@@ -47,7 +47,7 @@ import workloads as wl  # noqa: E402
 
 BYTES_PER_PARAM = {"e4": 20, "fp16": 20, "fp32": 28, "blockwise": 14 + 16 / 2048}
 KERNEL_NAME = {"e4": "adamw_step_pipe_kernel<0,true>", "fp16": "adamw_step_pipe_kernel<1,true>",
-               "fp32": "adamw_step_pipe_kernel<2,true>", "blockwise": "blockwise8_kernel"}
+               "fp32": "adamw_step_pipe_kernel<2,true>", "blockwise": "blockwise8_pipe_kernel<false>"}
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_HBM_GBS = 6800.0
 
