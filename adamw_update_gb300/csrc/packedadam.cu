@@ -1157,8 +1157,9 @@ pa_status make_scalars(int64_t step, double lr, double beta1, double beta2, doub
 
 // ---- per-device launch geometry --------------------------------------------
 // Kernels launched with kThreads threads and no dynamic shared memory: the
-// register-staged step (bfloat16 gradients) and the codecs.
-enum KernelSlot { kSlotBf16, kSlotBf16Multi, kSlotCodec, kNumSlots };
+// register-staged step (bfloat16 gradients; FP32 gradients in host memory)
+// and the codecs.
+enum KernelSlot { kSlotBf16, kSlotBf16Multi, kSlotHostE4, kSlotCodec, kNumSlots };
 
 struct DeviceInfo {
     bool ready = false;
@@ -1174,6 +1175,7 @@ const void *kernel_of(int slot)
     switch (slot) {
     case kSlotBf16: return (const void *)pa::adamw_step_kernel<pa::kE4, false, false, __nv_bfloat16>;
     case kSlotBf16Multi: return (const void *)pa::adamw_step_kernel<pa::kE4, true, false, __nv_bfloat16>;
+    case kSlotHostE4: return (const void *)pa::adamw_step_kernel<pa::kE4, false, false, float>;
     default: return (const void *)pa::encode_state_kernel<pa::kE4>;
     }
 }
@@ -1898,6 +1900,53 @@ pa_status host_pipe(int dev, HostPipe **out)
     return PA_OK;
 }
 
+// The device address of page-locked host memory mapped into the device's
+// address space (cudaHostAlloc / cudaMallocHost / cudaHostRegister), or false.
+bool device_view(const void *host, void **dev)
+{
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, host) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (a.type != cudaMemoryTypeHost || a.devicePointer == nullptr)
+        return false;
+    *dev = a.devicePointer;
+    return true;
+}
+
+// The step with the GPU reading and writing the mapped host arrays in place:
+// every byte crosses the host link once (12 in, 8 out per parameter), both
+// directions at once, with no copies and no staging in device memory.  The
+// register-staged kernel (plain 16-byte loads and stores) is used: the bulk
+// copies of the staged kernel are kept to device memory.
+pa_status host_step_in_place(float *p, const float *g, uint32_t *state, int64_t n, int64_t step,
+                             double lr, double beta1, double beta2, double eps, double wd,
+                             unsigned long long *nonfinite, pa_stream stream)
+{
+    Scalars s;
+    pa_status st = make_scalars(step, lr, beta1, beta2, eps, wd, &s);
+    if (st != PA_OK)
+        return st;
+    const pa_tensor t = {p, g, state, nullptr, n};
+    Desc d;
+    int64_t chunk = 0;
+    if ((st = chunk_size(kSlotHostE4, n, &chunk)) != PA_OK)
+        return st;
+    const int64_t chunks = describe(t, pa::kE4, chunk, &d);
+    d.chunk0 = 0;
+    int grid = 0;
+    if ((st = grid_for(kSlotHostE4, chunks, &grid)) != PA_OK)
+        return st;
+    if (s.bc2 == 1.0f)
+        pa::adamw_step_kernel<pa::kE4, false, true, float><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
+            nullptr, 1, chunks, chunk, d, s, nonfinite);
+    else
+        pa::adamw_step_kernel<pa::kE4, false, false, float><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
+            nullptr, 1, chunks, chunk, d, s, nonfinite);
+    return check_launch("adamw_step_kernel (host memory in place) launch");
+}
+
 }  // namespace
 
 extern "C" pa_status pa_adamw_step_packed_e4_host(float *p, const float *g, uint32_t *state,
@@ -1926,6 +1975,13 @@ extern "C" pa_status pa_adamw_step_packed_e4_host(float *p, const float *g, uint
         return st;
     // per stage: p, g, word arrays of `chunk` elements, each a multiple of 64
     int64_t chunk = workspace_bytes / (kHostStages * 12) / 64 * 64;
+    if (chunk >= 65536) {
+        void *dp = nullptr, *dg = nullptr, *ds = nullptr;
+        if (device_view(p, &dp) && device_view(g, &dg) && device_view(state, &ds))
+            return host_step_in_place(static_cast<float *>(dp), static_cast<const float *>(dg),
+                                      static_cast<uint32_t *>(ds), n, step, lr, beta1, beta2, eps,
+                                      wd, nonfinite, stream);
+    }
     if (chunk < 65536)
         return fail(PA_ERR_ARG, "workspace of %lld bytes is below the minimum of %lld "
                     "(3 stages x 12 bytes x 65536 elements)", (long long)workspace_bytes,

@@ -584,7 +584,8 @@ def measure_e2e(pa, w, hy, args, stream, nonfinite):
     if w.mode == "e4" and len(w.sizes) == 1 and not w.grad_bf16:
         ws = torch.empty(3 * 12 * (1 << 26), dtype=torch.uint8, device=w.p.device)
         hp, hg, hs = host[id(w.p)], host[id(w.g)], host[id(w.s[0])]
-        api = "pa_adamw_step_packed_e4_host (pinned host tensors, 2.4 GB workspace)"
+        api = ("pa_adamw_step_packed_e4_host (pinned host tensors, read and written in place over "
+               "the host link by the step kernel; its 2.4 GB workspace is not used then)")
 
         def one(t):
             pa.pa_adamw_step_packed_e4_host(hp, hg, hs, ws, t, nonfinite=nonfinite, **hy)

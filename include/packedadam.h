@@ -236,19 +236,23 @@ pa_status pa_adamw_step_packed_e4_multi_noalloc(const pa_tensor *list, int32_t n
  * off the device ("Packed AdamW Reference" README, "The canonical format": the
  * state is 4 bytes per parameter instead of 8, which also shrinks the traffic
  * over the host link: 12 bytes in and 8 bytes out per parameter).
- * p, g, state: host arrays of n elements, 4-byte aligned; page-locked memory
- * (cudaMallocHost or cudaHostRegister) lets the copies run asynchronously and
+ * p, g, state: host arrays of n elements, 4-byte aligned.
+ * When all three are page-locked and mapped into the device's address space
+ * (cudaHostAlloc / cudaMallocHost / cudaHostRegister; torch's pin_memory), the
+ * step kernel reads and writes them in place over the host link (one launch
+ * on `stream`, both link directions at once, no copies; the workspace is
+ * checked but not used).  Otherwise the call streams the arrays through the
+ * workspace: page-locked memory lets those copies run asynchronously and
  * overlap, pageable memory works but copies synchronously.
  * workspace: caller-owned device memory, 256-byte aligned, of workspace_bytes
- * >= 3 * 12 * 65536 bytes; the call streams the arrays through it in chunks of
- * workspace_bytes / 36 elements (three rotating stages), overlapping uploads,
- * the step and downloads on two internal streams (created on the first call on
- * a device) and `stream`.  The call returns after queueing; `stream` is
- * ordered after the last download, so synchronising `stream` makes the host
- * arrays current.  Host enqueues are serialised by a process-wide lock; the
- * workspace and host arrays must not be touched until `stream` has passed the
- * call.  Errors as for the other steps; a workspace below the minimum is
- * PA_ERR_ARG, a misaligned one PA_ERR_ALIGN.
+ * >= 3 * 12 * 65536 bytes; chunks of workspace_bytes / 36 elements (three
+ * rotating stages), overlapping uploads, the step and downloads on two
+ * internal streams (created on the first call on a device) and `stream`.
+ * Either way the call returns after queueing and synchronising `stream` makes
+ * the host arrays current.  Host enqueues are serialised by a process-wide
+ * lock; the workspace and host arrays must not be touched until `stream` has
+ * passed the call.  Errors as for the other steps; a workspace below the
+ * minimum is PA_ERR_ARG, a misaligned one PA_ERR_ALIGN.
  * ------------------------------------------------------------------------- */
 pa_status pa_adamw_step_packed_e4_host(float *p, const float *g, uint32_t *state, int64_t n,
                                        int64_t step, double lr, double beta1, double beta2,

@@ -1,7 +1,8 @@
-"""The packed-E4 step over host-resident tensors (pa_adamw_step_packed_e4_host):
-streamed through a small device workspace in many chunks, bit for bit equal to
-the oracle, with pinned and with pageable host memory, a ragged last chunk and
-two calls in a row ("Packed AdamW Reference" README, "The canonical format":
+"""The packed-E4 step over host-resident tensors (pa_adamw_step_packed_e4_host),
+bit for bit equal to the oracle: pinned tensors (the kernel reads and writes
+them in place over the host link), pageable or mixed ones (streamed through a
+small device workspace in many chunks with a ragged last chunk), views into
+pinned buffers at odd offsets, two calls in a row ("Packed AdamW Reference" README, "The canonical format":
 the 4-byte state word is what travels between host and device)."""
 import numpy as np
 import pytest
@@ -65,3 +66,40 @@ def test_host_step_small_tensor_and_errors():
     with pytest.raises(pa.PackedAdamError) as e:
         pa.pa_adamw_step_packed_e4_host(hp, hg, hs, ws[1:], 2, **HY)
     assert e.value.status == 3
+
+
+@pytest.mark.parametrize("case", ["mixed", "offset_views"])
+def test_host_step_in_place_and_mixed(case):
+    """offset_views: pinned buffers, views starting at 4-byte offsets (in
+    place, 4-byte path); mixed: pinned p and state with a pageable gradient
+    (streamed through the workspace)."""
+    import torch
+
+    import adamw_update_gb300 as pa
+
+    n = 300_007
+    rng = np.random.default_rng(7)
+    p = rng.normal(0, 0.02, n).astype(np.float32)
+    st = rng.integers(0, 1 << 31, n).astype(np.uint32)
+    bp = torch.zeros(n + 4, dtype=torch.float32).pin_memory()
+    bs = torch.zeros(n + 4, dtype=torch.int32).pin_memory()
+    bg = torch.zeros(n + 4, dtype=torch.float32).pin_memory()
+    o = (1, 3, 2) if case == "offset_views" else (0, 0, 0)
+    hp, hs = bp[o[0]:o[0] + n], bs[o[1]:o[1] + n]
+    hp.copy_(torch.from_numpy(p))
+    hs.copy_(torch.from_numpy(st.view(np.int32)))
+    ws = torch.empty(3 * 12 * 65536, dtype=torch.uint8, device="cuda")
+    bad = torch.zeros(1, dtype=torch.int64, device="cuda")
+    for t in (1, 2):
+        g = rng.normal(0, 1e-3, n).astype(np.float32)
+        if case == "offset_views":
+            hg = bg[o[2]:o[2] + n]
+            hg.copy_(torch.from_numpy(g))
+        else:
+            hg = torch.from_numpy(g)
+        pa.pa_adamw_step_packed_e4_host(hp, hg, hs, ws, t, nonfinite=bad, **HY)
+        torch.cuda.current_stream().synchronize()
+        p, st, _ = oracle.step_packed(p, g, st, t, **HY)
+        assert np.array_equal(hp.numpy().view(np.uint32), p.view(np.uint32)), f"p, call {t}"
+        assert np.array_equal(hs.numpy().view(np.uint32), st), f"state, call {t}"
+    assert int(bad.item()) == 0
