@@ -303,11 +303,18 @@ constexpr int kPipeThreads = kConsumers + 32;  // + the producer warp
 constexpr int kTileVecs = kTile / (4 * kConsumers);
 static_assert(kTile % (4 * kConsumers) == 0, "a tile is whole 16-byte vectors per consumer");
 
-template <int MODE>
+// A stage holds one tile of each stream: p, g (GT: float or bfloat16), the
+// state word or m, and v in the FP32 mode.
+template <int MODE, typename GT = float>
 struct PipeLayout {
-    static constexpr int kStreams = MODE == kF32 ? 4 : 3;  // p, g, word | p, g, m, v
-    static constexpr size_t kStageBytes = (size_t)kStreams * kTile * 4;
+    static constexpr size_t kG = (size_t)kTile * 4;                 // gradients
+    static constexpr size_t kS1 = kG + (size_t)kTile * sizeof(GT);  // state word | m
+    static constexpr size_t kS2 = kS1 + (size_t)kTile * 4;          // v (FP32 mode)
+    static constexpr size_t kStageBytes = MODE == kF32 ? kS2 + (size_t)kTile * 4 : kS2;
     static constexpr size_t kBytes = kStages * kStageBytes + 2 * kStages * sizeof(uint64_t);
+    static constexpr uint32_t kBytesPerElem = (uint32_t)(kStageBytes / kTile);
+    // a staged run is whole 16-byte units of every stream: 4 elements, 8 for bfloat16
+    static constexpr int kUnit = sizeof(GT) == 2 ? 8 : 4;
 };
 
 // Set (first code wins) when a bounded wait of a staged kernel gives up; the
@@ -324,14 +331,15 @@ __device__ __forceinline__ void pipe_fault(uint32_t code)
     atomicCAS(&g_pipe_fault, 0u, code);
 }
 
-// Elements [base, base + len) of the tensor form tile k; the first len4 of
-// them (a multiple of 4) are staged by bulk copies (0 on the 4-byte path).
+// Elements [base, base + len) of the tensor form tile k; the first `staged`
+// of them (whole units of `unit` elements: 4, or 8 with bfloat16 gradients)
+// are staged by bulk copies (none on the 4-byte path).
 struct Span {
     int64_t base;
-    int32_t len, len4;
+    int32_t len, staged;
 };
 
-__device__ __forceinline__ Span tile_span(const Desc &d, int64_t k)
+__device__ __forceinline__ Span tile_span(const Desc &d, int64_t k, int unit)
 {
     const int64_t b = k * kTile;
     int64_t len = (d.vec ? d.n - d.head : d.n) - b;
@@ -339,7 +347,7 @@ __device__ __forceinline__ Span tile_span(const Desc &d, int64_t k)
     Span sp;
     sp.base = d.vec ? d.head + b : b;
     sp.len = (int32_t)len;
-    sp.len4 = d.vec ? (int32_t)(len & ~(int64_t)3) : 0;
+    sp.staged = d.vec ? (int32_t)(len & ~(int64_t)(unit - 1)) : 0;
     return sp;
 }
 
@@ -370,12 +378,12 @@ struct TableCursor {
     }
 };
 
-template <int MODE, bool MULTI>
+template <int MODE, bool MULTI, typename GT>
 __device__ __forceinline__ void pipe_produce(unsigned char *smem, uint64_t *full, uint64_t *empty,
                                              const Desc *table, int32_t ntensors, int64_t total,
                                              const Desc &single)
 {
-    using L = PipeLayout<MODE>;
+    using L = PipeLayout<MODE, GT>;
     TableCursor<MULTI> cur(table, ntensors, total, single);
     int64_t k = 0;  // fills issued
     for (int64_t c = blockIdx.x; c < total; c += gridDim.x, ++k) {
@@ -386,18 +394,19 @@ __device__ __forceinline__ void pipe_produce(unsigned char *smem, uint64_t *full
             pipe_fault(kFaultEmptyWait);
             break;
         }
-        const Span sp = tile_span(cur.d, c - cur.d.chunk0);
-        const uint32_t bytes = (uint32_t)sp.len4 * 4u;
-        mbar_arrive_expect(&full[st], bytes * (uint32_t)L::kStreams);
-        if (bytes != 0) {
+        const Span sp = tile_span(cur.d, c - cur.d.chunk0, L::kUnit);
+        const uint32_t units = (uint32_t)sp.staged;
+        mbar_arrive_expect(&full[st], units * L::kBytesPerElem);
+        if (units != 0) {
             unsigned char *buf = smem + (size_t)st * L::kStageBytes;
-            bulk_load(buf, cur.d.p + sp.base, bytes, &full[st]);
-            bulk_load(buf + kTile * 4, cur.d.g + sp.base, bytes, &full[st]);
-            bulk_load(buf + 2 * kTile * 4, static_cast<const uint32_t *>(cur.d.s1) + sp.base, bytes,
+            bulk_load(buf, cur.d.p + sp.base, units * 4u, &full[st]);
+            bulk_load(buf + L::kG, reinterpret_cast<const GT *>(cur.d.g) + sp.base,
+                      units * (uint32_t)sizeof(GT), &full[st]);
+            bulk_load(buf + L::kS1, static_cast<const uint32_t *>(cur.d.s1) + sp.base, units * 4u,
                       &full[st]);
             if (MODE == kF32)
-                bulk_load(buf + 3 * kTile * 4, static_cast<const float *>(cur.d.s2) + sp.base,
-                          bytes, &full[st]);
+                bulk_load(buf + L::kS2, static_cast<const float *>(cur.d.s2) + sp.base, units * 4u,
+                          &full[st]);
         }
     }
     // The CTA's shared memory must outlive its copies: wait for the last fill
@@ -410,15 +419,16 @@ __device__ __forceinline__ void pipe_produce(unsigned char *smem, uint64_t *full
 // One staged 16-byte vector: elements e..e+3 of the stage buffer, which are
 // elements base+e.. of the tensor.  A warp with an exactly-zero gradient among
 // its lanes' elements takes the zero-safe arithmetic (same results).
-template <int MODE, bool U1, bool ZS>
+template <int MODE, bool U1, bool ZS, typename GT>
 __device__ __forceinline__ void pipe_vector_math(const unsigned char *buf, int e, const Desc &d,
                                                  int64_t base, float pp[4], const float gg[4],
                                                  const Scalars &s, const ZeroSafe &zs,
                                                  uint32_t &bad)
 {
+    using L = PipeLayout<MODE, GT>;
     if constexpr (MODE == kF32) {
-        const float4 mv = *reinterpret_cast<const float4 *>(buf + 2 * kTile * 4 + 4 * e);
-        const float4 vv = *reinterpret_cast<const float4 *>(buf + 3 * kTile * 4 + 4 * e);
+        const float4 mv = *reinterpret_cast<const float4 *>(buf + L::kS1 + 4 * e);
+        const float4 vv = *reinterpret_cast<const float4 *>(buf + L::kS2 + 4 * e);
         float mm[4] = {mv.x, mv.y, mv.z, mv.w};
         float vq[4] = {vv.x, vv.y, vv.z, vv.w};
 #pragma unroll
@@ -432,7 +442,7 @@ __device__ __forceinline__ void pipe_vector_math(const unsigned char *buf, int e
         store_stream(static_cast<float *>(d.s1) + base + e, make_float4(mm[0], mm[1], mm[2], mm[3]));
         store_stream(static_cast<float *>(d.s2) + base + e, make_float4(vq[0], vq[1], vq[2], vq[3]));
     } else {
-        const uint4 wv = *reinterpret_cast<const uint4 *>(buf + 2 * kTile * 4 + 4 * e);
+        const uint4 wv = *reinterpret_cast<const uint4 *>(buf + L::kS1 + 4 * e);
         uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j)
@@ -442,7 +452,7 @@ __device__ __forceinline__ void pipe_vector_math(const unsigned char *buf, int e
 }
 
 // One staged vector whose gradients gv are already loaded.
-template <int MODE, bool U1, bool ZS>
+template <int MODE, bool U1, bool ZS, typename GT>
 __device__ __forceinline__ void pipe_vector_g(const unsigned char *buf, int e, const Desc &d,
                                               int64_t base, const float4 gv, const Scalars &s,
                                               const ZeroSafe &zs, uint32_t &bad)
@@ -450,7 +460,7 @@ __device__ __forceinline__ void pipe_vector_g(const unsigned char *buf, int e, c
     const float4 pv = *reinterpret_cast<const float4 *>(buf + 4 * e);
     float pp[4] = {pv.x, pv.y, pv.z, pv.w};
     const float gg[4] = {gv.x, gv.y, gv.z, gv.w};
-    pipe_vector_math<MODE, U1, ZS>(buf, e, d, base, pp, gg, s, zs, bad);
+    pipe_vector_math<MODE, U1, ZS, GT>(buf, e, d, base, pp, gg, s, zs, bad);
     store_stream(d.p + base + e, make_float4(pp[0], pp[1], pp[2], pp[3]));
 }
 
@@ -459,31 +469,39 @@ __device__ __forceinline__ bool has_zero(const float4 g)
     return g.x == 0.0f || g.y == 0.0f || g.z == 0.0f || g.w == 0.0f;
 }
 
+// four staged gradients as binary32 (bfloat16 widened exactly)
+template <typename GT>
 __device__ __forceinline__ float4 staged_grad(const unsigned char *buf, int e)
 {
-    return *reinterpret_cast<const float4 *>(buf + kTile * 4 + 4 * e);
+    if constexpr (sizeof(GT) == 2) {
+        const uint2 r = *reinterpret_cast<const uint2 *>(buf + kTile * 4 + 2 * e);
+        return make_float4(__uint_as_float(r.x << 16), __uint_as_float(r.x & 0xFFFF0000u),
+                           __uint_as_float(r.y << 16), __uint_as_float(r.y & 0xFFFF0000u));
+    } else {
+        return *reinterpret_cast<const float4 *>(buf + kTile * 4 + 4 * e);
+    }
 }
 
 // Elements first, first+stride, ... below end, from global memory (head,
 // ragged tail, 4-byte-path tensors).  (Inlined: as an out-of-line call it
 // cost 2-9 % on GB300, the descriptor then living on the stack.)
-template <int MODE, bool U1>
+template <int MODE, bool U1, typename GT>
 __device__ __forceinline__ uint32_t pipe_scalar_run(const Desc &d, int64_t first, int64_t end,
                                                  int32_t stride, const Scalars &s)
 {
     uint32_t bad = 0;
     for (int64_t i = first; i < end; i += stride)
-        scalar_element<MODE, U1>(d, i, s, bad);
+        scalar_element<MODE, U1, GT>(d, i, s, bad);
     return bad;
 }
 
-template <int MODE, bool MULTI, bool U1>
+template <int MODE, bool MULTI, bool U1, typename GT>
 __device__ __forceinline__ void pipe_consume(const unsigned char *smem, uint64_t *full,
                                              uint64_t *empty, const Desc *table, int32_t ntensors,
                                              int64_t total, const Desc &single, const Scalars &s,
                                              uint32_t &bad)
 {
-    using L = PipeLayout<MODE>;
+    using L = PipeLayout<MODE, GT>;
     const int ct = threadIdx.x;  // consumer thread, 0 .. kConsumers-1
     const ZeroSafe zs = zero_safe_of(s);
     TableCursor<MULTI> cur(table, ntensors, total, single);
@@ -497,7 +515,7 @@ __device__ __forceinline__ void pipe_consume(const unsigned char *smem, uint64_t
         }
         const Desc &d = cur.d;
         const int64_t kt = c - d.chunk0;
-        const Span sp = tile_span(d, kt);
+        const Span sp = tile_span(d, kt, L::kUnit);
         if (d.vec) {
             const unsigned char *buf = smem + (size_t)st * L::kStageBytes;
             // Whole tile without a zero gradient in this warp: every vector
@@ -505,13 +523,13 @@ __device__ __forceinline__ void pipe_consume(const unsigned char *smem, uint64_t
             // each warp-vector choosing the plain or the zero-safe arithmetic
             // (one copy of each: the E4 element is large, and more inlined
             // copies missed in the instruction cache on GB300).
-            bool fast = sp.len4 == kTile;  // uniform over the CTA
+            bool fast = sp.staged == kTile;  // uniform over the CTA
             float4 gv[kTileVecs];
             if (fast) {
                 bool z = false;
 #pragma unroll
                 for (int v = 0; v < kTileVecs; ++v) {
-                    gv[v] = staged_grad(buf, 4 * (ct + v * kConsumers));
+                    gv[v] = staged_grad<GT>(buf, 4 * (ct + v * kConsumers));
                     z = z || has_zero(gv[v]);
                 }
                 fast = !__any_sync(0xFFFFFFFFu, z);
@@ -519,32 +537,33 @@ __device__ __forceinline__ void pipe_consume(const unsigned char *smem, uint64_t
             if (fast) {
 #pragma unroll
                 for (int v = 0; v < kTileVecs; ++v)
-                    pipe_vector_g<MODE, U1, false>(buf, 4 * (ct + v * kConsumers), d, sp.base, gv[v],
-                                                   s, zs, bad);
+                    pipe_vector_g<MODE, U1, false, GT>(buf, 4 * (ct + v * kConsumers), d, sp.base,
+                                                       gv[v], s, zs, bad);
             } else {
 #pragma unroll 1
                 for (int v = 0; v < kTileVecs; ++v) {
                     const int e = 4 * (ct + v * kConsumers);
-                    if (e < sp.len4) {
-                        const float4 g = staged_grad(buf, e);
+                    if (e < sp.staged) {
+                        const float4 g = staged_grad<GT>(buf, e);
                         if (__any_sync(__activemask(), has_zero(g)))
-                            pipe_vector_g<MODE, U1, true>(buf, e, d, sp.base, g, s, zs, bad);
+                            pipe_vector_g<MODE, U1, true, GT>(buf, e, d, sp.base, g, s, zs, bad);
                         else
-                            pipe_vector_g<MODE, U1, false>(buf, e, d, sp.base, g, s, zs, bad);
+                            pipe_vector_g<MODE, U1, false, GT>(buf, e, d, sp.base, g, s, zs, bad);
                     }
                 }
             }
             // the <= 3 elements before the 16-byte body (first tile) and the
-            // <= 3 after the staged part (last tile), one per thread
-            const bool head = kt == 0 && ct < d.head, tail = ct < sp.len - sp.len4;
+            // < unit after the staged part (last tile), one per thread
+            const bool head = kt == 0 && ct < d.head, tail = ct < sp.len - sp.staged;
             if (head || tail) {
 #pragma unroll 1
                 for (int r = head ? 0 : 1; r < (tail ? 2 : 1); ++r)
-                    bad += pipe_scalar_run<MODE, U1>(d, r == 0 ? ct : sp.base + sp.len4 + ct,
-                                                     (r == 0 ? ct : sp.base + sp.len4 + ct) + 1, 1, s);
+                    bad += pipe_scalar_run<MODE, U1, GT>(d, r == 0 ? ct : sp.base + sp.staged + ct,
+                                                         (r == 0 ? ct : sp.base + sp.staged + ct) + 1,
+                                                         1, s);
             }
         } else {
-            bad += pipe_scalar_run<MODE, U1>(d, sp.base + ct, sp.base + sp.len, kConsumers, s);
+            bad += pipe_scalar_run<MODE, U1, GT>(d, sp.base + ct, sp.base + sp.len, kConsumers, s);
         }
         __syncwarp();
         if ((ct & 31) == 0)
@@ -552,12 +571,12 @@ __device__ __forceinline__ void pipe_consume(const unsigned char *smem, uint64_t
     }
 }
 
-template <int MODE, bool MULTI, bool U1>
+template <int MODE, bool MULTI, bool U1, typename GT = float>
 __device__ __forceinline__ void pipe_body(const Desc *__restrict__ table, int32_t ntensors,
                                           int64_t total_tiles, const Desc &single,
                                           const Scalars &s, unsigned long long *nonfinite)
 {
-    using L = PipeLayout<MODE>;
+    using L = PipeLayout<MODE, GT>;
     extern __shared__ __align__(128) unsigned char pipe_smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(pipe_smem + kStages * L::kStageBytes);
     uint64_t *empty = full + kStages;
@@ -571,21 +590,22 @@ __device__ __forceinline__ void pipe_body(const Desc *__restrict__ table, int32_
     __syncthreads();
     if (threadIdx.x >= kConsumers) {
         if (threadIdx.x == kConsumers)
-            pipe_produce<MODE, MULTI>(pipe_smem, full, empty, table, ntensors, total_tiles, single);
+            pipe_produce<MODE, MULTI, GT>(pipe_smem, full, empty, table, ntensors, total_tiles,
+                                          single);
         return;
     }
     uint32_t bad = 0;
-    pipe_consume<MODE, MULTI, U1>(pipe_smem, full, empty, table, ntensors, total_tiles, single, s,
-                                  bad);
+    pipe_consume<MODE, MULTI, U1, GT>(pipe_smem, full, empty, table, ntensors, total_tiles, single,
+                                      s, bad);
     flush_nonfinite(bad, nonfinite);
 }
 
-template <int MODE, bool MULTI, bool U1>
+template <int MODE, bool MULTI, bool U1, typename GT = float>
 __global__ void __launch_bounds__(kPipeThreads, 1)
 adamw_step_pipe_kernel(const Desc *__restrict__ table, int32_t ntensors, int64_t total_tiles,
                        const Desc single, const Scalars s, unsigned long long *nonfinite)
 {
-    pipe_body<MODE, MULTI, U1>(table, ntensors, total_tiles, single, s, nonfinite);
+    pipe_body<MODE, MULTI, U1, GT>(table, ntensors, total_tiles, single, s, nonfinite);
 }
 
 // Graph-replayable variant: the scalars of the step are row *index of a
@@ -1157,9 +1177,8 @@ pa_status make_scalars(int64_t step, double lr, double beta1, double beta2, doub
 
 // ---- per-device launch geometry --------------------------------------------
 // Kernels launched with kThreads threads and no dynamic shared memory: the
-// register-staged step (bfloat16 gradients; FP32 gradients in host memory)
-// and the codecs.
-enum KernelSlot { kSlotBf16, kSlotBf16Multi, kSlotHostE4, kSlotCodec, kNumSlots };
+// register-staged step (on host memory) and the codecs.
+enum KernelSlot { kSlotHostE4, kSlotCodec, kNumSlots };
 
 struct DeviceInfo {
     bool ready = false;
@@ -1173,8 +1192,6 @@ DeviceInfo g_dev[64];
 const void *kernel_of(int slot)
 {
     switch (slot) {
-    case kSlotBf16: return (const void *)pa::adamw_step_kernel<pa::kE4, false, false, __nv_bfloat16>;
-    case kSlotBf16Multi: return (const void *)pa::adamw_step_kernel<pa::kE4, true, false, __nv_bfloat16>;
     case kSlotHostE4: return (const void *)pa::adamw_step_kernel<pa::kE4, false, false, float>;
     default: return (const void *)pa::encode_state_kernel<pa::kE4>;
     }
@@ -1295,8 +1312,13 @@ int64_t describe(const pa_tensor &t, int mode, int64_t chunk, Desc *d, int grad_
                 (reinterpret_cast<uintptr_t>(t.state) & 15u) == 4 * ph;
     if (mode == pa::kF32)
         same = same && (reinterpret_cast<uintptr_t>(t.state2) & 15u) == 4 * ph;
-    d->vec = same ? 1 : 0;
     int64_t head = same ? (int64_t)((4u - ph) & 3u) : 0;
+    // the staged body starts 16-byte aligned in every stream (a bfloat16
+    // gradient can share p's element phase and still be 8 bytes off)
+    same = same && ((reinterpret_cast<uintptr_t>(t.g) + (uintptr_t)grad_bytes * (uintptr_t)head) & 15u) == 0;
+    if (!same)
+        head = 0;
+    d->vec = same ? 1 : 0;
     if (head > t.n)
         head = t.n;
     d->head = (int32_t)head;
@@ -1343,38 +1365,21 @@ pa_status step_single(const pa_tensor &t, int64_t step, double lr, double beta1,
     if (t.n == 0)
         return ok();
     Desc d;
-    if constexpr (std::is_same<GT, float>::value) {
-        const int64_t tiles = describe(t, MODE, pa::kTile, &d);
-        d.chunk0 = 0;
-        const size_t smem = pa::PipeLayout<MODE>::kBytes;
-        const void *kern = s.bc2 == 1.0f ? (const void *)pa::adamw_step_pipe_kernel<MODE, false, true>
-                                         : (const void *)pa::adamw_step_pipe_kernel<MODE, false, false>;
-        int grid = 0;
-        if ((st = pipe_grid(kern, smem, tiles, &grid)) != PA_OK)
-            return st;
-        if (s.bc2 == 1.0f)
-            pa::adamw_step_pipe_kernel<MODE, false, true><<<grid, pa::kPipeThreads, smem, (cudaStream_t)stream>>>(
-                nullptr, 1, tiles, d, s, nonfinite);
-        else
-            pa::adamw_step_pipe_kernel<MODE, false, false><<<grid, pa::kPipeThreads, smem, (cudaStream_t)stream>>>(
-                nullptr, 1, tiles, d, s, nonfinite);
-        return check_launch("adamw_step_pipe_kernel launch");
-    }
-    int64_t chunk = 0;
-    if ((st = chunk_size(kSlotBf16, t.n, &chunk)) != PA_OK)
-        return st;
-    const int64_t chunks = describe(t, MODE, chunk, &d, (int)sizeof(GT));
+    const int64_t tiles = describe(t, MODE, pa::kTile, &d, (int)sizeof(GT));
     d.chunk0 = 0;
+    const size_t smem = pa::PipeLayout<MODE, GT>::kBytes;
+    const void *kern = s.bc2 == 1.0f ? (const void *)pa::adamw_step_pipe_kernel<MODE, false, true, GT>
+                                     : (const void *)pa::adamw_step_pipe_kernel<MODE, false, false, GT>;
     int grid = 0;
-    if ((st = grid_for(kSlotBf16, chunks, &grid)) != PA_OK)
+    if ((st = pipe_grid(kern, smem, tiles, &grid)) != PA_OK)
         return st;
     if (s.bc2 == 1.0f)
-        pa::adamw_step_kernel<MODE, false, true, GT><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
-            nullptr, 1, chunks, chunk, d, s, nonfinite);
+        pa::adamw_step_pipe_kernel<MODE, false, true, GT><<<grid, pa::kPipeThreads, smem, (cudaStream_t)stream>>>(
+            nullptr, 1, tiles, d, s, nonfinite);
     else
-        pa::adamw_step_kernel<MODE, false, false, GT><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
-            nullptr, 1, chunks, chunk, d, s, nonfinite);
-    return check_launch("adamw_step_kernel launch");
+        pa::adamw_step_pipe_kernel<MODE, false, false, GT><<<grid, pa::kPipeThreads, smem, (cudaStream_t)stream>>>(
+            nullptr, 1, tiles, d, s, nonfinite);
+    return check_launch("adamw_step_pipe_kernel launch");
 }
 
 // ---- cached device descriptor tables (multi-tensor calls) -----------------------
@@ -1491,39 +1496,22 @@ pa_status step_multi(const pa_tensor *list, int32_t ntensors, int64_t step, doub
     const Desc *table = nullptr;
     Desc none;
     std::memset(&none, 0, sizeof none);
-    if constexpr (std::is_same<GT, float>::value) {
-        int64_t tiles = 0;
-        if ((st = table_for(list, ntensors, MODE, pa::kTile, &table, &tiles)) != PA_OK)
-            return st;
-        const size_t smem = pa::PipeLayout<MODE>::kBytes;
-        const void *kern = s.bc2 == 1.0f ? (const void *)pa::adamw_step_pipe_kernel<MODE, true, true>
-                                         : (const void *)pa::adamw_step_pipe_kernel<MODE, true, false>;
-        int grid = 0;
-        if ((st = pipe_grid(kern, smem, tiles, &grid)) != PA_OK)
-            return st;
-        if (s.bc2 == 1.0f)
-            pa::adamw_step_pipe_kernel<MODE, true, true><<<grid, pa::kPipeThreads, smem, (cudaStream_t)stream>>>(
-                table, ntensors, tiles, none, s, nonfinite);
-        else
-            pa::adamw_step_pipe_kernel<MODE, true, false><<<grid, pa::kPipeThreads, smem, (cudaStream_t)stream>>>(
-                table, ntensors, tiles, none, s, nonfinite);
-        return check_launch("adamw_step_pipe_kernel (multi) launch");
-    }
-    int64_t chunks = 0, chunk = 0;
-    if ((st = chunk_size(kSlotBf16Multi, total, &chunk)) != PA_OK)
+    int64_t tiles = 0;
+    if ((st = table_for(list, ntensors, MODE, pa::kTile, &table, &tiles, (int)sizeof(GT))) != PA_OK)
         return st;
-    if ((st = table_for(list, ntensors, MODE, chunk, &table, &chunks, (int)sizeof(GT))) != PA_OK)
-        return st;
+    const size_t smem = pa::PipeLayout<MODE, GT>::kBytes;
+    const void *kern = s.bc2 == 1.0f ? (const void *)pa::adamw_step_pipe_kernel<MODE, true, true, GT>
+                                     : (const void *)pa::adamw_step_pipe_kernel<MODE, true, false, GT>;
     int grid = 0;
-    if ((st = grid_for(kSlotBf16Multi, chunks, &grid)) != PA_OK)
+    if ((st = pipe_grid(kern, smem, tiles, &grid)) != PA_OK)
         return st;
     if (s.bc2 == 1.0f)
-        pa::adamw_step_kernel<MODE, true, true, GT><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
-            table, ntensors, chunks, chunk, none, s, nonfinite);
+        pa::adamw_step_pipe_kernel<MODE, true, true, GT><<<grid, pa::kPipeThreads, smem, (cudaStream_t)stream>>>(
+            table, ntensors, tiles, none, s, nonfinite);
     else
-        pa::adamw_step_kernel<MODE, true, false, GT><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
-            table, ntensors, chunks, chunk, none, s, nonfinite);
-    return check_launch("adamw_step_kernel (multi) launch");
+        pa::adamw_step_pipe_kernel<MODE, true, false, GT><<<grid, pa::kPipeThreads, smem, (cudaStream_t)stream>>>(
+            table, ntensors, tiles, none, s, nonfinite);
+    return check_launch("adamw_step_pipe_kernel (multi) launch");
 }
 
 template <int MODE>

@@ -538,7 +538,7 @@ def run_ours(args):
                 "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_source": peak_kind,
                 "traffic": None if traffic is None else traffic * w.n,
-                "kernel": ("adamw_step_kernel<0,true,bfloat16>" if args.grad == "bf16"
+                "kernel": ("adamw_step_pipe_kernel<0,true,bfloat16>" if args.grad == "bf16"
                            else "adamw_step_table_kernel<0>" if args.graph
                            else KERNEL_NAME[w.mode]),
                 "kernel_ms": kernel_ms,
