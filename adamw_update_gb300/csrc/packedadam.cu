@@ -19,6 +19,7 @@
 #include <cuda_runtime.h>
 
 #include <climits>
+#include <cstddef>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -302,16 +303,46 @@ constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kPipeThreads = kConsumers + 32;  // + the producer warp
 constexpr int kTileVecs = kTile / (4 * kConsumers);
 static_assert(kTile % (4 * kConsumers) == 0, "a tile is whole 16-byte vectors per consumer");
+static_assert(sizeof(Desc) % sizeof(uint64_t) == 0, "descriptors copy as 8-byte words");
+
+// Lists of up to kSmemDescs tensors have their descriptor table copied into
+// shared memory at kernel start, so the producer's walk from tensor to tensor
+// costs no dependent global loads (with tens of tensors and few tiles each,
+// those loads outlasted a tile's computation).
+constexpr int kSmemDescs = 512;
+
+// What the consumers need to know about a staged tile, written by the
+// producer into the stage's slot before it signals the stage, so that only
+// the producer walks the descriptor table.
+struct TileInfo {
+    float *p;
+    const void *g;
+    void *s1, *s2;
+    int64_t base;     // first element of the tile in its tensor
+    int32_t len;      // elements in the tile
+    int32_t staged;   // of them, staged by the bulk copies
+    int32_t head;     // elements before the 16-byte body, updated with this tile
+    int32_t vec;      // the tensor's body is staged (else 4-byte accesses)
+};
 
 // A stage holds one tile of each stream: p, g (GT: float or bfloat16), the
-// state word or m, and v in the FP32 mode.
+// state word or m, and v in the FP32 mode; after the stages come the
+// barriers and the shared copy of the descriptor table.
 template <int MODE, typename GT = float>
 struct PipeLayout {
     static constexpr size_t kG = (size_t)kTile * 4;                 // gradients
     static constexpr size_t kS1 = kG + (size_t)kTile * sizeof(GT);  // state word | m
     static constexpr size_t kS2 = kS1 + (size_t)kTile * 4;          // v (FP32 mode)
     static constexpr size_t kStageBytes = MODE == kF32 ? kS2 + (size_t)kTile * 4 : kS2;
-    static constexpr size_t kBytes = kStages * kStageBytes + 2 * kStages * sizeof(uint64_t);
+    static constexpr size_t kBarriers = kStages * kStageBytes;
+    static constexpr size_t kInfo = kBarriers + 2 * kStages * sizeof(uint64_t);
+    static constexpr size_t kDescs = kInfo + kStages * sizeof(TileInfo);
+    static constexpr size_t kBytes = kDescs + (size_t)kSmemDescs * sizeof(Desc);  // the most
+    // dynamic shared memory of a launch over `ntensors` tensors (MULTI)
+    static size_t bytes_for(int32_t ntensors)
+    {
+        return kDescs + (ntensors <= kSmemDescs ? (size_t)ntensors * sizeof(Desc) : 0);
+    }
     static constexpr uint32_t kBytesPerElem = (uint32_t)(kStageBytes / kTile);
     // a staged run is whole 16-byte units of every stream: 4 elements, 8 for bfloat16
     static constexpr int kUnit = sizeof(GT) == 2 ? 8 : 4;
@@ -384,6 +415,7 @@ __device__ __forceinline__ void pipe_produce(unsigned char *smem, uint64_t *full
                                              const Desc &single)
 {
     using L = PipeLayout<MODE, GT>;
+    TileInfo *info = reinterpret_cast<TileInfo *>(smem + L::kInfo);
     TableCursor<MULTI> cur(table, ntensors, total, single);
     int64_t k = 0;  // fills issued
     for (int64_t c = blockIdx.x; c < total; c += gridDim.x, ++k) {
@@ -394,9 +426,20 @@ __device__ __forceinline__ void pipe_produce(unsigned char *smem, uint64_t *full
             pipe_fault(kFaultEmptyWait);
             break;
         }
-        const Span sp = tile_span(cur.d, c - cur.d.chunk0, L::kUnit);
+        const int64_t kt = c - cur.d.chunk0;
+        const Span sp = tile_span(cur.d, kt, L::kUnit);
+        TileInfo &ti = info[st];
+        ti.p = cur.d.p;
+        ti.g = cur.d.g;
+        ti.s1 = cur.d.s1;
+        ti.s2 = cur.d.s2;
+        ti.base = sp.base;
+        ti.len = sp.len;
+        ti.staged = sp.staged;
+        ti.head = (cur.d.vec && kt == 0) ? cur.d.head : 0;
+        ti.vec = cur.d.vec;
         const uint32_t units = (uint32_t)sp.staged;
-        mbar_arrive_expect(&full[st], units * L::kBytesPerElem);
+        mbar_arrive_expect(&full[st], units * L::kBytesPerElem);  // releases the slot too
         if (units != 0) {
             unsigned char *buf = smem + (size_t)st * L::kStageBytes;
             bulk_load(buf, cur.d.p + sp.base, units * 4u, &full[st]);
@@ -495,27 +538,33 @@ __device__ __forceinline__ uint32_t pipe_scalar_run(const Desc &d, int64_t first
     return bad;
 }
 
-template <int MODE, bool MULTI, bool U1, typename GT>
+template <int MODE, bool U1, typename GT>
 __device__ __forceinline__ void pipe_consume(const unsigned char *smem, uint64_t *full,
-                                             uint64_t *empty, const Desc *table, int32_t ntensors,
-                                             int64_t total, const Desc &single, const Scalars &s,
+                                             uint64_t *empty, int64_t total, const Scalars &s,
                                              uint32_t &bad)
 {
     using L = PipeLayout<MODE, GT>;
     const int ct = threadIdx.x;  // consumer thread, 0 .. kConsumers-1
     const ZeroSafe zs = zero_safe_of(s);
-    TableCursor<MULTI> cur(table, ntensors, total, single);
+    const TileInfo *info = reinterpret_cast<const TileInfo *>(smem + L::kInfo);
     int64_t k = 0;
     for (int64_t c = blockIdx.x; c < total; c += gridDim.x, ++k) {
-        cur.seek(c, total);
         const int st = (int)(k % kStages);
         if (!mbar_wait(&full[st], (uint32_t)((k / kStages) & 1))) {
             pipe_fault(kFaultFullWait);
             break;
         }
-        const Desc &d = cur.d;
-        const int64_t kt = c - d.chunk0;
-        const Span sp = tile_span(d, kt, L::kUnit);
+        const TileInfo ti = info[st];
+        Desc d;
+        d.p = ti.p;
+        d.g = static_cast<const float *>(ti.g);
+        d.s1 = ti.s1;
+        d.s2 = ti.s2;
+        d.vec = ti.vec;
+        Span sp;
+        sp.base = ti.base;
+        sp.len = ti.len;
+        sp.staged = ti.staged;
         if (d.vec) {
             const unsigned char *buf = smem + (size_t)st * L::kStageBytes;
             // Whole tile without a zero gradient in this warp: every vector
@@ -554,7 +603,7 @@ __device__ __forceinline__ void pipe_consume(const unsigned char *smem, uint64_t
             }
             // the <= 3 elements before the 16-byte body (first tile) and the
             // < unit after the staged part (last tile), one per thread
-            const bool head = kt == 0 && ct < d.head, tail = ct < sp.len - sp.staged;
+            const bool head = ct < ti.head, tail = ct < sp.len - sp.staged;
             if (head || tail) {
 #pragma unroll 1
                 for (int r = head ? 0 : 1; r < (tail ? 2 : 1); ++r)
@@ -578,7 +627,7 @@ __device__ __forceinline__ void pipe_body(const Desc *__restrict__ table, int32_
 {
     using L = PipeLayout<MODE, GT>;
     extern __shared__ __align__(128) unsigned char pipe_smem[];
-    uint64_t *full = reinterpret_cast<uint64_t *>(pipe_smem + kStages * L::kStageBytes);
+    uint64_t *full = reinterpret_cast<uint64_t *>(pipe_smem + L::kBarriers);
     uint64_t *empty = full + kStages;
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -588,15 +637,23 @@ __device__ __forceinline__ void pipe_body(const Desc *__restrict__ table, int32_
         mbar_init_fence();
     }
     __syncthreads();
-    if (threadIdx.x >= kConsumers) {
+    if (threadIdx.x >= kConsumers) {  // the producer warp
+        if (MULTI && ntensors <= kSmemDescs) {  // its copy of the table, in 8-byte words
+            const uint64_t *src = reinterpret_cast<const uint64_t *>(table);
+            uint64_t *dst = reinterpret_cast<uint64_t *>(pipe_smem + L::kDescs);
+            constexpr int kWords = sizeof(Desc) / sizeof(uint64_t);
+            for (int i = threadIdx.x - kConsumers; i < ntensors * kWords; i += 32)
+                dst[i] = __ldg(src + i);
+            __syncwarp();
+            table = reinterpret_cast<const Desc *>(pipe_smem + L::kDescs);
+        }
         if (threadIdx.x == kConsumers)
             pipe_produce<MODE, MULTI, GT>(pipe_smem, full, empty, table, ntensors, total_tiles,
                                           single);
         return;
     }
     uint32_t bad = 0;
-    pipe_consume<MODE, MULTI, U1, GT>(pipe_smem, full, empty, table, ntensors, total_tiles, single,
-                                      s, bad);
+    pipe_consume<MODE, U1, GT>(pipe_smem, full, empty, total_tiles, s, bad);
     flush_nonfinite(bad, nonfinite);
 }
 
@@ -1245,7 +1302,8 @@ pa_status chunk_size(int slot, int64_t elements, int64_t *chunk)
 
 // Grid of a staged kernel: one CTA per SM (its shared-memory ring takes most
 // of the SM), capped by the tiles.  The first launch of each kernel on a device
-// raises its dynamic shared-memory limit.
+// raises its dynamic shared-memory limit to `smem`, the most any launch of it
+// uses (a launch passes what it needs: the descriptor copy depends on the list).
 pa_status pipe_grid(const void *kernel, size_t smem, int64_t tiles, int *grid)
 {
     int dev = 0;
@@ -1367,17 +1425,18 @@ pa_status step_single(const pa_tensor &t, int64_t step, double lr, double beta1,
     Desc d;
     const int64_t tiles = describe(t, MODE, pa::kTile, &d, (int)sizeof(GT));
     d.chunk0 = 0;
-    const size_t smem = pa::PipeLayout<MODE, GT>::kBytes;
+    const size_t smem = pa::PipeLayout<MODE, GT>::kBytes;  // the kernel's limit
+    const size_t used = pa::PipeLayout<MODE, GT>::kDescs;  // no table: one tensor
     const void *kern = s.bc2 == 1.0f ? (const void *)pa::adamw_step_pipe_kernel<MODE, false, true, GT>
                                      : (const void *)pa::adamw_step_pipe_kernel<MODE, false, false, GT>;
     int grid = 0;
     if ((st = pipe_grid(kern, smem, tiles, &grid)) != PA_OK)
         return st;
     if (s.bc2 == 1.0f)
-        pa::adamw_step_pipe_kernel<MODE, false, true, GT><<<grid, pa::kPipeThreads, smem, (cudaStream_t)stream>>>(
+        pa::adamw_step_pipe_kernel<MODE, false, true, GT><<<grid, pa::kPipeThreads, used, (cudaStream_t)stream>>>(
             nullptr, 1, tiles, d, s, nonfinite);
     else
-        pa::adamw_step_pipe_kernel<MODE, false, false, GT><<<grid, pa::kPipeThreads, smem, (cudaStream_t)stream>>>(
+        pa::adamw_step_pipe_kernel<MODE, false, false, GT><<<grid, pa::kPipeThreads, used, (cudaStream_t)stream>>>(
             nullptr, 1, tiles, d, s, nonfinite);
     return check_launch("adamw_step_pipe_kernel launch");
 }
@@ -1499,17 +1558,18 @@ pa_status step_multi(const pa_tensor *list, int32_t ntensors, int64_t step, doub
     int64_t tiles = 0;
     if ((st = table_for(list, ntensors, MODE, pa::kTile, &table, &tiles, (int)sizeof(GT))) != PA_OK)
         return st;
-    const size_t smem = pa::PipeLayout<MODE, GT>::kBytes;
+    const size_t smem = pa::PipeLayout<MODE, GT>::kBytes;  // the kernel's limit
+    const size_t used = pa::PipeLayout<MODE, GT>::bytes_for(ntensors);
     const void *kern = s.bc2 == 1.0f ? (const void *)pa::adamw_step_pipe_kernel<MODE, true, true, GT>
                                      : (const void *)pa::adamw_step_pipe_kernel<MODE, true, false, GT>;
     int grid = 0;
     if ((st = pipe_grid(kern, smem, tiles, &grid)) != PA_OK)
         return st;
     if (s.bc2 == 1.0f)
-        pa::adamw_step_pipe_kernel<MODE, true, true, GT><<<grid, pa::kPipeThreads, smem, (cudaStream_t)stream>>>(
+        pa::adamw_step_pipe_kernel<MODE, true, true, GT><<<grid, pa::kPipeThreads, used, (cudaStream_t)stream>>>(
             table, ntensors, tiles, none, s, nonfinite);
     else
-        pa::adamw_step_pipe_kernel<MODE, true, false, GT><<<grid, pa::kPipeThreads, smem, (cudaStream_t)stream>>>(
+        pa::adamw_step_pipe_kernel<MODE, true, false, GT><<<grid, pa::kPipeThreads, used, (cudaStream_t)stream>>>(
             table, ntensors, tiles, none, s, nonfinite);
     return check_launch("adamw_step_pipe_kernel (multi) launch");
 }
@@ -1824,7 +1884,8 @@ extern "C" pa_status pa_adamw_step_packed_e4_multi_noalloc(
                                     cudaMemcpyHostToDevice, (cudaStream_t)stream);
     if (e != cudaSuccess)
         return cuda_fail(e, "descriptor upload to the fixed device array");
-    const size_t smem = pa::PipeLayout<pa::kE4>::kBytes;
+    const size_t smem = pa::PipeLayout<pa::kE4>::kBytes;  // the kernel's limit
+    const size_t used = pa::PipeLayout<pa::kE4>::bytes_for(ntensors);
     const void *kern = s.bc2 == 1.0f ? (const void *)pa::adamw_step_pipe_kernel<pa::kE4, true, true>
                                      : (const void *)pa::adamw_step_pipe_kernel<pa::kE4, true, false>;
     int grid = 0;
@@ -1833,10 +1894,10 @@ extern "C" pa_status pa_adamw_step_packed_e4_multi_noalloc(
     pa::Desc none;
     std::memset(&none, 0, sizeof none);
     if (s.bc2 == 1.0f)
-        pa::adamw_step_pipe_kernel<pa::kE4, true, true><<<grid, pa::kPipeThreads, smem, (cudaStream_t)stream>>>(
+        pa::adamw_step_pipe_kernel<pa::kE4, true, true><<<grid, pa::kPipeThreads, used, (cudaStream_t)stream>>>(
             table, ntensors, tiles, none, s, nonfinite);
     else
-        pa::adamw_step_pipe_kernel<pa::kE4, true, false><<<grid, pa::kPipeThreads, smem, (cudaStream_t)stream>>>(
+        pa::adamw_step_pipe_kernel<pa::kE4, true, false><<<grid, pa::kPipeThreads, used, (cudaStream_t)stream>>>(
             table, ntensors, tiles, none, s, nonfinite);
     return check_launch("adamw_step_pipe_kernel (no-alloc multi) launch");
 }
@@ -2096,12 +2157,13 @@ extern "C" pa_status pa_adamw_step_packed_e4_multi_graph(const pa_tensor *list, 
         int64_t tiles = 0;
         if ((st = table_for(list, ntensors, pa::kE4, pa::kTile, &table, &tiles)) != PA_OK)
             return st;
-        const size_t smem = pa::PipeLayout<pa::kE4>::kBytes;
+        const size_t smem = pa::PipeLayout<pa::kE4>::kBytes;  // the kernel's limit
+        const size_t used = pa::PipeLayout<pa::kE4>::bytes_for(ntensors);
         int grid = 0;
         if ((st = pipe_grid((const void *)pa::adamw_step_table_kernel<pa::kE4>, smem, tiles, &grid)) !=
             PA_OK)
             return st;
-        pa::adamw_step_table_kernel<pa::kE4><<<grid, pa::kPipeThreads, smem, cs>>>(
+        pa::adamw_step_table_kernel<pa::kE4><<<grid, pa::kPipeThreads, used, cs>>>(
             table, ntensors, tiles, reinterpret_cast<const Scalars *>(rows), nrows, index, status,
             nonfinite);
         if ((st = check_launch("adamw_step_table_kernel launch")) != PA_OK)
