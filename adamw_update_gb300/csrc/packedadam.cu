@@ -790,8 +790,21 @@ struct BlockwiseShared {
     uint32_t warp_max[kBwGroups][2][2][8];  // [group][block parity][m, v][warp of the group]
     uint32_t red[2][32];
 };
+// What the consumers need to know about a work item, written by the producer
+// into slot k % kBwSlots (k: the CTA's item count) before it signals the
+// item's stage.  The consumers hand a stage back before they compute, so a
+// slot must outlive its stage: the producer rewrites slot k % kBwSlots for
+// item k + kBwSlots only after every consumer warp has handed back item
+// k + kBwStages, which each does after finishing item k.
+constexpr int kBwSlots = 2 * kBwStages;
+struct BwItemInfo {
+    BlockwiseArgs a;
+    int64_t b0;    // first block of the item (a tile), or the short last block
+    int32_t nblk;  // whole blocks in the tile; 0: the short last block
+    int32_t codes; // the code arrays were staged
+};
 constexpr size_t kBwSmemBytes = kBwStages * kBwStageBytes + sizeof(BlockwiseShared) +
-                                2 * kBwStages * sizeof(uint64_t);
+                                2 * kBwStages * sizeof(uint64_t) + kBwSlots * sizeof(BwItemInfo);
 
 // Redo, with the IEEE divide, the codes of the values that need it.
 __device__ __noinline__ uint2 requantise_fixup(float x0, float x1, float x2, float x3, float x4,
@@ -1021,8 +1034,8 @@ __device__ __forceinline__ bool codes_staged(const BlockwiseArgs &a)
 
 template <bool MULTI>
 __device__ __forceinline__ void bw_produce(unsigned char *smem, uint64_t *full, uint64_t *empty,
-                                           const BwDesc *table, int32_t ntensors, int64_t total,
-                                           const BwDesc &single)
+                                           BwItemInfo *info, const BwDesc *table, int32_t ntensors,
+                                           int64_t total, const BwDesc &single)
 {
     BwCursor<MULTI> cur(table, ntensors, total, single);
     int64_t k = 0;
@@ -1037,13 +1050,18 @@ __device__ __forceinline__ void bw_produce(unsigned char *smem, uint64_t *full, 
         const BlockwiseArgs &a = cur.d.a;
         const int64_t kt = c - cur.d.item0;
         const int64_t nf = a.n / kBlock;
+        BwItemInfo &it = info[k % kBwSlots];
+        it.a = a;
         if (kt < bw_full_tiles(a.n)) {
             const int64_t b0 = kt * kBwGroups;
             const int64_t nb = nf - b0 < kBwGroups ? nf - b0 : kBwGroups;
             const uint32_t elems = (uint32_t)(nb * kBlock);
             const int64_t e0 = b0 * kBlock;
             const bool codes = codes_staged(a);
-            mbar_arrive_expect(&full[st], elems * (codes ? 10u : 8u));
+            it.b0 = b0;
+            it.nblk = (int32_t)nb;
+            it.codes = codes ? 1 : 0;
+            mbar_arrive_expect(&full[st], elems * (codes ? 10u : 8u));  // releases the slot too
             unsigned char *buf = smem + (size_t)st * kBwStageBytes;
             bulk_load(buf, a.p + e0, elems * 4u, &full[st]);
             bulk_load(buf + kBwTile * 4, a.g + e0, elems * 4u, &full[st]);
@@ -1051,8 +1069,11 @@ __device__ __forceinline__ void bw_produce(unsigned char *smem, uint64_t *full, 
                 bulk_load(buf + kBwTile * 8, a.m_code + e0, elems, &full[st]);
                 bulk_load(buf + kBwTile * 9, a.v_code + e0, elems, &full[st]);
             }
-        } else {
-            mbar_arrive_expect(&full[st], 0u);  // the short last block: read from global memory
+        } else {  // the short last block: read from global memory
+            it.b0 = nf;
+            it.nblk = 0;
+            it.codes = 0;
+            mbar_arrive_expect(&full[st], 0u);
         }
     }
     for (int64_t j = k > kBwStages ? k - kBwStages : 0; j < k; ++j)
@@ -1060,37 +1081,33 @@ __device__ __forceinline__ void bw_produce(unsigned char *smem, uint64_t *full, 
             pipe_fault(kFaultCopyWait);
 }
 
-template <bool MULTI>
 __device__ __forceinline__ void bw_consume(const unsigned char *smem, uint64_t *full, uint64_t *empty,
-                                           BlockwiseShared &sh, const BwDesc *table,
-                                           int32_t ntensors, int64_t total, const BwDesc &single,
-                                           const Scalars &s, int k1, int k2, uint32_t &bad)
+                                           BlockwiseShared &sh, const BwItemInfo *info,
+                                           int64_t total, const Scalars &s, int k1, int k2,
+                                           uint32_t &bad)
 {
     const int group = threadIdx.x >> 8, gt = threadIdx.x & 255;
     const int kmax = k1 > k2 ? k1 : k2;
     uint32_t gpar = 0;
-    BwCursor<MULTI> cur(table, ntensors, total, single);
     int64_t k = 0;
     for (int64_t c = blockIdx.x; c < total; c += gridDim.x, ++k) {
-        cur.seek(c, total);
         const int st = (int)(k % kBwStages);
         if (!mbar_wait(&full[st], (uint32_t)((k / kBwStages) & 1))) {
             pipe_fault(kFaultFullWait);
             break;
         }
-        const BlockwiseArgs &a = cur.d.a;
-        const int64_t kt = c - cur.d.item0;
-        const int64_t nf = a.n / kBlock;
-        const bool tile = kt < bw_full_tiles(a.n);
-        const int64_t b = tile ? kt * kBwGroups + group : nf;
-        const bool mine = tile ? b < nf : group == 0;
+        const BwItemInfo &it = info[k % kBwSlots];
+        const BlockwiseArgs &a = it.a;  // read from the slot where used
+        const bool tile = it.nblk > 0;
+        const int64_t b = tile ? it.b0 + group : it.b0;
+        const bool mine = tile ? group < it.nblk : group == 0;
         // this thread's elements and codes, into registers
         float pv[8], gv[8];
         uint32_t mc[2] = {0u, 0u}, vc[2] = {0u, 0u};
         if (tile && mine) {
             const unsigned char *buf = smem + (size_t)st * kBwStageBytes;
             const int o = group * kBlock + 4 * gt;
-            const bool codes = codes_staged(a);
+            const bool codes = it.codes != 0;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const float4 x = *reinterpret_cast<const float4 *>(buf + 4 * (o + 1024 * h));
@@ -1151,6 +1168,7 @@ blockwise8_pipe_kernel(const BwDesc *__restrict__ table, int32_t ntensors, int64
     BlockwiseShared &sh = *reinterpret_cast<BlockwiseShared *>(bw_smem + kBwStages * kBwStageBytes);
     uint64_t *full = reinterpret_cast<uint64_t *>(bw_smem + kBwStages * kBwStageBytes + sizeof(BlockwiseShared));
     uint64_t *empty = full + kBwStages;
+    BwItemInfo *info = reinterpret_cast<BwItemInfo *>(empty + kBwStages);
     int k1, k2;
     if (threadIdx.x == 0) {
         for (int i = 0; i < kBwStages; ++i) {
@@ -1162,11 +1180,11 @@ blockwise8_pipe_kernel(const BwDesc *__restrict__ table, int32_t ntensors, int64
     blockwise_setup(sh, qmap1, qmap2, k1, k2);  // ends with __syncthreads
     if (threadIdx.x >= kConsumers) {
         if (threadIdx.x == kConsumers)
-            bw_produce<MULTI>(bw_smem, full, empty, table, ntensors, total_items, single);
+            bw_produce<MULTI>(bw_smem, full, empty, info, table, ntensors, total_items, single);
         return;
     }
     uint32_t bad = 0;
-    bw_consume<MULTI>(bw_smem, full, empty, sh, table, ntensors, total_items, single, s, k1, k2, bad);
+    bw_consume(bw_smem, full, empty, sh, info, total_items, s, k1, k2, bad);
     flush_nonfinite(bad, nonfinite);
 }
 
