@@ -507,6 +507,60 @@ __device__ __forceinline__ void pipe_vector_g(const unsigned char *buf, int e, c
     store_stream(d.p + base + e, make_float4(pp[0], pp[1], pp[2], pp[3]));
 }
 
+// One staged vector held in registers (the whole-tile path copies all of a
+// thread's vectors out of the stage, hands the stage back, then computes).
+template <int MODE>
+struct RegVec {
+    float4 p, g;
+    uint4 w;      // packed modes
+    float4 m, v;  // FP32 mode
+};
+
+template <int MODE, typename GT>
+__device__ __forceinline__ RegVec<MODE> load_vec(const unsigned char *buf, int e, float4 g)
+{
+    using L = PipeLayout<MODE, GT>;
+    RegVec<MODE> r;
+    r.p = *reinterpret_cast<const float4 *>(buf + 4 * e);
+    r.g = g;
+    if constexpr (MODE == kF32) {
+        r.m = *reinterpret_cast<const float4 *>(buf + L::kS1 + 4 * e);
+        r.v = *reinterpret_cast<const float4 *>(buf + L::kS2 + 4 * e);
+    } else {
+        r.w = *reinterpret_cast<const uint4 *>(buf + L::kS1 + 4 * e);
+    }
+    return r;
+}
+
+template <int MODE, bool U1>
+__device__ __forceinline__ void compute_vec(const RegVec<MODE> &r, int e, const Desc &d,
+                                            int64_t base, const Scalars &s, uint32_t &bad)
+{
+    float pp[4] = {r.p.x, r.p.y, r.p.z, r.p.w};
+    const float gg[4] = {r.g.x, r.g.y, r.g.z, r.g.w};
+    if constexpr (MODE == kF32) {
+        float mm[4] = {r.m.x, r.m.y, r.m.z, r.m.w};
+        float vq[4] = {r.v.x, r.v.y, r.v.z, r.v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const Moments o = adamw_element<U1>(pp[j], gg[j], mm[j], vq[j], s);
+            bad += any_nonfinite(o);
+            pp[j] = o.p;
+            mm[j] = o.m;
+            vq[j] = o.v;
+        }
+        store_stream(static_cast<float *>(d.s1) + base + e, make_float4(mm[0], mm[1], mm[2], mm[3]));
+        store_stream(static_cast<float *>(d.s2) + base + e, make_float4(vq[0], vq[1], vq[2], vq[3]));
+    } else {
+        uint32_t ww[4] = {r.w.x, r.w.y, r.w.z, r.w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            ww[j] = packed_element<MODE, U1>(pp[j], gg[j], ww[j], s, bad);
+        store_stream(static_cast<uint32_t *>(d.s1) + base + e, make_uint4(ww[0], ww[1], ww[2], ww[3]));
+    }
+    store_stream(d.p + base + e, make_float4(pp[0], pp[1], pp[2], pp[3]));
+}
+
 __device__ __forceinline__ bool has_zero(const float4 g)
 {
     return g.x == 0.0f || g.y == 0.0f || g.z == 0.0f || g.w == 0.0f;
@@ -565,6 +619,8 @@ __device__ __forceinline__ void pipe_consume(const unsigned char *smem, uint64_t
         sp.base = ti.base;
         sp.len = ti.len;
         sp.staged = ti.staged;
+        const int32_t head_n = ti.head;
+        bool released = false;
         if (d.vec) {
             const unsigned char *buf = smem + (size_t)st * L::kStageBytes;
             // Whole tile without a zero gradient in this warp: every vector
@@ -584,10 +640,18 @@ __device__ __forceinline__ void pipe_consume(const unsigned char *smem, uint64_t
                 fast = !__any_sync(0xFFFFFFFFu, z);
             }
             if (fast) {
+                // everything into registers, the stage back to the producer, then compute
+                RegVec<MODE> rv[kTileVecs];
 #pragma unroll
                 for (int v = 0; v < kTileVecs; ++v)
-                    pipe_vector_g<MODE, U1, false, GT>(buf, 4 * (ct + v * kConsumers), d, sp.base,
-                                                       gv[v], s, zs, bad);
+                    rv[v] = load_vec<MODE, GT>(buf, 4 * (ct + v * kConsumers), gv[v]);
+                __syncwarp();
+                if ((ct & 31) == 0)
+                    mbar_arrive(&empty[st]);
+                released = true;
+#pragma unroll
+                for (int v = 0; v < kTileVecs; ++v)
+                    compute_vec<MODE, U1>(rv[v], 4 * (ct + v * kConsumers), d, sp.base, s, bad);
             } else {
 #pragma unroll 1
                 for (int v = 0; v < kTileVecs; ++v) {
@@ -603,7 +667,7 @@ __device__ __forceinline__ void pipe_consume(const unsigned char *smem, uint64_t
             }
             // the <= 3 elements before the 16-byte body (first tile) and the
             // < unit after the staged part (last tile), one per thread
-            const bool head = ct < ti.head, tail = ct < sp.len - sp.staged;
+            const bool head = ct < head_n, tail = ct < sp.len - sp.staged;
             if (head || tail) {
 #pragma unroll 1
                 for (int r = head ? 0 : 1; r < (tail ? 2 : 1); ++r)
@@ -614,9 +678,11 @@ __device__ __forceinline__ void pipe_consume(const unsigned char *smem, uint64_t
         } else {
             bad += pipe_scalar_run<MODE, U1, GT>(d, sp.base + ct, sp.base + sp.len, kConsumers, s);
         }
-        __syncwarp();
-        if ((ct & 31) == 0)
-            mbar_arrive(&empty[st]);
+        if (!released) {
+            __syncwarp();
+            if ((ct & 31) == 0)
+                mbar_arrive(&empty[st]);
+        }
     }
 }
 
