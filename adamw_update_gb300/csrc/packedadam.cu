@@ -639,8 +639,10 @@ __device__ __forceinline__ void pipe_consume(const unsigned char *smem, uint64_t
                 }
                 fast = !__any_sync(0xFFFFFFFFu, z);
             }
-            if (fast) {
-                // everything into registers, the stage back to the producer, then compute
+            if (fast && MODE != kFP16) {
+                // everything into registers, the stage back to the producer, then
+                // compute (measured on GB300: +0.2 % E4, +0.4 % FP32, but -9 % in
+                // the FP16 mode, which keeps the plain order below)
                 RegVec<MODE> rv[kTileVecs];
 #pragma unroll
                 for (int v = 0; v < kTileVecs; ++v)
@@ -652,6 +654,11 @@ __device__ __forceinline__ void pipe_consume(const unsigned char *smem, uint64_t
 #pragma unroll
                 for (int v = 0; v < kTileVecs; ++v)
                     compute_vec<MODE, U1>(rv[v], 4 * (ct + v * kConsumers), d, sp.base, s, bad);
+            } else if (fast) {
+#pragma unroll
+                for (int v = 0; v < kTileVecs; ++v)
+                    pipe_vector_g<MODE, U1, false, GT>(buf, 4 * (ct + v * kConsumers), d, sp.base,
+                                                       gv[v], s, zs, bad);
             } else {
 #pragma unroll 1
                 for (int v = 0; v < kTileVecs; ++v) {
