@@ -9,13 +9,18 @@
 // include/packedadam.h.
 //
 // Design.  The step is elementwise and bound by HBM bandwidth (20 bytes per
-// parameter for the packed modes), so the kernels are built for bytes in
-// flight: a persistent grid (resident CTAs per SM x SM count) strides over
-// 16384-element chunks (8 waves of 2048); every thread issues all of its 16-byte loads of p, g
-// and the state for a chunk before any arithmetic, then stores with streaming
-// hints.  A multi-tensor list becomes one launch over a device-side
-// descriptor table, whose chunk prefix sums let each CTA walk from tensor to
-// tensor without a search.  No tensor cores: nothing here is a contraction.
+// parameter for the packed modes) and by instruction issue (the correctly
+// rounded divisions and square roots).  The step kernels are staged: one CTA
+// per SM, whose producer warp streams tiles of every input into a two-stage
+// shared-memory ring with bulk (TMA) copies and mbarriers, while 24 consumer
+// warps update the staged tiles and store the results straight to global
+// memory with streaming hints (adamw_step_pipe_kernel, blockwise8_pipe_kernel).
+// A multi-tensor list becomes one launch over a device-side descriptor table,
+// whose tile prefix sums let the producer walk from tensor to tensor without a
+// search; it hands each tile's geometry to the consumers with the tile.  The
+// register-staged adamw_step_kernel (every thread issues its 16-byte loads
+// before its arithmetic) serves the step on host-resident memory.  No tensor
+// cores: nothing here is a contraction.
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -36,6 +41,7 @@
 
 namespace pa {
 
+// ---- the register-staged kernel (step on host memory) and the codecs ----------
 constexpr int kThreads = 256;         // threads per CTA
 #ifndef PA_UNROLL
 #define PA_UNROLL 2
@@ -66,7 +72,7 @@ struct Desc {
     void *s1;        // uint32 words (packed modes) or FP32 m
     void *s2;        // FP32 v (FP32 mode)
     int64_t n;
-    int64_t chunk0;  // first global chunk index of this tensor
+    int64_t chunk0;  // first global work unit of this tensor: tile (staged kernels) or chunk
     int32_t head;
     int32_t vec;
 };

@@ -265,6 +265,9 @@ pa_status pa_adamw_step_packed_e4_host(float *p, const float *g, uint32_t *state
  * aligned), as produced by mixed-precision backward passes: each gradient is
  * widened exactly to binary32 and the step is the packed E4 step above, bit for
  * bit.  The gradient costs 2 bytes instead of 4: 18 bytes per parameter.
+ * The staged copies need the gradient 16-byte aligned where p's 16-byte body
+ * starts (true for whole tensors from an allocator); a tensor without that is
+ * updated with per-element accesses, with the same results.
  * pa_adamw_step_packed_e4_multi_bf16g reads list[t].g as a uint16 pointer.
  * ------------------------------------------------------------------------- */
 pa_status pa_adamw_step_packed_e4_bf16g(float *p, const uint16_t *g, uint32_t *state, int64_t n,
