@@ -100,6 +100,22 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def kernel_code_digest_input() -> str:
+    """The kernel sources with // comments and blank lines removed: the traffic
+    record stays valid across comment edits, not across code changes."""
+    import re
+
+    src = os.path.join(ROOT, "adamw_update_gb300", "csrc")
+    out = []
+    for name in ("packedadam.cu", "codecs.cuh", "blockwise.cuh", "pipeline.cuh"):
+        with open(os.path.join(src, name)) as f:
+            for line in f:
+                code = re.sub(r"//.*$", "", line).rstrip()
+                if code:
+                    out.append(code)
+    return "\n".join(out)
+
+
 def traffic_per_param(mode):
     """DRAM bytes per parameter of the step kernel from the committed ncu
     summary, if it was taken on the current kernel source; else None."""
@@ -111,11 +127,7 @@ def traffic_per_param(mode):
             d = json.load(f)
     except (OSError, ValueError):
         return None
-    src = os.path.join(ROOT, "adamw_update_gb300", "csrc")
-    h = hashlib.sha256()
-    for name in ("packedadam.cu", "codecs.cuh", "blockwise.cuh", "pipeline.cuh"):
-        with open(os.path.join(src, name), "rb") as f:
-            h.update(f.read())
+    h = hashlib.sha256(kernel_code_digest_input().encode())
     entry = d.get(mode)
     if not entry or entry.get("source_sha256") != h.hexdigest():
         return None
