@@ -912,7 +912,7 @@ template <int K>
 __device__ __forceinline__ uint2 requantise_fast(const float *x, uint32_t sb, const float *mid,
                                                  const uint8_t *table, int k)
 {
-    const float scale = __uint_as_float(sb), y = __frcp_rn(scale);
+    const float scale = __uint_as_float(sb), y = reciprocal_rn(scale);
     const uint32_t floor = fast_quotient_floor(sb);
     const float floorf = __uint_as_float(floor);
     uint2 code = make_uint2(0u, 0u);

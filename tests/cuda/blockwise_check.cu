@@ -1,7 +1,10 @@
 // GPU check of the blockwise requantiser's helpers (test code): the bucket
 // search against the plain 8-step binary search for every binary32 c in
-// [-1, 1], and the FMA division by the block scale against __fdiv_rn on
-// random (x, scale) pairs.  Kernels only add to counters and write the first
+// [-1, 1], the FMA division by the block scale against __fdiv_rn on random
+// (x, scale) pairs, the Newton-refined reciprocal against __frcp_rn for every
+// scale of the fast range, and whole codes (reciprocal, FMA quotient, bucket
+// search, IEEE fix-up below the floor) against the count of midpoints below
+// the IEEE quotient.  Kernels only add to counters and write the first
 // mismatch into a fixed 4-word slot claimed with atomicCAS.
 #include <cuda_runtime.h>
 #include <cstdint>
@@ -77,6 +80,83 @@ extern "C" int run_search_all(const float *qmap_host, unsigned long long *count_
     cudaMemcpy(q, qmap_host, 256 * 4, cudaMemcpyHostToDevice);
     cudaMemset(c, 0, 8); cudaMemset(f, 0, 16);
     search_all<<<152 * 4, kThreadsPerBlockwiseCta>>>(q, c, f);
+    const int e = (int)cudaDeviceSynchronize();
+    cudaMemcpy(count_host, c, 8, cudaMemcpyDeviceToHost);
+    cudaMemcpy(first_host, f, 16, cudaMemcpyDeviceToHost);
+    cudaFree(q); cudaFree(c); cudaFree(f);
+    return e;
+}
+
+// every scale bit pattern of [2^-100, 2^100)
+__global__ void reciprocal_all(unsigned long long *count, uint32_t *first)
+{
+    const uint32_t lo = 0x0D800000u, n = 0x71800000u - 0x0D800000u;
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        const float b = __uint_as_float(lo + i);
+        const uint32_t got = __float_as_uint(reciprocal_rn(b)), want = __float_as_uint(__frcp_rn(b));
+        if (got != want)
+            note(count, first, lo + i, 0, got, want);
+    }
+}
+
+// whole codes as the requantiser forms them, against count_below(IEEE quotient)
+__global__ void codes_random(const float *qmap, uint64_t n, uint64_t seed, unsigned long long *count,
+                             uint32_t *first)
+{
+    __shared__ float q[256], mid[512];
+    __shared__ uint8_t table[kBuckets];
+    __shared__ uint32_t red[32];
+    const int tid = threadIdx.x;
+    q[tid] = qmap[tid];
+    __syncthreads();
+    mid[tid] = tid < 255 ? __fmul_rn(__fadd_rn(q[tid], q[tid + 1]), 0.5f) : INFINITY;
+    mid[256 + tid] = INFINITY;
+    __syncthreads();
+    const int k = build_buckets(mid, table, red);
+    __syncthreads();
+    for (uint64_t i = blockIdx.x * (uint64_t)blockDim.x + tid; i < n; i += (uint64_t)gridDim.x * blockDim.x) {
+        const uint32_t r0 = mix32(3 * i + seed), r1 = mix32(3 * i + 1 + seed), r2 = mix32(3 * i + 2 + seed);
+        const uint32_t sb = 0x0D800000u + r0 % 0x64000000u;  // scale in the fast range
+        const uint32_t drop = (r1 >> 24) % 160u;
+        uint32_t xb = (r1 & 0x007FFFFFu) | ((sb & 0x7F800000u) - (drop << 23) * ((sb >> 23) > drop));
+        if ((sb >> 23) <= drop) xb = r1 & 0x007FFFFFu;
+        if (xb > sb) xb = sb;
+        if ((r2 & 0xFFu) == 0u) xb = 0u;
+        xb |= r2 & 0x80000000u;
+        const float x = __uint_as_float(xb), s = __uint_as_float(sb);
+        uint32_t got;
+        if (fabsf(x) < __uint_as_float(fast_quotient_floor(sb)) && needs_ieee_divide(x, fast_quotient_floor(sb)))
+            got = (uint32_t)count_below(mid, __fdiv_rn(x, s));
+        else
+            got = k <= 2 ? code_by_bucket<2>(mid, table, divide_by_scale_fma(x, s, reciprocal_rn(s)), k)
+                         : code_by_bucket<0>(mid, table, divide_by_scale_fma(x, s, reciprocal_rn(s)), k);
+        const uint32_t want = (uint32_t)count_below(mid, __fdiv_rn(x, s));
+        if (got != want)
+            note(count, first, xb, sb, got, want);
+    }
+}
+
+extern "C" int run_reciprocal_all(unsigned long long *count_host, uint32_t *first_host)
+{
+    unsigned long long *c; uint32_t *f;
+    if (cudaMalloc(&c, 8) || cudaMalloc(&f, 16)) return -1;
+    cudaMemset(c, 0, 8); cudaMemset(f, 0, 16);
+    reciprocal_all<<<152 * 8, 256>>>(c, f);
+    const int e = (int)cudaDeviceSynchronize();
+    cudaMemcpy(count_host, c, 8, cudaMemcpyDeviceToHost);
+    cudaMemcpy(first_host, f, 16, cudaMemcpyDeviceToHost);
+    cudaFree(c); cudaFree(f);
+    return e;
+}
+
+extern "C" int run_codes_random(const float *qmap_host, uint64_t n, uint64_t seed,
+                                unsigned long long *count_host, uint32_t *first_host)
+{
+    float *q; unsigned long long *c; uint32_t *f;
+    if (cudaMalloc(&q, 256 * 4) || cudaMalloc(&c, 8) || cudaMalloc(&f, 16)) return -1;
+    cudaMemcpy(q, qmap_host, 256 * 4, cudaMemcpyHostToDevice);
+    cudaMemset(c, 0, 8); cudaMemset(f, 0, 16);
+    codes_random<<<152 * 4, kThreadsPerBlockwiseCta>>>(q, n, seed, c, f);
     const int e = (int)cudaDeviceSynchronize();
     cudaMemcpy(count_host, c, 8, cudaMemcpyDeviceToHost);
     cudaMemcpy(first_host, f, 16, cudaMemcpyDeviceToHost);

@@ -4,7 +4,11 @@ table search equals the binary search over the 255 midpoints for every
 binary32 c in [-1, 1] (exhaustive, three maps), and the FMA division by the
 block scale (Markstein's correction with the correctly rounded reciprocal)
 equals the IEEE quotient __fdiv_rn on 4e9 random (x, scale) pairs with
-|x| <= scale, zeros and subnormal x included."""
+|x| <= scale, zeros and subnormal x included; the Newton-refined reciprocal
+equals __frcp_rn for every scale of the fast range [2^-100, 2^100); and whole
+codes as the requantiser forms them (that reciprocal, the FMA quotient, the
+bucket search, the IEEE fix-up below the floor) equal
+the count of midpoints below the IEEE quotient on 2^30 random pairs per map."""
 import ctypes
 import os
 import shutil
@@ -48,3 +52,23 @@ def test_block_division_equals_ieee(lib):
     rc = lib.run_divide_random(ctypes.c_uint64(4 << 30), ctypes.c_uint64(99), ctypes.byref(count), first)
     assert rc == 0
     assert count.value == 0, (count.value, [hex(x) for x in first])
+
+
+def test_reciprocal_equals_ieee_on_the_fast_range(lib):
+    count = ctypes.c_ulonglong(0)
+    first = (ctypes.c_uint32 * 4)()
+    assert lib.run_reciprocal_all(ctypes.byref(count), first) == 0
+    assert count.value == 0, (count.value, [hex(x) for x in first])
+
+
+@pytest.mark.parametrize("kind", ["dynamic_signed", "dynamic_unsigned", "linear", "random"])
+def test_requantised_codes_equal_the_ieee_definition(lib, kind):
+    q = {"dynamic_signed": wl.dynamic_qmap_signed, "dynamic_unsigned": wl.dynamic_qmap_unsigned,
+         "linear": wl.linear_qmap_signed, "random": lambda: wl.random_qmap(7, True)}[kind]()
+    q = np.ascontiguousarray(q, np.float32)
+    count = ctypes.c_ulonglong(0)
+    first = (ctypes.c_uint32 * 4)()
+    rc = lib.run_codes_random(q.ctypes.data_as(ctypes.c_void_p), ctypes.c_uint64(1 << 30),
+                              ctypes.c_uint64(5), ctypes.byref(count), first)
+    assert rc == 0
+    assert count.value == 0, (kind, count.value, [hex(x) for x in first])
