@@ -1,7 +1,8 @@
 """Packed-E4 steps that read bfloat16 gradients: bit for bit equal to the
-oracle run on the exactly widened gradient, single tensors and lists, every
-element phase (the 16-byte path with 8-byte gradient loads after a head peel)
-and mismatched phases (the 4-byte path)."""
+oracle run on the exactly widened gradient, single tensors and lists: views
+whose gradient is 16-byte aligned where p's 16-byte body starts (staged, with
+and without a head peel: offsets (0,0,0), (1,5,1), (3,7,3)), views where it is
+only 8-byte aligned there, and mismatched phases (the 4-byte path)."""
 import numpy as np
 import pytest
 
@@ -19,8 +20,9 @@ def _bf16(rng, n):
     return bits, (bits.astype(np.uint32) << 16).view(np.float32)
 
 
-@pytest.mark.parametrize("n", [1, 7, 4096, 4099, 70_001])
-@pytest.mark.parametrize("offsets", [(0, 0, 0), (1, 1, 1), (3, 3, 3), (1, 2, 1)])
+@pytest.mark.parametrize("n", [1, 7, 4096, 4099, 12_300, 70_001])
+@pytest.mark.parametrize("offsets", [(0, 0, 0), (1, 5, 1), (3, 7, 3), (1, 1, 1), (3, 3, 3),
+                                     (1, 2, 1)])
 def test_single_bf16_gradient(n, offsets):
     import torch
 

@@ -206,6 +206,48 @@ def test_multi_tensor_list_ragged(pa, mode):
     assert int(bad.item()) == 0
 
 
+@pytest.mark.parametrize("mode", ["e4", "fp16", "fp32"])
+def test_multi_tensor_list_longer_than_the_shared_table(pa, mode):
+    """600 tensors (more than the 512 descriptors the staged kernel copies into
+    shared memory, so the producer walks the table in global memory): sizes
+    from 0 to two tiles, views at every 4-byte phase; equals the oracle."""
+    import torch
+
+    rng = np.random.default_rng(11)
+    sizes = [int(x) for x in rng.choice([0, 1, 3, 4, 7, 100, 6143, 6144, 6149, 12_300], 600)]
+    host = _tensors(sizes, rng, mode)
+    devs = []
+    for k, h in enumerate(host):
+        off = (k // 3) % 4
+        views = []
+        for a in h:
+            dt = torch.int32 if a.dtype == np.uint32 else torch.float32
+            buf = torch.zeros(a.size + 8, dtype=dt, device="cuda")
+            v = buf[off:off + a.size]
+            v.copy_(dev(a)) if a.size else None
+            views.append(v)
+        devs.append(views)
+    bad = torch.zeros(1, dtype=torch.int64, device="cuda")
+    fn = {"e4": pa.pa_adamw_step_packed_e4_multi, "fp16": pa.pa_adamw_step_packed_fp16_multi,
+          "fp32": pa.pa_adamw_step_fp32_multi}[mode]
+    for t in (1, 2):
+        gs = [rng.normal(0, 1e-3, n).astype(np.float32) for n in sizes]
+        dgs = [dev(g) for g in gs]
+        fn([(d[0], dg, *d[1:]) for d, dg in zip(devs, dgs)], t, nonfinite=bad, **HY)
+        for h, g in zip(host, gs):
+            if mode == "fp32":
+                h[0], h[1], h[2], _ = oracle.step_fp32(h[0], g, h[1], h[2], t, **HY)
+            else:
+                h[0], h[1], _ = oracle.step_packed(h[0], g, h[1], t, mode=mode, **HY)
+    torch.cuda.synchronize()
+    for k, (h, d) in enumerate(zip(host, devs)):
+        assert_same_bits(host_f32(d[0]), h[0], f"tensor {k} p")
+        for a, dd in zip(h[1:], d[1:]):
+            got = host_u32(dd) if a.dtype == np.uint32 else host_f32(dd)
+            assert_same_bits(got, a, f"tensor {k} state")
+    assert int(bad.item()) == 0
+
+
 def test_multi_gpt52_equals_oracle(pa):
     """The 52-tensor GPT list (9,677,312 parameters), packed E4, 2 steps."""
     import torch
