@@ -321,9 +321,11 @@ def _host_ptr(t, dtype):
 
 def pa_adamw_step_packed_e4_host(p, g, state, workspace, step, lr=1e-3, beta1=0.9, beta2=0.999,
                                  eps=1e-8, wd=0.0, nonfinite=None, stream=None):
-    """Packed-E4 step over host tensors (pinned for overlap), streamed through
-    the CUDA tensor `workspace` (uint8, >= 2.36 MB; larger means longer
-    chunks).  Synchronise `stream` before reading p or state."""
+    """Packed-E4 step over host tensors.  Pinned tensors are read and written
+    in place by the step kernel over the host link; otherwise they are
+    streamed through the CUDA tensor `workspace` (uint8, >= 2.36 MB; larger
+    means longer chunks), which is checked either way.  Synchronise `stream`
+    before reading p or state."""
     torch = _t()
     _check(_lib.pa_adamw_step_packed_e4_host(
         _host_ptr(p, torch.float32), _host_ptr(g, torch.float32), _host_ptr(state, torch.int32),
