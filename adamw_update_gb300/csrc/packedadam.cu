@@ -715,17 +715,20 @@ __device__ __forceinline__ void pipe_body(const Desc *__restrict__ table, int32_
         }
         mbar_init_fence();
     }
+    // the producer's copy of the table, in 8-byte words, by every thread (one
+    // or two loads each, so the first copies are not held up)
+    const bool table_shared = MULTI && ntensors <= kSmemDescs;
+    if (table_shared) {
+        const uint64_t *src = reinterpret_cast<const uint64_t *>(table);
+        uint64_t *dst = reinterpret_cast<uint64_t *>(pipe_smem + L::kDescs);
+        constexpr int kWords = sizeof(Desc) / sizeof(uint64_t);
+        for (int i = threadIdx.x; i < ntensors * kWords; i += kPipeThreads)
+            dst[i] = __ldg(src + i);
+    }
     __syncthreads();
     if (threadIdx.x >= kConsumers) {  // the producer warp
-        if (MULTI && ntensors <= kSmemDescs) {  // its copy of the table, in 8-byte words
-            const uint64_t *src = reinterpret_cast<const uint64_t *>(table);
-            uint64_t *dst = reinterpret_cast<uint64_t *>(pipe_smem + L::kDescs);
-            constexpr int kWords = sizeof(Desc) / sizeof(uint64_t);
-            for (int i = threadIdx.x - kConsumers; i < ntensors * kWords; i += 32)
-                dst[i] = __ldg(src + i);
-            __syncwarp();
+        if (table_shared)
             table = reinterpret_cast<const Desc *>(pipe_smem + L::kDescs);
-        }
         if (threadIdx.x == kConsumers)
             pipe_produce<MODE, MULTI, GT>(pipe_smem, full, empty, table, ntensors, total_tiles,
                                           single);
