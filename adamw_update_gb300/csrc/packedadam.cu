@@ -886,7 +886,8 @@ struct BwItemInfo {
     int32_t codes; // the code arrays were staged
 };
 constexpr size_t kBwSmemBytes = kBwStages * kBwStageBytes + sizeof(BlockwiseShared) +
-                                2 * kBwStages * sizeof(uint64_t) + kBwSlots * sizeof(BwItemInfo);
+                                2 * kBwStages * sizeof(uint64_t) + kBwSlots * sizeof(BwItemInfo) +
+                                sizeof(int64_t);
 
 // Redo, with the IEEE divide, the codes of the values that need it.
 __device__ __noinline__ uint2 requantise_fixup(float x0, float x1, float x2, float x3, float x4,
@@ -1114,65 +1115,88 @@ __device__ __forceinline__ bool codes_staged(const BlockwiseArgs &a)
     return ((reinterpret_cast<uintptr_t>(a.m_code) | reinterpret_cast<uintptr_t>(a.v_code)) & 15u) == 0;
 }
 
+// Stage an item: write its slot and issue its bulk copies into stage
+// j % kBwStages (j: the CTA's item count).  Issued by thread 0 for the first
+// two items and afterwards by the consumer warp whose release completes a
+// stage, so the kernel needs no producer warp (24 warps, 80 registers each).
+// `cur` is the shared table position: written by whichever thread issues,
+// possibly out of order, but every value written is the tensor of an item at
+// or before any later one, and the walk only moves forward from it.
 template <bool MULTI>
-__device__ __forceinline__ void bw_produce(unsigned char *smem, uint64_t *full, uint64_t *empty,
-                                           BwItemInfo *info, const BwDesc *table, int32_t ntensors,
-                                           int64_t total, const BwDesc &single)
+__device__ __forceinline__ void bw_issue(unsigned char *smem, uint64_t *full, BwItemInfo *info,
+                                         const BwDesc *table, int32_t ntensors,
+                                         const BwDesc &single, volatile int32_t *cur, int64_t j)
 {
-    BwCursor<MULTI> cur(table, ntensors, total, single);
-    int64_t k = 0;
-    for (int64_t c = blockIdx.x; c < total; c += gridDim.x, ++k) {
-        cur.seek(c, total);
-        const int st = (int)(k % kBwStages);
-        const uint32_t use = (uint32_t)(k / kBwStages);
-        if (!mbar_wait(&empty[st], (use & 1u) ^ 1u)) {
-            pipe_fault(kFaultEmptyWait);
-            break;
-        }
-        const BlockwiseArgs &a = cur.d.a;
-        const int64_t kt = c - cur.d.item0;
-        const int64_t nf = a.n / kBlock;
-        BwItemInfo &it = info[k % kBwSlots];
-        it.a = a;
-        if (kt < bw_full_tiles(a.n)) {
-            const int64_t b0 = kt * kBwGroups;
-            const int64_t nb = nf - b0 < kBwGroups ? nf - b0 : kBwGroups;
-            const uint32_t elems = (uint32_t)(nb * kBlock);
-            const int64_t e0 = b0 * kBlock;
-            const bool codes = codes_staged(a);
-            it.b0 = b0;
-            it.nblk = (int32_t)nb;
-            it.codes = codes ? 1 : 0;
-            mbar_arrive_expect(&full[st], elems * (codes ? 10u : 8u));  // releases the slot too
-            unsigned char *buf = smem + (size_t)st * kBwStageBytes;
-            bulk_load(buf, a.p + e0, elems * 4u, &full[st]);
-            bulk_load(buf + kBwTile * 4, a.g + e0, elems * 4u, &full[st]);
-            if (codes) {
-                bulk_load(buf + kBwTile * 8, a.m_code + e0, elems, &full[st]);
-                bulk_load(buf + kBwTile * 9, a.v_code + e0, elems, &full[st]);
-            }
-        } else {  // the short last block: read from global memory
-            it.b0 = nf;
-            it.nblk = 0;
-            it.codes = 0;
-            mbar_arrive_expect(&full[st], 0u);
-        }
+    const int64_t c = blockIdx.x + j * (int64_t)gridDim.x;
+    const int st = (int)(j % kBwStages);
+    const BwDesc *dp = &single;
+    if (MULTI) {
+        int32_t t = *cur;
+        while (t + 1 < ntensors && c >= table[t + 1].item0)
+            ++t;
+        *cur = t;
+        dp = table + t;
     }
-    for (int64_t j = k > kBwStages ? k - kBwStages : 0; j < k; ++j)
-        if (!mbar_wait(&full[j % kBwStages], (uint32_t)((j / kBwStages) & 1)))
-            pipe_fault(kFaultCopyWait);
+    const BlockwiseArgs a = dp->a;
+    const int64_t kt = c - dp->item0;
+    const int64_t nf = a.n / kBlock;
+    BwItemInfo &it = info[j % kBwSlots];
+    it.a = a;
+    if (kt < bw_full_tiles(a.n)) {
+        const int64_t b0 = kt * kBwGroups;
+        const int64_t nb = nf - b0 < kBwGroups ? nf - b0 : kBwGroups;
+        const uint32_t elems = (uint32_t)(nb * kBlock);
+        const int64_t e0 = b0 * kBlock;
+        const bool codes = codes_staged(a);
+        it.b0 = b0;
+        it.nblk = (int32_t)nb;
+        it.codes = codes ? 1 : 0;
+        mbar_arrive_expect(&full[st], elems * (codes ? 10u : 8u));  // releases the slot too
+        unsigned char *buf = smem + (size_t)st * kBwStageBytes;
+        bulk_load(buf, a.p + e0, elems * 4u, &full[st]);
+        bulk_load(buf + kBwTile * 4, a.g + e0, elems * 4u, &full[st]);
+        if (codes) {
+            bulk_load(buf + kBwTile * 8, a.m_code + e0, elems, &full[st]);
+            bulk_load(buf + kBwTile * 9, a.v_code + e0, elems, &full[st]);
+        }
+    } else {  // the short last block: read from global memory
+        it.b0 = nf;
+        it.nblk = 0;
+        it.codes = 0;
+        mbar_arrive_expect(&full[st], 0u);
+    }
 }
 
-__device__ __forceinline__ void bw_consume(const unsigned char *smem, uint64_t *full, uint64_t *empty,
-                                           BlockwiseShared &sh, const BwItemInfo *info,
-                                           int64_t total, const Scalars &s, int k1, int k2,
-                                           uint32_t &bad)
+// One release of stage st by a warp (lane 0); true for the warp whose release
+// completes it, which then owns the stage: every warp's reads of it are
+// ordered before the release (acquire-release counter), and the proxy fence
+// orders them before the bulk copies that will overwrite it.
+__device__ __forceinline__ bool bw_release(uint32_t *count)
+{
+    uint32_t old;
+    asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], 1;"
+                 : "=r"(old)
+                 : "r"(smem_addr(count))
+                 : "memory");
+    if (old != (uint32_t)(kConsumerWarps - 1))
+        return false;
+    *count = 0u;  // no release of this stage's next use precedes its refill
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    return true;
+}
+
+template <bool MULTI>
+__device__ __forceinline__ void bw_consume(unsigned char *smem, uint64_t *full, uint32_t *released,
+                                           BlockwiseShared &sh, BwItemInfo *info,
+                                           const BwDesc *table, int32_t ntensors,
+                                           const BwDesc &single, volatile int32_t *cur,
+                                           int64_t total, int64_t items, const Scalars &s, int k1,
+                                           int k2, uint32_t &bad)
 {
     const int group = threadIdx.x >> 8, gt = threadIdx.x & 255;
     const int kmax = k1 > k2 ? k1 : k2;
     uint32_t gpar = 0;
-    int64_t k = 0;
-    for (int64_t c = blockIdx.x; c < total; c += gridDim.x, ++k) {
+    for (int64_t k = 0; k < items; ++k) {
         const int st = (int)(k % kBwStages);
         if (!mbar_wait(&full[st], (uint32_t)((k / kBwStages) & 1))) {
             pipe_fault(kFaultFullWait);
@@ -1219,10 +1243,11 @@ __device__ __forceinline__ void bw_consume(const unsigned char *smem, uint64_t *
                 }
             }
         }
-        // the stage is no longer read: hand it back before computing
+        // the stage is no longer read: hand it back before computing; the last
+        // warp to do so refills it with the item kBwStages ahead
         __syncwarp();
-        if ((threadIdx.x & 31) == 0)
-            mbar_arrive(&empty[st]);
+        if ((threadIdx.x & 31) == 0 && bw_release(&released[st]) && k + kBwStages < items)
+            bw_issue<MULTI>(smem, full, info, table, ntensors, single, cur, k + kBwStages);
         if (mine) {
             // whole blocks with at most one midpoint per bucket (the log-linear
             // maps): the specialised body; anything else: the generic one
@@ -1235,12 +1260,13 @@ __device__ __forceinline__ void bw_consume(const unsigned char *smem, uint64_t *
     }
 }
 
-// The blockwise step over a tensor list (MULTI) or one tensor.  One CTA per
-// SM: the producer warp stages p, g and (when both code arrays are 16-byte
-// aligned) the two code arrays of a tile of kBwGroups blocks; three groups of
-// 8 consumer warps update one block each.
+// The blockwise step over a tensor list (MULTI) or one tensor.  One CTA of 24
+// warps per SM: three groups of 8 warps update one block each of a tile of
+// kBwGroups blocks staged (p, g and, when both code arrays are 16-byte
+// aligned, the two code arrays) by bulk copies into a two-stage ring; the
+// warp whose release completes a stage issues the copies of its next item.
 template <bool MULTI>
-__global__ void __launch_bounds__(kPipeThreads, 1)
+__global__ void __launch_bounds__(kConsumers, 1)
 blockwise8_pipe_kernel(const BwDesc *__restrict__ table, int32_t ntensors, int64_t total_items,
                        const BwDesc single, const float *__restrict__ qmap1,
                        const float *__restrict__ qmap2, const Scalars s,
@@ -1249,24 +1275,29 @@ blockwise8_pipe_kernel(const BwDesc *__restrict__ table, int32_t ntensors, int64
     extern __shared__ __align__(128) unsigned char bw_smem[];
     BlockwiseShared &sh = *reinterpret_cast<BlockwiseShared *>(bw_smem + kBwStages * kBwStageBytes);
     uint64_t *full = reinterpret_cast<uint64_t *>(bw_smem + kBwStages * kBwStageBytes + sizeof(BlockwiseShared));
-    uint64_t *empty = full + kBwStages;
-    BwItemInfo *info = reinterpret_cast<BwItemInfo *>(empty + kBwStages);
+    uint32_t *released = reinterpret_cast<uint32_t *>(full + kBwStages);  // kBwStages counters
+    BwItemInfo *info = reinterpret_cast<BwItemInfo *>(full + 2 * kBwStages);
+    volatile int32_t *cur = reinterpret_cast<volatile int32_t *>(info + kBwSlots);
+    // this CTA's items: blockIdx.x, blockIdx.x + gridDim.x, ...
+    const int64_t items = total_items > blockIdx.x
+                              ? (total_items - blockIdx.x + gridDim.x - 1) / gridDim.x
+                              : 0;
     int k1, k2;
     if (threadIdx.x == 0) {
         for (int i = 0; i < kBwStages; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], kConsumerWarps);
+            released[i] = 0u;
         }
+        *cur = 0;
         mbar_init_fence();
     }
     blockwise_setup(sh, qmap1, qmap2, k1, k2);  // ends with __syncthreads
-    if (threadIdx.x >= kConsumers) {
-        if (threadIdx.x == kConsumers)
-            bw_produce<MULTI>(bw_smem, full, empty, info, table, ntensors, total_items, single);
-        return;
-    }
+    if (threadIdx.x == 0)
+        for (int64_t j = 0; j < kBwStages && j < items; ++j)
+            bw_issue<MULTI>(bw_smem, full, info, table, ntensors, single, cur, j);
     uint32_t bad = 0;
-    bw_consume(bw_smem, full, empty, sh, info, total_items, s, k1, k2, bad);
+    bw_consume<MULTI>(bw_smem, full, released, sh, info, table, ntensors, single, cur,
+                      total_items, items, s, k1, k2, bad);
     flush_nonfinite(bad, nonfinite);
 }
 
@@ -1404,7 +1435,8 @@ pa_status chunk_size(int slot, int64_t elements, int64_t *chunk)
 // of the SM), capped by the tiles.  The first launch of each kernel on a device
 // raises its dynamic shared-memory limit to `smem`, the most any launch of it
 // uses (a launch passes what it needs: the descriptor copy depends on the list).
-pa_status pipe_grid(const void *kernel, size_t smem, int64_t tiles, int *grid)
+pa_status pipe_grid(const void *kernel, size_t smem, int64_t tiles, int *grid,
+                    int threads = pa::kPipeThreads)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1424,7 +1456,7 @@ pa_status pipe_grid(const void *kernel, size_t smem, int64_t tiles, int *grid)
         if (e != cudaSuccess)
             return cuda_fail(e, "raising the shared-memory limit of the staged step");
         int occ = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, pa::kPipeThreads, smem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, threads, smem);
         if (e != cudaSuccess)
             return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
         if (occ < 1)
@@ -1845,9 +1877,9 @@ pa_status pa_adamw_step_blockwise8(const float *p, const float *g, uint16_t *p_b
     const int64_t items = pa::bw_full_tiles(n) + (n % pa::kBlock != 0 ? 1 : 0);
     int grid = 0;
     if ((st = pipe_grid((const void *)pa::blockwise8_pipe_kernel<false>, pa::kBwSmemBytes, items,
-                        &grid)) != PA_OK)
+                        &grid, pa::kConsumers)) != PA_OK)
         return st;
-    pa::blockwise8_pipe_kernel<false><<<grid, pa::kPipeThreads, pa::kBwSmemBytes, (cudaStream_t)stream>>>(
+    pa::blockwise8_pipe_kernel<false><<<grid, pa::kConsumers, pa::kBwSmemBytes, (cudaStream_t)stream>>>(
         nullptr, 1, items, d, qmap1, qmap2, s, nonfinite);
     return check_launch("blockwise8_pipe_kernel launch");
 }
@@ -2425,11 +2457,11 @@ extern "C" pa_status pa_adamw_step_blockwise8_multi(const pa_blockwise_tensor *l
         return st;
     int grid = 0;
     if ((st = pipe_grid((const void *)pa::blockwise8_pipe_kernel<true>, pa::kBwSmemBytes, items,
-                        &grid)) != PA_OK)
+                        &grid, pa::kConsumers)) != PA_OK)
         return st;
     pa::BwDesc none;
     std::memset(&none, 0, sizeof none);
-    pa::blockwise8_pipe_kernel<true><<<grid, pa::kPipeThreads, pa::kBwSmemBytes, (cudaStream_t)stream>>>(
+    pa::blockwise8_pipe_kernel<true><<<grid, pa::kConsumers, pa::kBwSmemBytes, (cudaStream_t)stream>>>(
         table, ntensors, items, none, qmap1, qmap2, s, nonfinite);
     return check_launch("blockwise8_pipe_kernel (multi) launch");
 }
