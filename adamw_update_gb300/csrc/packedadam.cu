@@ -111,7 +111,7 @@ __device__ __forceinline__ uint32_t packed_element(float &p, float g, uint32_t w
     bad += any_nonfinite(o);
     p = o.p;
     if (!UNIT_BC2)
-        rn = __fsqrt_rn(o.v);  // with bc2 == 1 the update already took sqrt(v')
+        rn = ZS ? sqrt_zero_safe(o.v) : __fsqrt_rn(o.v);  // bc2 == 1: the update took sqrt(v')
     return MODE == kE4 ? encode_step_word_e4(o.m, o.v, rn) : encode_word_fp16(o.m, rn);
 }
 
@@ -344,7 +344,7 @@ struct PipeLayout {
     static constexpr size_t kInfo = kBarriers + 2 * kStages * sizeof(uint64_t);
     static constexpr size_t kDescs = kInfo + kStages * sizeof(TileInfo);
     static constexpr size_t kBytes = kDescs + (size_t)kSmemDescs * sizeof(Desc);  // the most
-    // dynamic shared memory of a launch over `ntensors` tensors (MULTI)
+    // dynamic shared memory of a launch over `ntensors` tensors
     static size_t bytes_for(int32_t ntensors)
     {
         return kDescs + (ntensors <= kSmemDescs ? (size_t)ntensors * sizeof(Desc) : 0);
@@ -389,40 +389,32 @@ __device__ __forceinline__ Span tile_span(const Desc &d, int64_t k, int unit)
 }
 
 // Walks the descriptor table forward to the tensor of global tile c.
-template <bool MULTI>
 struct TableCursor {
     const Desc *table;
     int32_t ntensors, t;
     int64_t next;
     Desc d;
-    __device__ __forceinline__ TableCursor(const Desc *tab, int32_t nt, int64_t total,
-                                           const Desc &single)
-        : table(tab), ntensors(nt), t(0), next(total), d(single)
+    __device__ __forceinline__ TableCursor(const Desc *tab, int32_t nt, int64_t total)
+        : table(tab), ntensors(nt), t(0), next(nt > 1 ? tab[1].chunk0 : total), d(tab[0])
     {
-        if (MULTI) {
-            d = table[0];
-            next = ntensors > 1 ? table[1].chunk0 : total;
-        }
     }
     __device__ __forceinline__ void seek(int64_t c, int64_t total)
     {
-        if (MULTI)
-            while (c >= next) {
-                ++t;
-                d = table[t];
-                next = t + 1 < ntensors ? table[t + 1].chunk0 : total;
-            }
+        while (c >= next) {
+            ++t;
+            d = table[t];
+            next = t + 1 < ntensors ? table[t + 1].chunk0 : total;
+        }
     }
 };
 
-template <int MODE, bool MULTI, typename GT>
+template <int MODE, typename GT>
 __device__ __forceinline__ void pipe_produce(unsigned char *smem, uint64_t *full, uint64_t *empty,
-                                             const Desc *table, int32_t ntensors, int64_t total,
-                                             const Desc &single)
+                                             const Desc *table, int32_t ntensors, int64_t total)
 {
     using L = PipeLayout<MODE, GT>;
     TileInfo *info = reinterpret_cast<TileInfo *>(smem + L::kInfo);
-    TableCursor<MULTI> cur(table, ntensors, total, single);
+    TableCursor cur(table, ntensors, total);
     int64_t k = 0;  // fills issued
     for (int64_t c = blockIdx.x; c < total; c += gridDim.x, ++k) {
         cur.seek(c, total);
@@ -699,7 +691,8 @@ __device__ __forceinline__ void pipe_consume(const unsigned char *smem, uint64_t
     }
 }
 
-template <int MODE, bool MULTI, bool U1, typename GT = float>
+// table == nullptr: one tensor, described by `single` (ntensors == 1).
+template <int MODE, bool U1, typename GT = float>
 __device__ __forceinline__ void pipe_body(const Desc *__restrict__ table, int32_t ntensors,
                                           int64_t total_tiles, const Desc &single,
                                           const Scalars &s, unsigned long long *nonfinite)
@@ -716,9 +709,15 @@ __device__ __forceinline__ void pipe_body(const Desc *__restrict__ table, int32_
         mbar_init_fence();
     }
     // the producer's copy of the table, in 8-byte words, by every thread (one
-    // or two loads each, so the first copies are not held up)
-    const bool table_shared = MULTI && ntensors <= kSmemDescs;
-    if (table_shared) {
+    // or two loads each, so the first copies are not held up); a descriptor
+    // passed by value is stored by thread 0.  (One tensor through this table
+    // path measured 0.4 % faster on GB300 than a producer reading the
+    // descriptor from the launch parameters.)
+    const bool table_shared = ntensors <= kSmemDescs;
+    if (table == nullptr) {
+        if (threadIdx.x == 0)
+            *reinterpret_cast<Desc *>(pipe_smem + L::kDescs) = single;
+    } else if (table_shared) {
         const uint64_t *src = reinterpret_cast<const uint64_t *>(table);
         uint64_t *dst = reinterpret_cast<uint64_t *>(pipe_smem + L::kDescs);
         constexpr int kWords = sizeof(Desc) / sizeof(uint64_t);
@@ -730,8 +729,7 @@ __device__ __forceinline__ void pipe_body(const Desc *__restrict__ table, int32_
         if (table_shared)
             table = reinterpret_cast<const Desc *>(pipe_smem + L::kDescs);
         if (threadIdx.x == kConsumers)
-            pipe_produce<MODE, MULTI, GT>(pipe_smem, full, empty, table, ntensors, total_tiles,
-                                          single);
+            pipe_produce<MODE, GT>(pipe_smem, full, empty, table, ntensors, total_tiles);
         return;
     }
     uint32_t bad = 0;
@@ -739,12 +737,12 @@ __device__ __forceinline__ void pipe_body(const Desc *__restrict__ table, int32_
     flush_nonfinite(bad, nonfinite);
 }
 
-template <int MODE, bool MULTI, bool U1, typename GT = float>
+template <int MODE, bool U1, typename GT = float>
 __global__ void __launch_bounds__(kPipeThreads, 1)
 adamw_step_pipe_kernel(const Desc *__restrict__ table, int32_t ntensors, int64_t total_tiles,
                        const Desc single, const Scalars s, unsigned long long *nonfinite)
 {
-    pipe_body<MODE, MULTI, U1, GT>(table, ntensors, total_tiles, single, s, nonfinite);
+    pipe_body<MODE, U1, GT>(table, ntensors, total_tiles, single, s, nonfinite);
 }
 
 // Graph-replayable variant: the scalars of the step are row *index of a
@@ -766,7 +764,7 @@ adamw_step_table_kernel(const Desc *__restrict__ table, int32_t ntensors, int64_
     }
     const Scalars s = rows[i];
     Desc none = {};
-    pipe_body<MODE, true, false>(table, ntensors, total_tiles, none, s, nonfinite);
+    pipe_body<MODE, false>(table, ntensors, total_tiles, none, s, nonfinite);
 }
 
 __global__ void advance_index_kernel(int64_t *index)
@@ -1558,17 +1556,17 @@ pa_status step_single(const pa_tensor &t, int64_t step, double lr, double beta1,
     const int64_t tiles = describe(t, MODE, pa::kTile, &d, (int)sizeof(GT));
     d.chunk0 = 0;
     const size_t smem = pa::PipeLayout<MODE, GT>::kBytes;  // the kernel's limit
-    const size_t used = pa::PipeLayout<MODE, GT>::kDescs;  // no table: one tensor
-    const void *kern = s.bc2 == 1.0f ? (const void *)pa::adamw_step_pipe_kernel<MODE, false, true, GT>
-                                     : (const void *)pa::adamw_step_pipe_kernel<MODE, false, false, GT>;
+    const size_t used = pa::PipeLayout<MODE, GT>::bytes_for(1);  // the descriptor, by value
+    const void *kern = s.bc2 == 1.0f ? (const void *)pa::adamw_step_pipe_kernel<MODE, true, GT>
+                                     : (const void *)pa::adamw_step_pipe_kernel<MODE, false, GT>;
     int grid = 0;
     if ((st = pipe_grid(kern, smem, tiles, &grid)) != PA_OK)
         return st;
     if (s.bc2 == 1.0f)
-        pa::adamw_step_pipe_kernel<MODE, false, true, GT><<<grid, pa::kPipeThreads, used, (cudaStream_t)stream>>>(
+        pa::adamw_step_pipe_kernel<MODE, true, GT><<<grid, pa::kPipeThreads, used, (cudaStream_t)stream>>>(
             nullptr, 1, tiles, d, s, nonfinite);
     else
-        pa::adamw_step_pipe_kernel<MODE, false, false, GT><<<grid, pa::kPipeThreads, used, (cudaStream_t)stream>>>(
+        pa::adamw_step_pipe_kernel<MODE, false, GT><<<grid, pa::kPipeThreads, used, (cudaStream_t)stream>>>(
             nullptr, 1, tiles, d, s, nonfinite);
     return check_launch("adamw_step_pipe_kernel launch");
 }
@@ -1684,6 +1682,11 @@ pa_status step_multi(const pa_tensor *list, int32_t ntensors, int64_t step, doub
     }
     if (total == 0)
         return ok();
+    // A one-tensor list goes by value in the launch's parameters: no table to
+    // look up, allocate or upload, so a list whose pointers change from step
+    // to step never meets cudaMalloc's or cudaMemcpy's synchronisation.
+    if (ntensors == 1)
+        return step_single<MODE, GT>(list[0], step, lr, beta1, beta2, eps, wd, nonfinite, stream);
     const Desc *table = nullptr;
     Desc none;
     std::memset(&none, 0, sizeof none);
@@ -1692,16 +1695,16 @@ pa_status step_multi(const pa_tensor *list, int32_t ntensors, int64_t step, doub
         return st;
     const size_t smem = pa::PipeLayout<MODE, GT>::kBytes;  // the kernel's limit
     const size_t used = pa::PipeLayout<MODE, GT>::bytes_for(ntensors);
-    const void *kern = s.bc2 == 1.0f ? (const void *)pa::adamw_step_pipe_kernel<MODE, true, true, GT>
-                                     : (const void *)pa::adamw_step_pipe_kernel<MODE, true, false, GT>;
+    const void *kern = s.bc2 == 1.0f ? (const void *)pa::adamw_step_pipe_kernel<MODE, true, GT>
+                                     : (const void *)pa::adamw_step_pipe_kernel<MODE, false, GT>;
     int grid = 0;
     if ((st = pipe_grid(kern, smem, tiles, &grid)) != PA_OK)
         return st;
     if (s.bc2 == 1.0f)
-        pa::adamw_step_pipe_kernel<MODE, true, true, GT><<<grid, pa::kPipeThreads, used, (cudaStream_t)stream>>>(
+        pa::adamw_step_pipe_kernel<MODE, true, GT><<<grid, pa::kPipeThreads, used, (cudaStream_t)stream>>>(
             table, ntensors, tiles, none, s, nonfinite);
     else
-        pa::adamw_step_pipe_kernel<MODE, true, false, GT><<<grid, pa::kPipeThreads, used, (cudaStream_t)stream>>>(
+        pa::adamw_step_pipe_kernel<MODE, false, GT><<<grid, pa::kPipeThreads, used, (cudaStream_t)stream>>>(
             table, ntensors, tiles, none, s, nonfinite);
     return check_launch("adamw_step_pipe_kernel (multi) launch");
 }
@@ -2018,18 +2021,18 @@ extern "C" pa_status pa_adamw_step_packed_e4_multi_noalloc(
         return cuda_fail(e, "descriptor upload to the fixed device array");
     const size_t smem = pa::PipeLayout<pa::kE4>::kBytes;  // the kernel's limit
     const size_t used = pa::PipeLayout<pa::kE4>::bytes_for(ntensors);
-    const void *kern = s.bc2 == 1.0f ? (const void *)pa::adamw_step_pipe_kernel<pa::kE4, true, true>
-                                     : (const void *)pa::adamw_step_pipe_kernel<pa::kE4, true, false>;
+    const void *kern = s.bc2 == 1.0f ? (const void *)pa::adamw_step_pipe_kernel<pa::kE4, true>
+                                     : (const void *)pa::adamw_step_pipe_kernel<pa::kE4, false>;
     int grid = 0;
     if ((st = pipe_grid(kern, smem, tiles, &grid)) != PA_OK)
         return st;
     pa::Desc none;
     std::memset(&none, 0, sizeof none);
     if (s.bc2 == 1.0f)
-        pa::adamw_step_pipe_kernel<pa::kE4, true, true><<<grid, pa::kPipeThreads, used, (cudaStream_t)stream>>>(
+        pa::adamw_step_pipe_kernel<pa::kE4, true><<<grid, pa::kPipeThreads, used, (cudaStream_t)stream>>>(
             table, ntensors, tiles, none, s, nonfinite);
     else
-        pa::adamw_step_pipe_kernel<pa::kE4, true, false><<<grid, pa::kPipeThreads, used, (cudaStream_t)stream>>>(
+        pa::adamw_step_pipe_kernel<pa::kE4, false><<<grid, pa::kPipeThreads, used, (cudaStream_t)stream>>>(
             table, ntensors, tiles, none, s, nonfinite);
     return check_launch("adamw_step_pipe_kernel (no-alloc multi) launch");
 }

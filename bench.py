@@ -46,8 +46,8 @@ sys.path.insert(0, ROOT)
 import workloads as wl  # noqa: E402
 
 BYTES_PER_PARAM = {"e4": 20, "fp16": 20, "fp32": 28, "blockwise": 14 + 16 / 2048}
-KERNEL_NAME = {"e4": "adamw_step_pipe_kernel<0,true>", "fp16": "adamw_step_pipe_kernel<1,true>",
-               "fp32": "adamw_step_pipe_kernel<2,true>", "blockwise": "blockwise8_pipe_kernel<false>"}
+KERNEL_NAME = {"e4": "adamw_step_pipe_kernel<0>", "fp16": "adamw_step_pipe_kernel<1>",
+               "fp32": "adamw_step_pipe_kernel<2>", "blockwise": "blockwise8_pipe_kernel<false>"}
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_HBM_GBS = 6800.0
 
@@ -551,7 +551,7 @@ def run_ours(args):
                 "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "peak_source": peak_kind,
                 "traffic": None if traffic is None else traffic * w.n,
-                "kernel": ("adamw_step_pipe_kernel<0,true,bfloat16>" if args.grad == "bf16"
+                "kernel": ("adamw_step_pipe_kernel<0,bfloat16>" if args.grad == "bf16"
                            else "adamw_step_table_kernel<0>" if args.graph
                            else KERNEL_NAME[w.mode]),
                 "kernel_ms": kernel_ms,

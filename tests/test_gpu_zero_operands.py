@@ -2,14 +2,15 @@
 against the CPU oracle.
 
 The step kernels keep exactly-zero gradients on zero state off the slow path
-of CUDA's correctly rounded division and square root: v' is raised to a floor
-before the square roots when the launch has shown that this cannot change
-den = sqrt(v'/bc2) + eps, and u/den with u = +-0 selects u.  These tests feed
-what those substitutions must leave untouched: +-0 and subnormal gradients,
-gradients whose square underflows, zero and random prior state (every E4
-code; binary16 words with NaN and Inf codes), p = +-0, and hyperparameters on
-both sides of the floor condition (eps = 0, eps far below sqrt(2^-126/bc2),
-bc2 near 0, lr = 0, early and late steps, where bc2 rounds to 1).
+of CUDA's correctly rounded division and square root: a warp holding such a
+gradient divides v' by bc2 with Markstein's method (rb = RN(1/bc2)), takes
+u/den with u = +-0 as u, and the roots of a zero v'/bc2 or v' as that zero.
+These tests feed what those substitutions must leave untouched: +-0 and
+subnormal gradients, gradients whose square underflows, zero and random prior
+state (every E4 code; binary16 words with NaN and Inf codes), p = +-0, and
+hyperparameters at the edges (eps = 0, where den may be 0; eps far below the
+root of the smallest normal; bc2 near 0, outside the Markstein range; lr = 0;
+early and late steps, where bc2 rounds to 1).
 """
 import numpy as np
 import pytest
