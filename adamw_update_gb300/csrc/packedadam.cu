@@ -858,9 +858,12 @@ struct BlockwiseArgs {
 
 // Staged blockwise kernel: one CTA per SM; a tile is kBwGroups consecutive
 // 2048-element blocks of one tensor, and consumer group j (8 warps, 256
-// threads) updates block j of a tile.
-constexpr int kBwGroups = kConsumerWarps / 8;  // 3
-constexpr int kBwTile = kBwGroups * kBlock;    // 6144 elements
+// threads) updates block j of a tile.  32 warps (64 registers each) ran 1.2 %
+// faster on GB300 than 24 warps with 80 registers.
+constexpr int kBwWarps = 32;
+constexpr int kBwThreads = kBwWarps * 32;
+constexpr int kBwGroups = kBwWarps / 8;      // 4
+constexpr int kBwTile = kBwGroups * kBlock;  // 8192 elements
 constexpr int kBwStages = 2;
 constexpr size_t kBwStageBytes = (size_t)kBwTile * (4 + 4 + 1 + 1);  // p, g, m_code, v_code
 
@@ -1116,7 +1119,7 @@ __device__ __forceinline__ bool codes_staged(const BlockwiseArgs &a)
 // Stage an item: write its slot and issue its bulk copies into stage
 // j % kBwStages (j: the CTA's item count).  Issued by thread 0 for the first
 // two items and afterwards by the consumer warp whose release completes a
-// stage, so the kernel needs no producer warp (24 warps, 80 registers each).
+// stage, so the kernel needs no producer warp.
 // `cur` is the shared table position: written by whichever thread issues,
 // possibly out of order, but every value written is the tensor of an item at
 // or before any later one, and the walk only moves forward from it.
@@ -1176,7 +1179,7 @@ __device__ __forceinline__ bool bw_release(uint32_t *count)
                  : "=r"(old)
                  : "r"(smem_addr(count))
                  : "memory");
-    if (old != (uint32_t)(kConsumerWarps - 1))
+    if (old != (uint32_t)(kBwWarps - 1))
         return false;
     *count = 0u;  // no release of this stage's next use precedes its refill
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -1258,13 +1261,13 @@ __device__ __forceinline__ void bw_consume(unsigned char *smem, uint64_t *full, 
     }
 }
 
-// The blockwise step over a tensor list (MULTI) or one tensor.  One CTA of 24
-// warps per SM: three groups of 8 warps update one block each of a tile of
+// The blockwise step over a tensor list (MULTI) or one tensor.  One CTA of 32
+// warps per SM: four groups of 8 warps update one block each of a tile of
 // kBwGroups blocks staged (p, g and, when both code arrays are 16-byte
 // aligned, the two code arrays) by bulk copies into a two-stage ring; the
 // warp whose release completes a stage issues the copies of its next item.
 template <bool MULTI>
-__global__ void __launch_bounds__(kConsumers, 1)
+__global__ void __launch_bounds__(kBwThreads, 1)
 blockwise8_pipe_kernel(const BwDesc *__restrict__ table, int32_t ntensors, int64_t total_items,
                        const BwDesc single, const float *__restrict__ qmap1,
                        const float *__restrict__ qmap2, const Scalars s,
@@ -1880,9 +1883,9 @@ pa_status pa_adamw_step_blockwise8(const float *p, const float *g, uint16_t *p_b
     const int64_t items = pa::bw_full_tiles(n) + (n % pa::kBlock != 0 ? 1 : 0);
     int grid = 0;
     if ((st = pipe_grid((const void *)pa::blockwise8_pipe_kernel<false>, pa::kBwSmemBytes, items,
-                        &grid, pa::kConsumers)) != PA_OK)
+                        &grid, pa::kBwThreads)) != PA_OK)
         return st;
-    pa::blockwise8_pipe_kernel<false><<<grid, pa::kConsumers, pa::kBwSmemBytes, (cudaStream_t)stream>>>(
+    pa::blockwise8_pipe_kernel<false><<<grid, pa::kBwThreads, pa::kBwSmemBytes, (cudaStream_t)stream>>>(
         nullptr, 1, items, d, qmap1, qmap2, s, nonfinite);
     return check_launch("blockwise8_pipe_kernel launch");
 }
@@ -2460,11 +2463,11 @@ extern "C" pa_status pa_adamw_step_blockwise8_multi(const pa_blockwise_tensor *l
         return st;
     int grid = 0;
     if ((st = pipe_grid((const void *)pa::blockwise8_pipe_kernel<true>, pa::kBwSmemBytes, items,
-                        &grid, pa::kConsumers)) != PA_OK)
+                        &grid, pa::kBwThreads)) != PA_OK)
         return st;
     pa::BwDesc none;
     std::memset(&none, 0, sizeof none);
-    pa::blockwise8_pipe_kernel<true><<<grid, pa::kConsumers, pa::kBwSmemBytes, (cudaStream_t)stream>>>(
+    pa::blockwise8_pipe_kernel<true><<<grid, pa::kBwThreads, pa::kBwSmemBytes, (cudaStream_t)stream>>>(
         table, ntensors, items, none, qmap1, qmap2, s, nonfinite);
     return check_launch("blockwise8_pipe_kernel (multi) launch");
 }
