@@ -67,3 +67,25 @@ def test_multi_bf16_gradient_list():
     for k in range(len(sizes)):
         assert_same_bits(host_f32(dps[k]), ps[k], f"p {k}")
         assert_same_bits(host_u32(dss[k]), sts[k], f"state {k}")
+
+
+@pytest.mark.parametrize("n", [7, 6149, 20_003])
+def test_one_tensor_bf16_gradient_list(n):
+    """A one-tensor list of the bfloat16-gradient call (passed by value, no
+    descriptor table) equals the oracle on the widened gradient."""
+    import torch
+
+    import adamw_update_gb300 as pa
+
+    rng = np.random.default_rng(n)
+    p = rng.normal(0, 0.02, n).astype(np.float32)
+    st = np.zeros(n, np.uint32)
+    dp, ds = dev(p), torch.zeros(n, dtype=torch.int32, device="cuda")
+    for t in (1, 2, 3):
+        gb, gf = _bf16(rng, n)
+        dg = torch.from_numpy(gb.view(np.int16)).cuda().view(torch.bfloat16)
+        pa.pa_adamw_step_packed_e4_multi_bf16g([(dp, dg, ds)], t, **HY)
+        p, st, _ = oracle.step_packed(p, gf, st, t, **HY)
+    torch.cuda.synchronize()
+    assert_same_bits(host_f32(dp), p, "p")
+    assert_same_bits(host_u32(ds), st, "state")

@@ -207,6 +207,45 @@ def test_multi_tensor_list_ragged(pa, mode):
 
 
 @pytest.mark.parametrize("mode", ["e4", "fp16", "fp32"])
+@pytest.mark.parametrize("n,off", [(1, 0), (6143, 1), (6145, 3), (3 * 6144 + 7, 2)])
+def test_one_tensor_list_with_a_new_gradient_buffer_every_step(pa, mode, n, off):
+    """A one-tensor list is passed by value (no descriptor table); each step
+    brings a gradient buffer at a new address, as a training loop that
+    reallocates its gradients does.  Equals the oracle bit for bit."""
+    import torch
+
+    rng = np.random.default_rng(n + off)
+    host = _tensors([n], rng, mode)[0]
+    views = []
+    for a in host:
+        dt = torch.int32 if a.dtype == np.uint32 else torch.float32
+        buf = torch.zeros(n + 8, dtype=dt, device="cuda")
+        views.append(buf[off:off + n])
+        views[-1].copy_(dev(a))
+    bad = torch.zeros(1, dtype=torch.int64, device="cuda")
+    fn = {"e4": pa.pa_adamw_step_packed_e4_multi, "fp16": pa.pa_adamw_step_packed_fp16_multi,
+          "fp32": pa.pa_adamw_step_fp32_multi}[mode]
+    keep = []
+    for t in range(1, 5):
+        g = rng.normal(0, 1e-3, n).astype(np.float32)
+        gbuf = torch.zeros(n + 8 + t, dtype=torch.float32, device="cuda")
+        dg = gbuf[off:off + n]
+        dg.copy_(dev(g))
+        keep.append(gbuf)  # every step's buffer at its own address
+        fn([(views[0], dg, *views[1:])], t, nonfinite=bad, **HY)
+        if mode == "fp32":
+            host[0], host[1], host[2], _ = oracle.step_fp32(host[0], g, host[1], host[2], t, **HY)
+        else:
+            host[0], host[1], _ = oracle.step_packed(host[0], g, host[1], t, mode=mode, **HY)
+    torch.cuda.synchronize()
+    assert_same_bits(host_f32(views[0]), host[0], "p")
+    for a, d in zip(host[1:], views[1:]):
+        got = host_u32(d) if a.dtype == np.uint32 else host_f32(d)
+        assert_same_bits(got, a, "state")
+    assert int(bad.item()) == 0
+
+
+@pytest.mark.parametrize("mode", ["e4", "fp16", "fp32"])
 def test_multi_tensor_list_longer_than_the_shared_table(pa, mode):
     """600 tensors (more than the 512 descriptors the staged kernel copies into
     shared memory, so the producer walks the table in global memory): sizes
