@@ -867,8 +867,15 @@ constexpr int kBwTile = kBwGroups * kBlock;  // 8192 elements
 constexpr int kBwStages = 2;
 constexpr size_t kBwStageBytes = (size_t)kBwTile * (4 + 4 + 1 + 1);  // p, g, m_code, v_code
 
+// The maps and midpoints are gathered at data-dependent indices; each is held
+// kMapCopies times, a copy kCopyShift banks over from the previous, and lane
+// l reads copy l % kMapCopies, so lanes whose indices share a bank mostly
+// read different banks.
+constexpr int kMapCopies = 4;
+constexpr int kCopyShift = 8;
 struct BlockwiseShared {
-    float q1[256], q2[256], mid1[512], mid2[512];  // midpoints padded with +Inf
+    float q1[kMapCopies][256 + kCopyShift], q2[kMapCopies][256 + kCopyShift];
+    float mid1[kMapCopies][512 + kCopyShift], mid2[kMapCopies][512 + kCopyShift];  // +Inf padded
     uint8_t bucket1[kBuckets], bucket2[kBuckets];
     uint32_t warp_max[kBwGroups][2][2][8];  // [group][block parity][m, v][warp of the group]
     uint32_t red[2][32];
@@ -953,7 +960,7 @@ __device__ __forceinline__ void blockwise_block(const BlockwiseArgs &a, Blockwis
                                                 const uint32_t mc[2], const uint32_t vc[2],
                                                 const Scalars &s, int k1, int k2, uint32_t &bad)
 {
-    const int lane = gt & 31, warp = gt >> 5;
+    const int lane = gt & 31, warp = gt >> 5, copy = lane % kMapCopies;
     const int64_t base = b * kBlock;
     const float am = a.m_absmax[b], av = a.v_absmax[b];
     float mn[8], vn[8];
@@ -964,8 +971,8 @@ __device__ __forceinline__ void blockwise_block(const BlockwiseArgs &a, Blockwis
         float po[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const float m = __fmul_rn(sh.q1[__byte_perm(mc[h], 0u, 0x4440u + j)], am);
-            const float v = __fmul_rn(sh.q2[__byte_perm(vc[h], 0u, 0x4440u + j)], av);
+            const float m = __fmul_rn(sh.q1[copy][__byte_perm(mc[h], 0u, 0x4440u + j)], am);
+            const float v = __fmul_rn(sh.q2[copy][__byte_perm(vc[h], 0u, 0x4440u + j)], av);
             const Moments o = adamw_element(pv[4 * h + j], gv[4 * h + j], m, v, s);
             po[j] = o.p;
             if (WHOLE || e0 + j < a.n) {
@@ -1012,22 +1019,22 @@ __device__ __forceinline__ void blockwise_block(const BlockwiseArgs &a, Blockwis
     const uint32_t smb = max(um, floor_bits), svb = max(uv, floor_bits);  // NaN bits stay NaN
     uint32_t mcode[2], vcode[2];
     if (scale_in_fast_range(smb)) {  // uniform over the group
-        const uint2 cm = requantise_fast<K>(mn, smb, sh.mid1, sh.bucket1, k1);
+        const uint2 cm = requantise_fast<K>(mn, smb, sh.mid1[copy], sh.bucket1, k1);
         mcode[0] = cm.x;
         mcode[1] = cm.y;
     } else {
         const uint2 cm = requantise_slow(mn[0], mn[1], mn[2], mn[3], mn[4], mn[5], mn[6], mn[7],
-                                         __uint_as_float(smb), sh.mid1);
+                                         __uint_as_float(smb), sh.mid1[copy]);
         mcode[0] = cm.x;
         mcode[1] = cm.y;
     }
     if (scale_in_fast_range(svb)) {
-        const uint2 cv = requantise_fast<K>(vn, svb, sh.mid2, sh.bucket2, k2);
+        const uint2 cv = requantise_fast<K>(vn, svb, sh.mid2[copy], sh.bucket2, k2);
         vcode[0] = cv.x;
         vcode[1] = cv.y;
     } else {
         const uint2 cv = requantise_slow(vn[0], vn[1], vn[2], vn[3], vn[4], vn[5], vn[6], vn[7],
-                                         __uint_as_float(svb), sh.mid2);
+                                         __uint_as_float(svb), sh.mid2[copy]);
         vcode[0] = cv.x;
         vcode[1] = cv.y;
     }
@@ -1056,19 +1063,25 @@ __device__ __forceinline__ void blockwise_setup(BlockwiseShared &sh, const float
 {
     const int tid = threadIdx.x;
     if (tid < 256) {
-        sh.q1[tid] = __ldg(qmap1 + tid);
-        sh.q2[tid] = __ldg(qmap2 + tid);
+        for (int c = 0; c < kMapCopies; ++c) {
+            sh.q1[c][tid] = __ldg(qmap1 + tid);
+            sh.q2[c][tid] = __ldg(qmap2 + tid);
+        }
     }
     __syncthreads();
     if (tid < 256) {
-        sh.mid1[tid] = tid < 255 ? __fmul_rn(__fadd_rn(sh.q1[tid], sh.q1[tid + 1]), 0.5f) : INFINITY;
-        sh.mid2[tid] = tid < 255 ? __fmul_rn(__fadd_rn(sh.q2[tid], sh.q2[tid + 1]), 0.5f) : INFINITY;
-        sh.mid1[256 + tid] = INFINITY;
-        sh.mid2[256 + tid] = INFINITY;
+        const float a = tid < 255 ? __fmul_rn(__fadd_rn(sh.q1[0][tid], sh.q1[0][tid + 1]), 0.5f) : INFINITY;
+        const float b = tid < 255 ? __fmul_rn(__fadd_rn(sh.q2[0][tid], sh.q2[0][tid + 1]), 0.5f) : INFINITY;
+        for (int c = 0; c < kMapCopies; ++c) {
+            sh.mid1[c][tid] = a;
+            sh.mid2[c][tid] = b;
+            sh.mid1[c][256 + tid] = INFINITY;
+            sh.mid2[c][256 + tid] = INFINITY;
+        }
     }
     __syncthreads();
-    k1 = build_buckets(sh.mid1, sh.bucket1, sh.red[0]);
-    k2 = build_buckets(sh.mid2, sh.bucket2, sh.red[1]);
+    k1 = build_buckets(sh.mid1[0], sh.bucket1, sh.red[0]);
+    k2 = build_buckets(sh.mid2[0], sh.bucket2, sh.red[1]);
     __syncthreads();
 }
 
