@@ -14,7 +14,8 @@
 // per SM, whose producer warp streams tiles of every input into a two-stage
 // shared-memory ring with bulk (TMA) copies and mbarriers, while 24 consumer
 // warps update the staged tiles and store the results straight to global
-// memory with streaming hints (adamw_step_pipe_kernel, blockwise8_pipe_kernel).
+// memory with streaming hints (adamw_step_pipe_kernel; blockwise8_pipe_kernel
+// has 32 warps and no producer: the last warp to hand a stage back refills it).
 // A multi-tensor list becomes one launch over a device-side descriptor table,
 // whose tile prefix sums let the producer walk from tensor to tensor without a
 // search; it hands each tile's geometry to the consumers with the tile.  The
