@@ -283,7 +283,7 @@ adamw_step_kernel(const Desc *__restrict__ table, int32_t ntensors, int64_t tota
                                          nonfinite);
 }
 
-// ---- the staged step (FP32 gradients) -----------------------------------------
+// ---- the staged step (FP32 or bfloat16 gradients) -----------------------------
 // One CTA per SM: a producer warp whose lane 0 streams tiles of p, g and the
 // state (p, g, m, v in the FP32 mode) into a two-stage shared-memory ring
 // with bulk (TMA) copies, and 24 consumer warps that update a staged tile
