@@ -83,6 +83,15 @@ def test_host_validation_without_gpu(lib):
     t = (lib.PaTensor * 2)(lib.PaTensor(0x1000, 0x2000, 0x3000, None, -5), lib.PaTensor())
     assert L.pa_adamw_step_packed_e4_multi(t, 2, 1, *hy, None, None) == 2
     assert b"tensor 0" in L.pa_last_error()
+    # a one-tensor list (passed by value, no table) is checked like any list
+    one = (lib.PaTensor * 1)(lib.PaTensor(0x1000, 0x2000, 0x3000, None, -5))
+    assert L.pa_adamw_step_packed_e4_multi(one, 1, 1, *hy, None, None) == 2
+    assert b"tensor 0" in L.pa_last_error()
+    one = (lib.PaTensor * 1)(lib.PaTensor(0x1002, 0x2000, 0x3000, None, 4))
+    assert L.pa_adamw_step_packed_e4_multi(one, 1, 1, *hy, None, None) == 3
+    assert L.pa_adamw_step_fp32_multi(one, 1, 1, *hy, None, None) == 1  # no v
+    one = (lib.PaTensor * 1)(lib.PaTensor(0x1000, 0x2000, 0x3000, None, 0))
+    assert L.pa_adamw_step_packed_fp16_multi(one, 1, 1, *hy, None, None) == 0  # empty: no-op
     al = ctypes.c_void_p(0x1000)
     assert L.pa_adamw_step_blockwise8(al, ctypes.c_void_p(0x1004), al, al, al, al, al, al, al,
                                       4, 1, *hy, None, None) == 3  # g not 16-byte aligned
