@@ -1,0 +1,77 @@
+"""Host-side logic of bench.py, on the CPU: the workload shapes it steps and
+the rule that reports ncu traffic only for the kernel code it was taken on."""
+import hashlib
+import importlib.util
+import json
+import os
+import shutil
+
+import pytest
+
+import workloads as wl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SOURCES = ("packedadam.cu", "codecs.cuh", "blockwise.cuh", "pipeline.cuh")
+
+
+@pytest.fixture(scope="module")
+def bench():
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def test_workload_shapes(bench):
+    """The configurations' tensor lists: 52 tensors of 9,677,312 parameters
+    (biases folded into their weights), GPT-2 small's 148 tensors of
+    124,439,808, one tensor each for the flat and blockwise workloads."""
+    g52 = bench.tensor_sizes("gpt-52")
+    assert len(g52) == 52 and sum(g52) == 9_677_312
+    assert g52[:2] == [3_096_576, 262_144]
+    assert g52[2:8] == [197_376, 65_792, 263_168, 262_400, 512, 512]
+    g2 = bench.tensor_sizes("gpt2-148")
+    assert len(g2) == 148 and sum(g2) == 124_439_808
+    assert bench.tensor_sizes("flat-7e9") == [7_000_000_000]
+    assert bench.tensor_sizes("single-4096") == [4096]
+    n = bench.tensor_sizes("blockwise-1e9")[0]
+    assert wl.blocks(n) == 488_282 and n - (wl.blocks(n) - 1) * 2048 == 512
+
+
+def _tree(tmp_path):
+    src = os.path.join(ROOT, "adamw_update_gb300", "csrc")
+    dst = tmp_path / "adamw_update_gb300" / "csrc"
+    dst.mkdir(parents=True)
+    for name in SOURCES:
+        shutil.copy(os.path.join(src, name), dst / name)
+    (tmp_path / "profiles").mkdir()
+    return dst
+
+
+def test_traffic_is_reported_only_for_the_captured_code(bench, tmp_path, monkeypatch):
+    dst = _tree(tmp_path)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.traffic_per_param("e4") is None  # no record
+    digest = hashlib.sha256(bench.kernel_code_digest_input().encode()).hexdigest()
+    record = {"e4": {"source_sha256": digest, "dram_bytes_per_param": 19.78}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(record))
+    assert bench.traffic_per_param("e4") == pytest.approx(19.78)
+    assert bench.traffic_per_param("fp32") is None  # no capture of that mode
+    cu = dst / "pipeline.cuh"
+    text = cu.read_text()
+    cu.write_text(text + "\n// a comment added after the capture\n\n")
+    assert bench.traffic_per_param("e4") == pytest.approx(19.78)  # comments do not count
+    cu.write_text(text.replace("2000000000ull", "1000000000ull", 1))
+    assert bench.traffic_per_param("e4") is None  # the code changed
+
+
+def test_committed_traffic_record_is_sane():
+    """Whatever code it was taken on, the committed record's traffic is close
+    to the algorithmic bytes of each mode (no re-reads)."""
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        rec = json.load(f)
+    algorithmic = {"e4": 20.0, "fp16": 20.0, "fp32": 28.0, "blockwise": 14.0 + 16 / 2048}
+    for mode, b in algorithmic.items():
+        got = rec[mode]["dram_bytes_per_param"]
+        assert 0.95 * b <= got <= 1.02 * b, (mode, got)
+        assert os.path.exists(os.path.join(ROOT, rec[mode]["capture"]))
