@@ -425,14 +425,32 @@ def host_available_bytes():
     return None
 
 
+def prefix_sample(arrays, mode, s):
+    """The first s elements of a host sample (s whole 2048-blocks, or all of it,
+    in the blockwise mode, whose absmax arrays are per block)."""
+    if mode == "blockwise":
+        nb = wl.blocks(s)
+        p, g, mc, ma, vc, va = arrays
+        return [p[:s], g[:s], mc[:s], ma[:nb], vc[:s], va[:nb]]
+    return [a[:s] for a in arrays]
+
+
 def cpu_baseline(w, seconds):
+    """The oracle on all host cores for `seconds`, then on one thread for a
+    quarter of that on a prefix of the same sample."""
     cores = host_cores()
     s = sample_size(w.mode, seconds / 4, cores, w.n)
     arrays, q = host_sample(w, s)
     rate, n, passes = oracle_sample_rate(arrays, w.mode, seconds, cores, q)
+    s1 = min(s, max(2048, int(rate / cores * seconds / 8) // 2048 * 2048))
+    rate1, n1, passes1 = oracle_sample_rate(prefix_sample(arrays, w.mode, s1), w.mode,
+                                            seconds / 4, 1, q)
     return {"value": rate, "unit": "params/s", "cores": cores, "kind": "oracle",
             "sample": f"first {n} parameters of the {w.name} workload, {passes} oracle "
-                      f"steps in {cores} host threads"}
+                      f"steps in {cores} host threads",
+            "single_thread": {"value": rate1, "unit": "params/s",
+                              "sample": f"first {n1} parameters, {passes1} oracle steps "
+                                        f"in 1 thread"}}
 
 
 # ---------------------------------------------------------------------------

@@ -75,3 +75,35 @@ def test_committed_traffic_record_is_sane():
         got = rec[mode]["dram_bytes_per_param"]
         assert 0.95 * b <= got <= 1.02 * b, (mode, got)
         assert os.path.exists(os.path.join(ROOT, rec[mode]["capture"]))
+
+
+@pytest.mark.parametrize("mode", ["e4", "fp32", "blockwise"])
+def test_cpu_baseline_times_all_cores_and_one_thread(bench, mode):
+    """The oracle arm of the bench line on a small host-resident workload."""
+    import numpy as np
+    import torch
+
+    class W:
+        pass
+
+    w = W()
+    w.name, w.mode, w.n = "gpt-52", mode, 1 << 16
+    rng = np.random.default_rng(0)
+    w.p = torch.from_numpy(rng.normal(0, 0.02, w.n).astype(np.float32))
+    w.g = torch.from_numpy(rng.normal(0, 1e-3, w.n).astype(np.float32))
+    if mode == "blockwise":
+        q1, q2 = wl.dynamic_qmap_signed(), wl.dynamic_qmap_unsigned()
+        nb = wl.blocks(w.n)
+        w.m_code = torch.full((w.n,), wl.nearest_zero_code(q1), dtype=torch.uint8)
+        w.v_code = torch.full((w.n,), wl.nearest_zero_code(q2), dtype=torch.uint8)
+        w.m_absmax = torch.zeros(nb)
+        w.v_absmax = torch.zeros(nb)
+        w.q1, w.q2 = torch.from_numpy(q1), torch.from_numpy(q2)
+    elif mode == "fp32":
+        w.s = [torch.zeros(w.n), torch.zeros(w.n)]
+    else:
+        w.s = [torch.zeros(w.n, dtype=torch.int32)]
+    cpu = bench.cpu_baseline(w, 0.2)
+    assert cpu["value"] > 0 and cpu["cores"] >= 1 and cpu["kind"] == "oracle"
+    one = cpu["single_thread"]
+    assert one["value"] > 0 and "1 thread" in one["sample"]
