@@ -178,11 +178,13 @@ pa_status pa_adamw_step_blockwise8_multi(const pa_blockwise_tensor *list, int32_
  *   g      float[n]
  *   state  uint32[n] (packed modes) or float m[n] (FP32 mode)
  *   state2 NULL (packed modes) or float v[n] (FP32 mode)
- * The library keeps a device copy of each distinct list it is given (its
- * descriptor table, allocated with cudaMalloc on first use of that list on
- * the current device and reused while the list is unchanged; at most 64 lists
- * are kept, the oldest is freed first).  pa_release_tables() frees them all;
- * it synchronises the device.
+ * The library keeps a device copy of each distinct list of two or more
+ * tensors it is given (its descriptor table, allocated with cudaMalloc on
+ * first use of that list on the current device and reused while the list is
+ * unchanged; at most 64 lists are kept, the oldest is freed first).
+ * pa_release_tables() frees them all; it synchronises the device.  A
+ * one-tensor list is passed by value in the launch, like the single-tensor
+ * calls: no table, no allocation, no copy, whatever its pointers.
  * ------------------------------------------------------------------------- */
 typedef struct pa_tensor {
     float *p;
