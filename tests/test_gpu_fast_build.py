@@ -13,8 +13,6 @@ of m' when the two terms nearly cancel.  When upd nearly cancels p*dk the
 difference is many ulps of the small result, so no bound in ulps of p' alone
 holds for this build.
 """
-import ctypes
-
 import numpy as np
 import pytest
 
