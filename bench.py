@@ -516,10 +516,11 @@ def run_ours(args):
     region_ms = first.elapsed_time(last)
     step_ms = statistics.mean(launch_ms) if flush is not None else region_ms / args.steps
     kernel_ms = statistics.mean(launch_ms)
-    t = torch.tensor([step_ms, kernel_ms], dtype=torch.float64, device=device)
+    median_ms = statistics.median(launch_ms)
+    t = torch.tensor([step_ms, kernel_ms, median_ms], dtype=torch.float64, device=device)
     if world > 1:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    step_ms, kernel_ms = float(t[0]), float(t[1])
+    step_ms, kernel_ms, median_ms = float(t[0]), float(t[1]), float(t[2])
 
     e2e = None
     if not args.no_e2e:
@@ -573,6 +574,7 @@ def run_ours(args):
                            else "adamw_step_table_kernel<0>" if args.graph
                            else KERNEL_NAME[w.mode]),
                 "kernel_ms": kernel_ms,
+                "kernel_ms_median": median_ms,
             },
             "cpu_baseline": cpu,
             "e2e": e2e,
