@@ -6,8 +6,10 @@ libpackedadam.so       the product library: every binary32 operation of the
                        update rounds once (no FMA contraction, IEEE division
                        and square root, subnormals kept), so its results are
                        bit-identical to a strict binary32 evaluation.
-libpackedadam_fast.so  the same source with PA_FAST_MATH: contractions and
-                       approximate divisions allowed (a tolerance build).
+libpackedadam_fast.so  the same source with PA_FAST_MATH: the decoupled-decay
+                       line p*(1-lr*wd) - upd is one FMA (a tolerance build:
+                       parameters within 2 ulp of the largest term, state
+                       words unchanged).
 
 Both are compiled in parallel with one -gencode (sm_103a) and linked against
 the static CUDA runtime; host code is built with -ffp-contract=off so the

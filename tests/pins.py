@@ -327,6 +327,96 @@ def check_fp32_matches_torch_adamw(orc):
         np.testing.assert_allclose(v, st["exp_avg_sq"].numpy(), rtol=2e-5, atol=1e-16)
 
 
+def _ieee_sqrt_f32(x):
+    """Correctly rounded binary32 square root of a float32 tensor (x >= 0),
+    checked: y is the root exactly when x lies between the squares of the
+    midpoints from y to its two binary32 neighbours, and both squares are
+    exact in binary64 (25-bit factors)."""
+    import torch
+
+    y = torch.sqrt(x.double()).float()
+    y32 = y.numpy()
+    xd, yd = x.double().numpy(), y32.astype(np.float64)
+    up = (np.nextafter(y32, np.float32(np.inf)).astype(np.float64) - yd) / 2
+    down = (yd - np.nextafter(y32, np.float32(0)).astype(np.float64)) / 2
+    pos = yd > 0
+    assert np.all((yd[pos] - down[pos]) ** 2 <= xd[pos]), "square root rounded up too far"
+    assert np.all(xd[pos] <= (yd[pos] + up[pos]) ** 2), "square root rounded down too far"
+    return y
+
+
+def _page_spec_fp32_step(p, g, m, v, step, lr, beta1, beta2, eps, wd):
+    """The FP32 update as KBench "quantized-optimizer-state" reference.py
+    (quantized_adamw_step) prints it: torch float32 tensors on the CPU meeting
+    Python floats, each operator one float32 rounding, evaluated left to right
+    as Python parses it -- so ((1-beta2)*g)*g, ((lr/bc1)*m_new)/denom and
+    (p*(1-lr*wd)) - upd.  The scalars (1-beta1, beta2**step, lr/bc1, 1-lr*wd)
+    are Python doubles, which torch rounds once to float32 when it meets the
+    tensors.
+
+    One exception: torch's CPU square root is not correctly rounded on every
+    machine (with AVX-512 it comes out one ulp low for about 0.6 % of binary32
+    inputs), while the page's float32 .sqrt() means the IEEE one.  So the root
+    is taken in float64 and rounded once to float32 -- the correctly rounded
+    binary32 root, since a binary64 result rounded to binary32 is never double
+    rounded for the square root of a binary32 operand (S. A. Figueroa, "When is
+    double rounding innocuous?", SIGNUM Newsletter 30(3), 1995) -- and each
+    root is checked against its exact bracket."""
+    import torch
+
+    p, g, m, v = (torch.from_numpy(np.array(a, np.float32)) for a in (p, g, m, v))
+    new_m = beta1 * m + (1.0 - beta1) * g
+    new_v = beta2 * v + (1.0 - beta2) * g * g
+    corr1 = 1.0 - beta1 ** step
+    corr2 = 1.0 - beta2 ** step
+    den = _ieee_sqrt_f32(new_v / corr2) + eps
+    step_size = lr / corr1
+    update = step_size * new_m / den
+    p_new = p * (1.0 - lr * wd) - update
+    return p_new.numpy(), new_m.numpy(), new_v.numpy()
+
+
+def _adversarial_elements(rng, n):
+    """p, g, m, v: typical Adam scales, plus exact zeros of either sign,
+    subnormals, huge and tiny magnitudes, and moments that nearly cancel the
+    new gradient term (a large share of each kind)."""
+    p = rng.normal(0, 0.02, n).astype(np.float32)
+    g = (rng.choice([-1.0, 1.0], n) * 10.0 ** rng.uniform(-12, 1, n)).astype(np.float32)
+    m = (rng.choice([-1.0, 1.0], n) * 10.0 ** rng.uniform(-12, 0, n)).astype(np.float32)
+    v = (10.0 ** rng.uniform(-30, 0, n)).astype(np.float32)
+    k = n // 10
+    g[:k] = np.where(rng.random(k) < 0.5, 0.0, -0.0)
+    m[k:2 * k] = np.where(rng.random(k) < 0.5, 0.0, -0.0)
+    v[k:2 * k] = 0.0
+    sub = np.float32(2.0 ** -126) * rng.random(k).astype(np.float32)
+    g[2 * k:3 * k] = sub * rng.choice([-1, 1], k)
+    m[3 * k:4 * k] = sub
+    v[4 * k:5 * k] = np.abs(sub)
+    p[5 * k:6 * k] = sub * 3
+    # first-moment cancellation: beta1*m close to -(1-beta1)*g
+    m[6 * k:7 * k] = (-g[6 * k:7 * k] / 9.0 * (1 + 1e-6 * rng.normal(size=k))).astype(np.float32)
+    # update about as large as the decayed parameter
+    p[7 * k:8 * k] = (np.sign(m[7 * k:8 * k]) * 1e-3).astype(np.float32)
+    return p, g, m, v
+
+
+def check_fp32_element_matches_page_spec(orc):
+    """The oracle's FP32 element is, bit for bit, the page's own update
+    expression evaluated in float32 (torch on the CPU), over typical and
+    adversarial inputs (zeros, subnormals, extreme magnitudes, cancellation)
+    at early steps and at late steps where 1 - beta2**step rounds to 1."""
+    rng = np.random.default_rng(31)
+    n = 40000
+    for hy in HYPER_SETS:
+        for step in (1, 2, 10, 1000, 20000, 10 ** 6):
+            p, g, m, v = _adversarial_elements(rng, n)
+            ep, em, ev = _page_spec_fp32_step(p, g, m, v, step, **hy)
+            op, om, ov, _ = orc.step_fp32(p, g, m, v, step, **hy)
+            assert_bits_equal(om, em, f"m' at step {step}")
+            assert_bits_equal(ov, ev, f"v' at step {step}")
+            assert_bits_equal(op, ep, f"p' at step {step}")
+
+
 def _random_state_words(rng, n, mode):
     if mode == "e4":
         m = rng.integers(0, 65536, n)
@@ -560,6 +650,7 @@ ALL_CHECKS = {
     "zero_gradient_decay_fp16": lambda o: check_zero_gradient_pure_decay(o, "fp16"),
     "zero_gradient_decay_fp32": lambda o: check_zero_gradient_pure_decay(o, "fp32"),
     "fp32_matches_torch_adamw": check_fp32_matches_torch_adamw,
+    "fp32_element_matches_page_spec": check_fp32_element_matches_page_spec,
     "packed_e4_is_fp32_on_decoded": lambda o: check_packed_is_fp32_step_on_decoded_state(o, "e4"),
     "packed_fp16_is_fp32_on_decoded":
         lambda o: check_packed_is_fp32_step_on_decoded_state(o, "fp16"),

@@ -86,6 +86,23 @@ MUTANTS = [
      ["blockwise_step_composition"]),
     ("bf16_truncates", "pick = (lo % 2u == 0u) ? lo : lo + 1u;", "pick = lo;",
      ["bf16_matches_torch"]),
+    # re-associations and contractions: the same algebra, other roundings
+    ("gradient_squared_first", "float t = h->c2 * g;\n    float t2 = t * g;",
+     "float t = g * g;\n    float t2 = h->c2 * t;", ["fp32_element_matches_page_spec"]),
+    ("step_size_after_division", "float u = h->ss * mn;\n    float upd = u / den;",
+     "float u = mn / den;\n    float upd = h->ss * u;", ["fp32_element_matches_page_spec"]),
+    ("root_of_each_factor", "float q = vn / h->bc2;\n    float s = sqrtf(q);",
+     "float q = sqrtf(vn);\n    float s = q / sqrtf(h->bc2);", ["fp32_element_matches_page_spec"]),
+    ("bc2_by_reciprocal", "float q = vn / h->bc2;", "float q = vn * (1.0f / h->bc2);",
+     ["fp32_element_matches_page_spec"]),
+    ("first_moment_contracted", "float mn = m1 + m2;", "float mn = fmaf(h->b1, m, m2);",
+     ["fp32_element_matches_page_spec"]),
+    ("decay_line_contracted", "*p_new = pd - upd;", "*p_new = fmaf(p, h->dk, -upd);",
+     ["fp32_element_matches_page_spec"]),
+    ("decay_after_update", "float pd = p * h->dk;\n    *p_new = pd - upd;",
+     "float pd = p - upd;\n    *p_new = pd * h->dk;", ["fp32_element_matches_page_spec"]),
+    ("one_minus_beta_in_float", "h.c1 = (float)(1.0 - beta1);", "h.c1 = 1.0f - (float)beta1;",
+     ["fp32_element_matches_page_spec"]),
 ]
 
 
