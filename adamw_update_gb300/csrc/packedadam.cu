@@ -1593,7 +1593,9 @@ pa_status step_single(const pa_tensor &t, int64_t step, double lr, double beta1,
 // A list is uploaded once per device and reused while it is unchanged, so a
 // training loop that steps the same tensors pays no host-to-device copy.  The
 // table of a list is immutable once uploaded, so calls on different streams
-// never see a table change under them.
+// never see a table change under them.  A table that the graph-replayable step
+// has used is pinned: a captured launch holds its address, so the
+// least-recently-used eviction never frees it (only pa_release_tables does).
 struct Table {
     int device;
     int mode;
@@ -1603,6 +1605,7 @@ struct Table {
     Desc *dev;
     int64_t chunks;
     uint64_t last_use;
+    bool pinned;
 };
 
 std::mutex g_tab_mu;
@@ -1611,7 +1614,8 @@ uint64_t g_tick = 0;
 constexpr size_t kMaxTables = 64;
 
 pa_status table_for(const pa_tensor *list, int32_t ntensors, int mode, int64_t chunk,
-                    const Desc **dev_table, int64_t *chunks, int grad_bytes = 4)
+                    const Desc **dev_table, int64_t *chunks, int grad_bytes = 4,
+                    bool pin = false)
 {
     std::vector<Desc> host((size_t)ntensors);
     int64_t total = 0;
@@ -1631,21 +1635,25 @@ pa_status table_for(const pa_tensor *list, int32_t ntensors, int mode, int64_t c
             t.host.size() == host.size() &&
             std::memcmp(t.host.data(), host.data(), host.size() * sizeof(Desc)) == 0) {
             t.last_use = g_tick;
+            t.pinned = t.pinned || pin;
             *dev_table = t.dev;
             *chunks = t.chunks;
             return PA_OK;
         }
     }
-    if (g_tables.size() >= kMaxTables) {  // free the least recently used list
-        size_t old = 0;
-        for (size_t k = 1; k < g_tables.size(); ++k)
-            if (g_tables[k].last_use < g_tables[old].last_use)
+    if (g_tables.size() >= kMaxTables) {  // free the least recently used unpinned list
+        size_t old = g_tables.size();
+        for (size_t k = 0; k < g_tables.size(); ++k)
+            if (!g_tables[k].pinned &&
+                (old == g_tables.size() || g_tables[k].last_use < g_tables[old].last_use))
                 old = k;
-        int cur = dev;
-        cudaSetDevice(g_tables[old].device);
-        cudaFree(g_tables[old].dev);  // synchronises that device: no kernel still reads it
-        cudaSetDevice(cur);
-        g_tables.erase(g_tables.begin() + (long)old);
+        if (old < g_tables.size()) {
+            int cur = dev;
+            cudaSetDevice(g_tables[old].device);
+            cudaFree(g_tables[old].dev);  // synchronises that device: no kernel still reads it
+            cudaSetDevice(cur);
+            g_tables.erase(g_tables.begin() + (long)old);
+        }
     }
     Table t;
     t.device = dev;
@@ -1654,6 +1662,7 @@ pa_status table_for(const pa_tensor *list, int32_t ntensors, int mode, int64_t c
     t.chunk = chunk;
     t.chunks = total;
     t.last_use = g_tick;
+    t.pinned = pin;
     t.dev = nullptr;
     const size_t bytes = host.size() * sizeof(Desc);
     e = cudaMalloc((void **)&t.dev, bytes);
@@ -1964,11 +1973,32 @@ constexpr int32_t kNoAllocMaxTensors = PA_NOALLOC_MAX_TENSORS;
 
 static __device__ __align__(256) pa::Desc g_noalloc_table[PA_NOALLOC_MAX_TENSORS];
 
+// The descriptors reach the array as kernel parameters, up to kNoAllocBatch per
+// launch (8 + 512 * 56 = 28,680 bytes, under the 32,764-byte parameter limit),
+// written by a small kernel on the caller's stream: the launch copies its
+// parameters when it is issued, so the host buffer is free again at once and
+// nothing waits for the stream (a copy from pageable host memory would).
+constexpr int kNoAllocBatch = 512;
+struct NoAllocBatch {
+    int32_t first;  // index of d[0] in the array
+    int32_t count;  // descriptors in d
+    pa::Desc d[kNoAllocBatch];
+};
+
+__global__ void noalloc_upload_kernel(const __grid_constant__ NoAllocBatch b)
+{
+    constexpr int kWords = sizeof(pa::Desc) / sizeof(uint64_t);
+    const uint64_t *src = reinterpret_cast<const uint64_t *>(b.d);
+    uint64_t *dst = reinterpret_cast<uint64_t *>(g_noalloc_table + b.first);
+    for (int i = threadIdx.x; i < b.count * kWords; i += blockDim.x)
+        dst[i] = src[i];
+}
+
 namespace {
 
 std::mutex g_noalloc_mu;
 pa::Desc *g_noalloc_ptr[64] = {nullptr};  // device address of the array, per device
-thread_local pa::Desc g_noalloc_host[PA_NOALLOC_MAX_TENSORS];
+thread_local NoAllocBatch g_noalloc_batch;
 
 // The array's name is only a host-side stand-in in host code; its device
 // address is looked up once per device, with that device current.
@@ -2023,20 +2053,24 @@ extern "C" pa_status pa_adamw_step_packed_e4_multi_noalloc(
     }
     if (total == 0)
         return ok();
-    for (int32_t i = 0; i < ntensors; ++i) {
-        const int64_t c = describe(list[i], pa::kE4, pa::kTile, &g_noalloc_host[i]);
-        g_noalloc_host[i].chunk0 = tiles;
-        tiles += c;
-    }
     pa::Desc *table = nullptr;
     if ((st = noalloc_table_address(&table)) != PA_OK)
         return st;
-    // The whole used prefix is rewritten, so nothing of an earlier call is read.
-    // A pageable-to-device async copy returns once the source has been staged.
-    cudaError_t e = cudaMemcpyAsync(table, g_noalloc_host, (size_t)ntensors * sizeof(pa::Desc),
-                                    cudaMemcpyHostToDevice, (cudaStream_t)stream);
-    if (e != cudaSuccess)
-        return cuda_fail(e, "descriptor upload to the fixed device array");
+    // The whole used prefix is rewritten, in batches of kNoAllocBatch, so
+    // nothing of an earlier call is read.
+    NoAllocBatch &b = g_noalloc_batch;
+    for (int32_t first = 0; first < ntensors; first += kNoAllocBatch) {
+        b.first = first;
+        b.count = ntensors - first < kNoAllocBatch ? ntensors - first : kNoAllocBatch;
+        for (int32_t k = 0; k < b.count; ++k) {
+            const int64_t c = describe(list[first + k], pa::kE4, pa::kTile, &b.d[k]);
+            b.d[k].chunk0 = tiles;
+            tiles += c;
+        }
+        noalloc_upload_kernel<<<1, 256, 0, (cudaStream_t)stream>>>(b);
+        if ((st = check_launch("descriptor upload to the fixed device array")) != PA_OK)
+            return st;
+    }
     const size_t smem = pa::PipeLayout<pa::kE4>::kBytes;  // the kernel's limit
     const size_t used = pa::PipeLayout<pa::kE4>::bytes_for(ntensors);
     const void *kern = s.bc2 == 1.0f ? (const void *)pa::adamw_step_pipe_kernel<pa::kE4, true>
@@ -2308,7 +2342,7 @@ extern "C" pa_status pa_adamw_step_packed_e4_multi_graph(const pa_tensor *list, 
     if (total > 0) {
         const Desc *table = nullptr;
         int64_t tiles = 0;
-        if ((st = table_for(list, ntensors, pa::kE4, pa::kTile, &table, &tiles)) != PA_OK)
+        if ((st = table_for(list, ntensors, pa::kE4, pa::kTile, &table, &tiles, 4, true)) != PA_OK)
             return st;
         const size_t smem = pa::PipeLayout<pa::kE4>::kBytes;  // the kernel's limit
         const size_t used = pa::PipeLayout<pa::kE4>::bytes_for(ntensors);

@@ -124,9 +124,33 @@ class PackedAdamW(torch.optim.Optimizer):
         return loss
 
 
+_PLAIN = (type(None), bool, int, float, str, bytes, torch.Tensor)
+
+
+def _check_plain(x, where="extra"):
+    """Checkpoints are read back with torch.load(weights_only=True), which
+    unpickles tensors and plain containers only; refuse anything else when
+    saving rather than writing a file that cannot be loaded."""
+    if isinstance(x, _PLAIN):
+        return
+    if isinstance(x, (list, tuple)):
+        for k, v in enumerate(x):
+            _check_plain(v, f"{where}[{k}]")
+        return
+    if isinstance(x, dict):
+        for k, v in x.items():
+            _check_plain(k, f"{where} key")
+            _check_plain(v, f"{where}[{k!r}]")
+        return
+    raise TypeError(f"{where}: {type(x).__name__} is not plain data (None, bool, int, float, "
+                    "str, bytes, tensors, and lists, tuples and dicts of them)")
+
+
 def save_checkpoint(path: str, params, optimizer: PackedAdamW, extra=None) -> None:
     """Write a latest-only checkpoint (parameters, optimizer state, global
-    step) atomically: a temporary file renamed over `path`."""
+    step) atomically: a temporary file renamed over `path`.  `extra` must be
+    plain data (see _check_plain): the loader unpickles nothing else."""
+    _check_plain(extra)
     blob = {"params": [p.detach().clone() for p in params],
             "optimizer": optimizer.state_dict(), "extra": extra}
     tmp = f"{path}.tmp.{os.getpid()}"
@@ -136,8 +160,10 @@ def save_checkpoint(path: str, params, optimizer: PackedAdamW, extra=None) -> No
 
 def load_checkpoint(path: str, params, optimizer: PackedAdamW):
     """Restore parameters and optimizer state written by save_checkpoint, bit
-    for bit; returns the `extra` object that was saved."""
-    blob = torch.load(path, map_location="cpu", weights_only=False)
+    for bit; returns the `extra` object that was saved.  The file is read with
+    torch.load(weights_only=True): tensors and plain containers only, so a file
+    holding any other pickled object is refused before anything is restored."""
+    blob = torch.load(path, map_location="cpu", weights_only=True)
     with torch.no_grad():
         for p, saved in zip(params, blob["params"]):
             p.copy_(saved)

@@ -24,6 +24,13 @@ N > 1 (torchrun): each rank steps its own shard of the same size on its own
 GPU (elements are independent, so no collective is on the data path); a
 barrier and a max-reduction of the timings are the only communication.
 
+The default line (flat-7e9, packed E4, N = 1) also carries `configs`: every
+workload of the benchmark measured the same way after the headline, each with
+its own buffers, warm-up, timed steps and oracle baseline -- single-4096 (10
+steps), gpt-52 packed E4 and FP32 (100 steps each), gpt2-148 packed E4 and FP16
+(50 steps each), flat-7e9 (the headline's numbers) and the 8-bit blockwise
+mode on 1e9 parameters (20 steps).
+
 --impl reference times the CPU oracle, as it stands, on this machine's cores on a
 bounded sample of the same workload (rank 0 only).
 """
@@ -70,6 +77,13 @@ def parse():
     ap.add_argument("--graph", action="store_true",
                     help="packed E4: capture the step (device-indexed scalar rows) in a CUDA "
                          "graph and time its replays")
+    ap.add_argument("--op", default="step", choices=["step", "encode", "decode"],
+                    help="encode/decode: time the standalone E4 state codecs (12 B/param) on "
+                         "the one-tensor workload instead of the step")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-configuration measurements (the `configs` object)")
+    ap.add_argument("--config-cpu-seconds", type=float, default=3.0,
+                    help="oracle seconds per configuration's cpu_baseline")
     ap.add_argument("--params", type=int, default=None,
                     help="override the parameter count of a one-tensor workload (flat-7e9, "
                          "blockwise-1e9): the same distributions at another size, for profiling")
@@ -457,6 +471,85 @@ def cpu_baseline(w, seconds):
 # Our arm
 # ---------------------------------------------------------------------------
 
+def time_launches(run, first_step, steps, flush, stream):
+    """CUDA events on the launching stream around each of `steps` launches
+    (steps first_step, first_step+1, ...), an L2 flush between launches when
+    `flush` is a buffer (outside the launch's events), and events around the
+    whole region.  Returns (per-launch ms, region ms)."""
+    import torch
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    first = torch.cuda.Event(enable_timing=True)
+    last = torch.cuda.Event(enable_timing=True)
+    first.record(stream)
+    for k in range(steps):
+        if flush is not None:
+            flush.fill_(float(k))
+        starts[k].record(stream)
+        run(first_step + k)
+        ends[k].record(stream)
+    last.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in zip(starts, ends)], first.elapsed_time(last)
+
+
+def l2_policy(w, flush):
+    return ("flushed between steps (512 MB write)" if flush is not None
+            else f"inputs larger than L2 ({w.bytes_per_step() / 1e9:.1f} GB per step)")
+
+
+def kernel_name(w, graph=False):
+    if w.grad_bf16:
+        return "adamw_step_pipe_kernel<0,bfloat16>"
+    return "adamw_step_table_kernel<0>" if graph else KERNEL_NAME[w.mode]
+
+
+def run_codec(lib, args, device):
+    """pa_encode_state or pa_decode_state over the one-tensor workload: m and
+    the RMS from the oracle-free seeded generators (m ~ N(0, 1e-3), RMS =
+    |N(0, 1e-3)|), words from encoding them; 12 bytes per parameter (read 8,
+    write 4 to encode; read 4, write 8 to decode)."""
+    import torch
+
+    if args.workload not in ("flat-7e9", "blockwise-1e9"):
+        raise SystemExit("--op encode/decode applies to the one-tensor workloads")
+    n = tensor_sizes(args.workload)[0]
+    m = wl.fill_normal_(torch.empty(n, dtype=torch.float32, device=device), 1e-3, 5)
+    r = wl.fill_normal_(torch.empty(n, dtype=torch.float32, device=device), 1e-3, 6).abs_()
+    w = torch.empty(n, dtype=torch.int32, device=device)
+    lib.pa_encode_state(m, r, w)
+    if args.op == "encode":
+        def run(t):
+            lib.pa_encode_state(m, r, w)
+    else:
+        def run(t):
+            lib.pa_decode_state(w, m, r)
+    stream = torch.cuda.current_stream()
+    for t in range(args.warmup):
+        run(t)
+    torch.cuda.synchronize()
+    launch_ms, _ = time_launches(run, 0, args.steps, None, stream)
+    kernel_ms = statistics.mean(launch_ms)
+    peak, peak_kind = measured_peak()
+    achieved = 12 * n / (kernel_ms / 1e3) / 1e9
+    name = "encode_state_kernel<0>" if args.op == "encode" else "decode_state_kernel<0>"
+    line = {"metric": f"E4 state {args.op}: params/s and HBM GB/s", "value": n / (kernel_ms / 1e3),
+            "unit": "params/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": kernel_ms, "higher_is_better": True, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": args.workload if args.params is None
+                       else f"{args.workload} at {n} params", "op": args.op,
+                       "bytes_per_param": 12,
+                       "l2": f"inputs larger than L2 ({12 * n / 1e9:.1f} GB per step)"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": peak_kind, "kernel": name,
+                         "kernel_ms": kernel_ms,
+                         "kernel_ms_median": statistics.median(launch_ms)},
+            "gpu_launches": args.steps}
+    print(json.dumps(line), flush=True)
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -469,6 +562,32 @@ def run_ours(args):
     if args.fast:
         os.environ["PA_LIBRARY_VARIANT"] = "fast"
     import adamw_update_gb300 as lib
+
+    if args.op != "step":
+        if world > 1:
+            raise SystemExit("--op encode/decode runs on one GPU")
+        run_codec(lib, args, device)
+        return
+    line = headline(lib, args, device, world, rank)
+    if rank == 0 and world == 1 and want_configs(args):
+        import gc
+
+        gc.collect()
+        torch.cuda.empty_cache()
+        line["configs"] = measure_configs(lib, args, device, line)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def headline(lib, args, device, world, rank):
+    """The bench line's workload: timed steps, roofline, e2e, cpu_baseline,
+    clocks.  Returns the line (rank 0) or None; every device buffer it made is
+    released when it returns."""
+    import torch
+    import torch.distributed as dist
+
     w = Workload(args.workload, args.mode, device, seed=1234 + rank)
     hy = wl.HYPER
     nonfinite = torch.zeros(1, dtype=torch.int64, device=device)
@@ -488,8 +607,6 @@ def run_ours(args):
     for t in range(1, args.warmup + 1):
         run(t)
     torch.cuda.synchronize()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     props = torch.cuda.get_device_properties(device)
     sampler = ClockSampler(getattr(props, "pci_bus_id", None) and
                            f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0")
@@ -498,22 +615,10 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    first = torch.cuda.Event(enable_timing=True)
-    last = torch.cuda.Event(enable_timing=True)
-    first.record(stream)
-    for k in range(args.steps):
-        if flush is not None:
-            flush.fill_(float(k))
-        starts[k].record(stream)
-        run(args.warmup + 1 + k)
-        ends[k].record(stream)
-    last.record(stream)
-    torch.cuda.synchronize()
+    launch_ms, region_ms = time_launches(run, args.warmup + 1, args.steps, flush, stream)
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
-    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    region_ms = first.elapsed_time(last)
     step_ms = statistics.mean(launch_ms) if flush is not None else region_ms / args.steps
     kernel_ms = statistics.mean(launch_ms)
     median_ms = statistics.median(launch_ms)
@@ -535,56 +640,124 @@ def run_ours(args):
     cpu = None
     if rank == 0 and world == 1:
         cpu = cpu_baseline(w, args.cpu_seconds)
+    if rank != 0:
+        return None
+    peak, peak_kind = measured_peak()
+    bpp = w.bytes_per_param()
+    achieved = bpp * w.n / (kernel_ms / 1e3) / 1e9
+    traffic = None if w.grad_bf16 else traffic_per_param(w.mode)
+    return {
+        "metric": "packed-E4 AdamW step: params/s and HBM GB/s as % of GB300 peak, 1 GPU"
+                  if w.mode == "e4" else f"{w.mode} AdamW step: params/s and HBM GB/s",
+        "value": w.n * world / (step_ms / 1e3),
+        "unit": "params/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": step_ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": w.name if args.params is None else f"{w.name} at {w.n} params",
+            "mode": w.mode, "params_per_gpu": w.n,
+            "tensors": len(w.sizes), "bytes_per_param": bpp,
+            "l2": l2_policy(w, flush),
+            "parallelism": f"{world} independent shards, no data-path collective",
+            "library": "libpackedadam_fast.so" if args.fast else "libpackedadam.so",
+            "grad": args.grad,
+            "launch": "CUDA graph replay" if args.graph else "C-ABI call per step",
+        },
+        "roofline": {
+            "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "peak_source": peak_kind,
+            "traffic": None if traffic is None else traffic * w.n,
+            "kernel": kernel_name(w, args.graph),
+            "kernel_ms": kernel_ms,
+            "kernel_ms_median": median_ms,
+        },
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps * (2 if args.graph else 1),
+        "clocks": clocks,
+        "nonfinite": int(nonfinite.item()),
+    }
 
-    if rank == 0:
-        peak, peak_kind = measured_peak()
-        bpp = w.bytes_per_param()
-        achieved = bpp * w.n / (kernel_ms / 1e3) / 1e9
-        traffic = None if w.grad_bf16 else traffic_per_param(w.mode)
-        line = {
-            "metric": "packed-E4 AdamW step: params/s and HBM GB/s as % of GB300 peak, 1 GPU"
-                      if w.mode == "e4" else f"{w.mode} AdamW step: params/s and HBM GB/s",
-            "value": w.n * world / (step_ms / 1e3),
-            "unit": "params/s",
-            "n_gpus": world,
-            "steps": args.steps,
-            "warmup": args.warmup,
-            "ms_per_step": step_ms,
-            "higher_is_better": True,
-            "scaling": "weak",
-            "vs_baseline": None,
-            "dtype": "f32",
-            "data": "synthetic",
-            "config": {
-                "workload": w.name if args.params is None else f"{w.name} at {w.n} params",
-                "mode": w.mode, "params_per_gpu": w.n,
-                "tensors": len(w.sizes), "bytes_per_param": bpp,
-                "l2": "flushed between steps (512 MB write)" if flush is not None
-                      else f"inputs larger than L2 ({w.bytes_per_step() / 1e9:.1f} GB per step)",
-                "parallelism": f"{world} independent shards, no data-path collective",
-                "library": "libpackedadam_fast.so" if args.fast else "libpackedadam.so",
-                "grad": args.grad,
-                "launch": "CUDA graph replay" if args.graph else "C-ABI call per step",
-            },
-            "roofline": {
-                "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "peak_source": peak_kind,
-                "traffic": None if traffic is None else traffic * w.n,
-                "kernel": ("adamw_step_pipe_kernel<0,bfloat16>" if args.grad == "bf16"
-                           else "adamw_step_table_kernel<0>" if args.graph
-                           else KERNEL_NAME[w.mode]),
-                "kernel_ms": kernel_ms,
-                "kernel_ms_median": median_ms,
-            },
-            "cpu_baseline": cpu,
-            "e2e": e2e,
-            "gpu_launches": args.steps * (2 if args.graph else 1),
-            "clocks": clocks,
-            "nonfinite": int(nonfinite.item()),
-        }
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
+
+# The five workloads of the benchmark, each measured on its own after the
+# headline (flat-7e9 is the headline itself): (workload, mode, timed steps).
+CONFIGS = [
+    ("single-4096", "e4", 10),
+    ("gpt-52", "e4", 100),
+    ("gpt-52", "fp32", 100),
+    ("gpt2-148", "e4", 50),
+    ("gpt2-148", "fp16", 50),
+    ("flat-7e9", "e4", None),
+    ("blockwise-1e9", "blockwise", 20),
+]
+
+
+def want_configs(args):
+    return not (args.no_configs or args.params is not None or args.graph or args.fast
+                or args.grad != "fp32" or args.workload != "flat-7e9" or args.mode != "e4"
+                or args.op != "step")
+
+
+def measure_configs(lib, args, device, head):
+    """Every workload of CONFIGS, one after the other, each with its own device
+    buffers (released before the next), 3 warm-up steps, CUDA events around
+    each timed launch, an L2 flush between launches when its bytes per step
+    are under 4x the L2, and the oracle on a bounded sample of it."""
+    out = {}
+    for name, mode, steps in CONFIGS:
+        key = f"{name}/{mode}"
+        if steps is None:  # the headline's own numbers
+            r = head["roofline"]
+            out[key] = {"workload": name, "mode": mode, "params": head["config"]["params_per_gpu"],
+                        "tensors": head["config"]["tensors"], "steps": head["steps"],
+                        "warmup": head["warmup"], "us_per_step": head["ms_per_step"] * 1e3,
+                        "params_per_s": head["value"], "gb_s": r["achieved"], "frac": r["frac"],
+                        "kernel": r["kernel"], "kernel_ms": r["kernel_ms"],
+                        "kernel_ms_median": r["kernel_ms_median"], "l2": head["config"]["l2"],
+                        "cpu_baseline": head["cpu_baseline"], "measured": "the headline"}
+            continue
+        out[key] = measure_config(lib, name, mode, steps, max(3, args.warmup), device,
+                                  args.config_cpu_seconds)
+    return out
+
+
+def measure_config(lib, name, mode, steps, warmup, device, cpu_seconds):
+    import torch
+
+    w = Workload(name, mode, device, seed=1234)
+    nonfinite = torch.zeros(1, dtype=torch.int64, device=device)
+    run = step_fn(lib, w, wl.HYPER, nonfinite)
+    stream = torch.cuda.current_stream()
+    flush = None
+    if w.bytes_per_step() < 4 * L2_BYTES:
+        flush = torch.empty(512 * 2 ** 20 // 4, dtype=torch.float32, device=device)
+    for t in range(1, warmup + 1):
+        run(t)
+    torch.cuda.synchronize()
+    launch_ms, region_ms = time_launches(run, warmup + 1, steps, flush, stream)
+    kernel_ms = statistics.mean(launch_ms)
+    step_ms = kernel_ms if flush is not None else region_ms / steps
+    peak, peak_kind = measured_peak()
+    bpp = w.bytes_per_param()
+    gbs = bpp * w.n / (kernel_ms / 1e3) / 1e9
+    entry = {"workload": name, "mode": w.mode, "params": w.n, "tensors": len(w.sizes),
+             "steps": steps, "warmup": warmup, "bytes_per_param": bpp,
+             "us_per_step": step_ms * 1e3, "params_per_s": w.n / (step_ms / 1e3),
+             "gb_s": gbs, "frac": gbs / peak, "peak_source": peak_kind,
+             "kernel": kernel_name(w), "kernel_ms": kernel_ms,
+             "kernel_ms_median": statistics.median(launch_ms), "l2": l2_policy(w, flush),
+             "gpu_launches": steps, "nonfinite": int(nonfinite.item())}
+    if name == "single-4096":
+        entry["note"] = "launch-latency bound: the fraction of peak is not meaningful here"
+    entry["cpu_baseline"] = cpu_baseline(w, cpu_seconds)
+    return entry
 
 
 def measure_e2e(pa, w, hy, args, stream, nonfinite):

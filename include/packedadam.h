@@ -181,7 +181,9 @@ pa_status pa_adamw_step_blockwise8_multi(const pa_blockwise_tensor *list, int32_
  * The library keeps a device copy of each distinct list of two or more
  * tensors it is given (its descriptor table, allocated with cudaMalloc on
  * first use of that list on the current device and reused while the list is
- * unchanged; at most 64 lists are kept, the oldest is freed first).
+ * unchanged; at most 64 lists are kept, the least recently used is freed
+ * first, except the lists of pa_adamw_step_packed_e4_multi_graph below, which
+ * are kept until pa_release_tables).
  * pa_release_tables() frees them all; it synchronises the device.  A
  * one-tensor list is passed by value in the launch, like the single-tensor
  * calls: no table, no allocation, no copy, whatever its pointers.
@@ -216,10 +218,13 @@ pa_status pa_adamw_step_fp32_multi(const pa_tensor *list, int32_t ntensors, int6
  * this entry point is an addition of this library.
  *
  * It calls no cudaMalloc, cudaFree or other allocating routine.  The list's
- * descriptor table is copied (cudaMemcpyAsync on `stream`) into a fixed device
- * array compiled into the library: PA_NOALLOC_MAX_TENSORS = 1024 descriptors
- * of 56 bytes, which every device that loads the library holds until the
- * process exits.  ntensors > 1024 returns PA_ERR_ARG.
+ * descriptor table goes into a fixed device array compiled into the library:
+ * PA_NOALLOC_MAX_TENSORS = 1024 descriptors of 56 bytes, which every device
+ * that loads the library holds until the process exits.  ntensors > 1024
+ * returns PA_ERR_ARG.  The descriptors travel as the launch parameters of a
+ * small kernel on `stream` (up to 512 per launch) that writes them into the
+ * array ahead of the step kernel, so the call neither copies from host memory
+ * nor waits for work already queued on `stream`.
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current); make that first call
  * before any stream capture.  All calls share the array and each rewrites the
@@ -302,8 +307,13 @@ pa_status pa_adamw_step_packed_e4_multi_bf16g(const pa_tensor *list, int32_t nte
  *   is updated and *status (device int32, nullable) is set to 1; the index
  *   still advances.  The list's descriptor table is made on the first call
  *   with that list (a cudaMalloc); make that first call before capturing, so a
- *   captured call finds it.  Results equal pa_adamw_step_packed_e4_multi at the
- *   same step and hyperparameters, bit for bit.
+ *   captured call finds it.  A captured launch holds that table's address, so
+ *   the library keeps the table of every list given to this call, whatever
+ *   other lists it sees later, until pa_release_tables or pa_shutdown, which
+ *   free it: replaying a graph captured before either of them reads freed
+ *   memory, so capture it again after them.  Results equal
+ *   pa_adamw_step_packed_e4_multi at the same step and hyperparameters, bit
+ *   for bit.
  * ------------------------------------------------------------------------- */
 typedef struct pa_hyper {
     float b1, b2, c1, c2, bc2, ss, dk, ef;

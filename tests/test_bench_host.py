@@ -107,3 +107,32 @@ def test_cpu_baseline_times_all_cores_and_one_thread(bench, mode):
     assert cpu["value"] > 0 and cpu["cores"] >= 1 and cpu["kind"] == "oracle"
     one = cpu["single_thread"]
     assert one["value"] > 0 and "1 thread" in one["sample"]
+
+
+def test_configs_cover_every_benchmark_workload(bench):
+    """The `configs` object of the default bench line measures all five
+    workloads: single-4096 (10 steps), gpt-52 packed E4 and FP32 (100 steps
+    each), gpt2-148 packed E4 and FP16 (50 steps each), flat-7e9 (the headline
+    itself) and the 8-bit blockwise mode on 1e9 parameters."""
+    got = {(name, mode): steps for name, mode, steps in bench.CONFIGS}
+    assert got == {("single-4096", "e4"): 10, ("gpt-52", "e4"): 100, ("gpt-52", "fp32"): 100,
+                   ("gpt2-148", "e4"): 50, ("gpt2-148", "fp16"): 50, ("flat-7e9", "e4"): None,
+                   ("blockwise-1e9", "blockwise"): 20}
+    assert {name for name, _, _ in bench.CONFIGS} == set(wl.WORKLOADS)
+
+
+def test_configs_only_on_the_default_headline(bench):
+    """The per-configuration measurements ride only on the default bench line
+    (flat-7e9, packed E4, the product library, a C-ABI call per step)."""
+    import sys
+
+    argv = sys.argv
+    try:
+        sys.argv = ["bench.py"]
+        assert bench.want_configs(bench.parse())
+        for extra in (["--no-configs"], ["--params", "1024"], ["--graph"], ["--fast"],
+                      ["--grad", "bf16"], ["--workload", "gpt-52"], ["--mode", "fp32"]):
+            sys.argv = ["bench.py", *extra]
+            assert not bench.want_configs(bench.parse()), extra
+    finally:
+        sys.argv = argv

@@ -98,3 +98,49 @@ def test_index_past_the_table_changes_nothing():
     assert int(status.item()) == 1 and int(index.item()) == 3
     for a, b, s in zip(dp, before, ds):
         assert torch.equal(a, b) and not s.any()
+
+
+def test_captured_graph_survives_many_other_lists():
+    """A captured launch holds its list's descriptor table: stepping more other
+    lists than the table cache keeps (64) between replays must not free it, so
+    later replays still step the captured tensors, bit for bit as the oracle."""
+    import torch
+
+    import adamw_update_gb300 as pa
+
+    ps, gs, dp, dg, ds = _setup(4)
+    entries = pa.tensor_list(list(zip(dp, dg, ds)))
+    rows = torch.empty(8 * 8, dtype=torch.float32, device="cuda")
+    pa.pa_hyper_table_fill(rows, 1, 8, **HY)
+    index = torch.zeros(1, dtype=torch.int64, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        pa.pa_adamw_step_packed_e4_multi_graph(entries, rows, 8, index, status)
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        pa.pa_adamw_step_packed_e4_multi_graph(entries, rows, 8, index, status)
+    graph.replay()
+    # 70 other two-tensor lists, each a distinct table
+    others = []
+    for k in range(70):
+        a = [torch.zeros(64 + k, device="cuda") for _ in range(2)]
+        b = [torch.zeros(64 + k, device="cuda") for _ in range(2)]
+        c = [torch.zeros(64 + k, dtype=torch.int32, device="cuda") for _ in range(2)]
+        others.append((a, b, c))
+        pa.pa_adamw_step_packed_e4_multi(list(zip(a, b, c)), 1, **HY)
+    torch.cuda.synchronize()
+    graph.replay()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert int(index.item()) == 4 and int(status.item()) == 0
+    hp = [p.copy() for p in ps]
+    hs = [np.zeros(n, np.uint32) for n in SIZES]
+    for t in range(1, 5):
+        for k in range(len(SIZES)):
+            hp[k], hs[k], _ = oracle.step_packed(hp[k], gs[k], hs[k], t, **HY)
+    for k in range(len(SIZES)):
+        assert np.array_equal(dp[k].cpu().numpy().view(np.uint32), hp[k].view(np.uint32))
+        assert np.array_equal(ds[k].cpu().numpy().view(np.uint32), hs[k])
