@@ -116,6 +116,44 @@ __device__ __forceinline__ uint32_t packed_element(float &p, float g, uint32_t w
     return MODE == kE4 ? encode_step_word_e4(o.m, o.v, rn) : encode_word_fp16(o.m, rn);
 }
 
+// Two elements of packed_element (lanes x and y) with packed arithmetic: the
+// exact rebias multiplies of the E4 decode, v = r*r and the update's multiplies
+// and adds are one instruction per pair (adamw_element2); same bits.
+__device__ __forceinline__ float2 decode_m_pair(uint32_t w0, uint32_t w1)
+{
+    const uint32_t b0 = ((w0 & 0x7FFFu) << 12) | ((w0 & 0x8000u) << 16);
+    const uint32_t b1 = ((w1 & 0x7FFFu) << 12) | ((w1 & 0x8000u) << 16);
+    return mul2(make_float2(__uint_as_float(b0), __uint_as_float(b1)), make_float2(0x1p112f, 0x1p112f));
+}
+
+__device__ __forceinline__ float2 decode_rms_pair(uint32_t w0, uint32_t w1)
+{
+    const uint32_t b0 = (w0 >> 5) & 0x07FFF800u, b1 = (w1 >> 5) & 0x07FFF800u;
+    return mul2(make_float2(__uint_as_float(b0), __uint_as_float(b1)), make_float2(0x1p112f, 0x1p112f));
+}
+
+template <int MODE, bool UNIT_BC2, bool ZS = false>
+__device__ __forceinline__ uint2 packed_element2(float2 &p, float2 g, uint32_t w0, uint32_t w1,
+                                                 const Scalars &s, const Pairs &k, uint32_t &bad,
+                                                 const ZeroSafe *zs = nullptr)
+{
+    const float2 m = MODE == kE4 ? decode_m_pair(w0, w1)
+                                 : make_float2(decode_fp16_low(w0), decode_fp16_low(w1));
+    const float2 r = MODE == kE4 ? decode_rms_pair(w0, w1)
+                                 : make_float2(decode_fp16_high(w0), decode_fp16_high(w1));
+    float2 rn = make_float2(0.0f, 0.0f);
+    const Moments2 o = adamw_element2<UNIT_BC2, ZS>(p, g, m, mul2(r, r), s, k, &rn, zs);
+    bad += any_nonfinite(Moments{o.p.x, o.m.x, o.v.x}) + any_nonfinite(Moments{o.p.y, o.m.y, o.v.y});
+    p = o.p;
+    if (!UNIT_BC2) {  // bc2 == 1: the update took sqrt(v')
+        rn.x = ZS ? sqrt_zero_safe(o.v.x) : __fsqrt_rn(o.v.x);
+        rn.y = ZS ? sqrt_zero_safe(o.v.y) : __fsqrt_rn(o.v.y);
+    }
+    return MODE == kE4 ? make_uint2(encode_step_word_e4(o.m.x, o.v.x, rn.x),
+                                    encode_step_word_e4(o.m.y, o.v.y, rn.y))
+                       : make_uint2(encode_word_fp16(o.m.x, rn.x), encode_word_fp16(o.m.y, rn.y));
+}
+
 // Element i of tensor d with 4-byte accesses (heads, tails, unaligned tensors).
 template <int MODE, bool U1, typename GT = float>
 __device__ __forceinline__ void scalar_element(const Desc &d, int64_t i, const Scalars &s,
@@ -377,11 +415,11 @@ struct Span {
     int32_t len, staged;
 };
 
-__device__ __forceinline__ Span tile_span(const Desc &d, int64_t k, int unit)
+__device__ __forceinline__ Span tile_span(const Desc &d, int64_t k, int unit, int32_t tile)
 {
-    const int64_t b = k * kTile;
+    const int64_t b = k * tile;
     int64_t len = (d.vec ? d.n - d.head : d.n) - b;
-    len = len < 0 ? 0 : (len > kTile ? kTile : len);
+    len = len < 0 ? 0 : (len > tile ? tile : len);
     Span sp;
     sp.base = d.vec ? d.head + b : b;
     sp.len = (int32_t)len;
@@ -411,7 +449,8 @@ struct TableCursor {
 
 template <int MODE, typename GT>
 __device__ __forceinline__ void pipe_produce(unsigned char *smem, uint64_t *full, uint64_t *empty,
-                                             const Desc *table, int32_t ntensors, int64_t total)
+                                             const Desc *table, int32_t ntensors, int64_t total,
+                                             int32_t tile)
 {
     using L = PipeLayout<MODE, GT>;
     TileInfo *info = reinterpret_cast<TileInfo *>(smem + L::kInfo);
@@ -426,7 +465,7 @@ __device__ __forceinline__ void pipe_produce(unsigned char *smem, uint64_t *full
             break;
         }
         const int64_t kt = c - cur.d.chunk0;
-        const Span sp = tile_span(cur.d, kt, L::kUnit);
+        const Span sp = tile_span(cur.d, kt, L::kUnit, tile);
         TileInfo &ti = info[st];
         ti.p = cur.d.p;
         ti.g = cur.d.g;
@@ -468,28 +507,42 @@ __device__ __forceinline__ void pipe_vector_math(const unsigned char *buf, int e
                                                  uint32_t &bad)
 {
     using L = PipeLayout<MODE, GT>;
+    const Pairs k = pairs_of(s);
     if constexpr (MODE == kF32) {
         const float4 mv = *reinterpret_cast<const float4 *>(buf + L::kS1 + 4 * e);
         const float4 vv = *reinterpret_cast<const float4 *>(buf + L::kS2 + 4 * e);
         float mm[4] = {mv.x, mv.y, mv.z, mv.w};
         float vq[4] = {vv.x, vv.y, vv.z, vv.w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const Moments o = adamw_element<U1, ZS>(pp[j], gg[j], mm[j], vq[j], s, nullptr, &zs);
-            bad += any_nonfinite(o);
-            pp[j] = o.p;
-            mm[j] = o.m;
-            vq[j] = o.v;
+        for (int j = 0; j < 4; j += 2) {
+            const Moments2 o = adamw_element2<U1, ZS>(make_float2(pp[j], pp[j + 1]),
+                                                      make_float2(gg[j], gg[j + 1]),
+                                                      make_float2(mm[j], mm[j + 1]),
+                                                      make_float2(vq[j], vq[j + 1]), s, k, nullptr,
+                                                      &zs);
+            bad += any_nonfinite(Moments{o.p.x, o.m.x, o.v.x}) +
+                   any_nonfinite(Moments{o.p.y, o.m.y, o.v.y});
+            pp[j] = o.p.x;
+            pp[j + 1] = o.p.y;
+            mm[j] = o.m.x;
+            mm[j + 1] = o.m.y;
+            vq[j] = o.v.x;
+            vq[j + 1] = o.v.y;
         }
         store_stream(static_cast<float *>(d.s1) + base + e, make_float4(mm[0], mm[1], mm[2], mm[3]));
         store_stream(static_cast<float *>(d.s2) + base + e, make_float4(vq[0], vq[1], vq[2], vq[3]));
     } else {
         const uint4 wv = *reinterpret_cast<const uint4 *>(buf + L::kS1 + 4 * e);
-        uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            ww[j] = packed_element<MODE, U1, ZS>(pp[j], gg[j], ww[j], s, bad, &zs);
-        store_stream(static_cast<uint32_t *>(d.s1) + base + e, make_uint4(ww[0], ww[1], ww[2], ww[3]));
+        float2 p01 = make_float2(pp[0], pp[1]), p23 = make_float2(pp[2], pp[3]);
+        const uint2 w01 = packed_element2<MODE, U1, ZS>(p01, make_float2(gg[0], gg[1]), wv.x, wv.y,
+                                                        s, k, bad, &zs);
+        const uint2 w23 = packed_element2<MODE, U1, ZS>(p23, make_float2(gg[2], gg[3]), wv.z, wv.w,
+                                                        s, k, bad, &zs);
+        pp[0] = p01.x;
+        pp[1] = p01.y;
+        pp[2] = p23.x;
+        pp[3] = p23.y;
+        store_stream(static_cast<uint32_t *>(d.s1) + base + e, make_uint4(w01.x, w01.y, w23.x, w23.y));
     }
 }
 
@@ -535,29 +588,26 @@ template <int MODE, bool U1>
 __device__ __forceinline__ void compute_vec(const RegVec<MODE> &r, int e, const Desc &d,
                                             int64_t base, const Scalars &s, uint32_t &bad)
 {
-    float pp[4] = {r.p.x, r.p.y, r.p.z, r.p.w};
-    const float gg[4] = {r.g.x, r.g.y, r.g.z, r.g.w};
+    const Pairs k = pairs_of(s);
+    float2 p01 = make_float2(r.p.x, r.p.y), p23 = make_float2(r.p.z, r.p.w);
+    const float2 g01 = make_float2(r.g.x, r.g.y), g23 = make_float2(r.g.z, r.g.w);
     if constexpr (MODE == kF32) {
-        float mm[4] = {r.m.x, r.m.y, r.m.z, r.m.w};
-        float vq[4] = {r.v.x, r.v.y, r.v.z, r.v.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const Moments o = adamw_element<U1>(pp[j], gg[j], mm[j], vq[j], s);
-            bad += any_nonfinite(o);
-            pp[j] = o.p;
-            mm[j] = o.m;
-            vq[j] = o.v;
-        }
-        store_stream(static_cast<float *>(d.s1) + base + e, make_float4(mm[0], mm[1], mm[2], mm[3]));
-        store_stream(static_cast<float *>(d.s2) + base + e, make_float4(vq[0], vq[1], vq[2], vq[3]));
+        const Moments2 a = adamw_element2<U1>(p01, g01, make_float2(r.m.x, r.m.y),
+                                              make_float2(r.v.x, r.v.y), s, k);
+        const Moments2 b = adamw_element2<U1>(p23, g23, make_float2(r.m.z, r.m.w),
+                                              make_float2(r.v.z, r.v.w), s, k);
+        bad += any_nonfinite(Moments{a.p.x, a.m.x, a.v.x}) + any_nonfinite(Moments{a.p.y, a.m.y, a.v.y}) +
+               any_nonfinite(Moments{b.p.x, b.m.x, b.v.x}) + any_nonfinite(Moments{b.p.y, b.m.y, b.v.y});
+        p01 = a.p;
+        p23 = b.p;
+        store_stream(static_cast<float *>(d.s1) + base + e, make_float4(a.m.x, a.m.y, b.m.x, b.m.y));
+        store_stream(static_cast<float *>(d.s2) + base + e, make_float4(a.v.x, a.v.y, b.v.x, b.v.y));
     } else {
-        uint32_t ww[4] = {r.w.x, r.w.y, r.w.z, r.w.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            ww[j] = packed_element<MODE, U1>(pp[j], gg[j], ww[j], s, bad);
-        store_stream(static_cast<uint32_t *>(d.s1) + base + e, make_uint4(ww[0], ww[1], ww[2], ww[3]));
+        const uint2 w01 = packed_element2<MODE, U1>(p01, g01, r.w.x, r.w.y, s, k, bad);
+        const uint2 w23 = packed_element2<MODE, U1>(p23, g23, r.w.z, r.w.w, s, k, bad);
+        store_stream(static_cast<uint32_t *>(d.s1) + base + e, make_uint4(w01.x, w01.y, w23.x, w23.y));
     }
-    store_stream(d.p + base + e, make_float4(pp[0], pp[1], pp[2], pp[3]));
+    store_stream(d.p + base + e, make_float4(p01.x, p01.y, p23.x, p23.y));
 }
 
 __device__ __forceinline__ bool has_zero(const float4 g)
@@ -692,11 +742,13 @@ __device__ __forceinline__ void pipe_consume(const unsigned char *smem, uint64_t
     }
 }
 
-// table == nullptr: one tensor, described by `single` (ntensors == 1).
+// table == nullptr: one tensor, described by `single` (ntensors == 1).  `tile`:
+// elements per tile (kTile, or fewer for a launch too small to fill the GPU).
 template <int MODE, bool U1, typename GT = float>
 __device__ __forceinline__ void pipe_body(const Desc *__restrict__ table, int32_t ntensors,
                                           int64_t total_tiles, const Desc &single,
-                                          const Scalars &s, unsigned long long *nonfinite)
+                                          const Scalars &s, unsigned long long *nonfinite,
+                                          int32_t tile)
 {
     using L = PipeLayout<MODE, GT>;
     extern __shared__ __align__(128) unsigned char pipe_smem[];
@@ -730,7 +782,7 @@ __device__ __forceinline__ void pipe_body(const Desc *__restrict__ table, int32_
         if (table_shared)
             table = reinterpret_cast<const Desc *>(pipe_smem + L::kDescs);
         if (threadIdx.x == kConsumers)
-            pipe_produce<MODE, GT>(pipe_smem, full, empty, table, ntensors, total_tiles);
+            pipe_produce<MODE, GT>(pipe_smem, full, empty, table, ntensors, total_tiles, tile);
         return;
     }
     uint32_t bad = 0;
@@ -741,9 +793,10 @@ __device__ __forceinline__ void pipe_body(const Desc *__restrict__ table, int32_
 template <int MODE, bool U1, typename GT = float>
 __global__ void __launch_bounds__(kPipeThreads, 1)
 adamw_step_pipe_kernel(const Desc *__restrict__ table, int32_t ntensors, int64_t total_tiles,
-                       const Desc single, const Scalars s, unsigned long long *nonfinite)
+                       const Desc single, const Scalars s, unsigned long long *nonfinite,
+                       int32_t tile)
 {
-    pipe_body<MODE, U1, GT>(table, ntensors, total_tiles, single, s, nonfinite);
+    pipe_body<MODE, U1, GT>(table, ntensors, total_tiles, single, s, nonfinite, tile);
 }
 
 // Graph-replayable variant: the scalars of the step are row *index of a
@@ -765,7 +818,7 @@ adamw_step_table_kernel(const Desc *__restrict__ table, int32_t ntensors, int64_
     }
     const Scalars s = rows[i];
     Desc none = {};
-    pipe_body<MODE, false>(table, ntensors, total_tiles, none, s, nonfinite);
+    pipe_body<MODE, false>(table, ntensors, total_tiles, none, s, nonfinite, kTile);
 }
 
 __global__ void advance_index_kernel(int64_t *index)
@@ -800,6 +853,106 @@ decode_state_kernel(const uint32_t *__restrict__ word, float *__restrict__ m,
         const uint32_t w = __ldg(word + i);
         m[i] = MODE == kE4 ? decode_m_lane(w) : decode_fp16_low(w);
         rms[i] = MODE == kE4 ? decode_rms_lane(w) : decode_fp16_high(w);
+    }
+}
+
+// Vectorised codecs: when m, rms and the words share their address modulo 16,
+// the elements after the first `head` (< 4) go as 16-byte vectors, kUnroll of
+// each array per thread and wave, every load of a wave issued before any
+// arithmetic (the scalar kernels above keep one 4-byte load per thread in
+// flight and wait on memory).  The head and the < 4 elements after the last
+// whole vector are coded by single threads of the first CTA.
+template <int MODE>
+__global__ void __launch_bounds__(kThreads)
+encode_state_vec_kernel(const float *__restrict__ m, const float *__restrict__ rms,
+                        uint32_t *__restrict__ word, int64_t n, int64_t head,
+                        unsigned long long *nonfinite)
+{
+    uint32_t bad = 0;
+    const int64_t nv = (n - head) / 4;
+    const float *M = m + head, *R = rms + head;
+    uint32_t *W = word + head;
+    const int64_t wave = (int64_t)gridDim.x * kThreads * kUnroll;
+    for (int64_t v0 = (int64_t)blockIdx.x * kThreads * kUnroll + threadIdx.x; v0 < nv; v0 += wave) {
+        float4 a[kUnroll], b[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t v = v0 + (int64_t)u * kThreads;
+            if (v < nv) {
+                a[u] = load_stream(M + 4 * v);
+                b[u] = load_stream(R + 4 * v);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t v = v0 + (int64_t)u * kThreads;
+            if (v < nv) {
+                const float x[4] = {a[u].x, a[u].y, a[u].z, a[u].w};
+                const float y[4] = {b[u].x, b[u].y, b[u].z, b[u].w};
+                uint32_t w[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    w[j] = MODE == kE4 ? encode_word_e4(x[j], y[j]) : encode_word_fp16(x[j], y[j]);
+                    const uint32_t ea = __float_as_uint(x[j]) & 0x7FFFFFFFu;
+                    const uint32_t eb = __float_as_uint(y[j]) & 0x7FFFFFFFu;
+                    bad += max(ea, eb) >= 0x7F800000u ? 1u : 0u;
+                }
+                store_stream(W + 4 * v, make_uint4(w[0], w[1], w[2], w[3]));
+            }
+        }
+    }
+    if (blockIdx.x == 0 && threadIdx.x < 8) {  // head (threads 0..3) and tail (4..7)
+        const int64_t i = threadIdx.x < 4 ? (int64_t)threadIdx.x : head + 4 * nv + threadIdx.x - 4;
+        if ((threadIdx.x < 4 ? i < head : i < n)) {
+            const float a = m[i], b = rms[i];
+            word[i] = MODE == kE4 ? encode_word_e4(a, b) : encode_word_fp16(a, b);
+            const uint32_t ea = __float_as_uint(a) & 0x7FFFFFFFu, eb = __float_as_uint(b) & 0x7FFFFFFFu;
+            bad += max(ea, eb) >= 0x7F800000u ? 1u : 0u;
+        }
+    }
+    flush_nonfinite(bad, nonfinite);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads)
+decode_state_vec_kernel(const uint32_t *__restrict__ word, float *__restrict__ m,
+                        float *__restrict__ rms, int64_t n, int64_t head)
+{
+    const int64_t nv = (n - head) / 4;
+    const uint32_t *W = word + head;
+    float *M = m + head, *R = rms + head;
+    const int64_t wave = (int64_t)gridDim.x * kThreads * kUnroll;
+    for (int64_t v0 = (int64_t)blockIdx.x * kThreads * kUnroll + threadIdx.x; v0 < nv; v0 += wave) {
+        uint4 a[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t v = v0 + (int64_t)u * kThreads;
+            if (v < nv)
+                a[u] = load_stream(W + 4 * v);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t v = v0 + (int64_t)u * kThreads;
+            if (v < nv) {
+                const uint32_t w[4] = {a[u].x, a[u].y, a[u].z, a[u].w};
+                float x[4], y[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    x[j] = MODE == kE4 ? decode_m_lane(w[j]) : decode_fp16_low(w[j]);
+                    y[j] = MODE == kE4 ? decode_rms_lane(w[j]) : decode_fp16_high(w[j]);
+                }
+                store_stream(M + 4 * v, make_float4(x[0], x[1], x[2], x[3]));
+                store_stream(R + 4 * v, make_float4(y[0], y[1], y[2], y[3]));
+            }
+        }
+    }
+    if (blockIdx.x == 0 && threadIdx.x < 8) {
+        const int64_t i = threadIdx.x < 4 ? (int64_t)threadIdx.x : head + 4 * nv + threadIdx.x - 4;
+        if ((threadIdx.x < 4 ? i < head : i < n)) {
+            const uint32_t w = word[i];
+            m[i] = MODE == kE4 ? decode_m_lane(w) : decode_fp16_low(w);
+            rms[i] = MODE == kE4 ? decode_rms_lane(w) : decode_fp16_high(w);
+        }
     }
 }
 
@@ -948,24 +1101,25 @@ __device__ __forceinline__ uint2 requantise_fast(const float *x, uint32_t sb, co
 
 // One 2048-element block b, by one group of 256 threads (thread gt of the
 // group holds elements 4gt..4gt+3 and 1024+4gt..1024+4gt+3: pv, gv, and the
-// codes mc, vc packed four to a word).  WHOLE: every element is in range (all
+// codes mc, vc packed four to a word; amv the block's two absmax values, read
+// before the stage was handed back).  WHOLE: every element is in range (all
 // blocks but a short last one), so no per-element bound logic is compiled in.
-// The block absmax is a warp max (redux.sync on the binary32 bits of |x|,
-// which orders non-negative floats and lets a NaN win) and a max over the
-// group's 8 warps through shared memory, between which the group meets at
-// its named barrier; `gpar` alternates the shared slots between consecutive
-// blocks of the group.
+// (Packed f32x2 arithmetic, pairing an element's two moments, measured slower
+// here: this kernel is at its register limit.)  The block absmax is a warp max
+// (redux.sync on the binary32 bits of |x|, which orders non-negative floats and
+// lets a NaN win) and a max over the group's 8 warps through shared memory,
+// between which the group meets at its named barrier; `gpar` alternates the
+// shared slots between consecutive blocks of the group.
 template <bool WHOLE, int K>
 __device__ __forceinline__ void blockwise_block(const BlockwiseArgs &a, BlockwiseShared &sh,
                                                 int64_t b, int group, int gt, uint32_t gpar,
-                                                const float pv[8], const float gv[8],
+                                                float2 amv, const float pv[8], const float gv[8],
                                                 const uint32_t mc[2], const uint32_t vc[2],
                                                 const Scalars &s, int k1, int k2, uint32_t &bad)
 {
     const int lane = gt & 31, warp = gt >> 5, copy = lane % kMapCopies;
     const int64_t base = b * kBlock;
-    const float am = a.m_absmax[b], av = a.v_absmax[b];
-    float mn[8], vn[8];
+    float2 nv[8];  // (m', v') of the thread's 8 elements
     uint32_t um = 0, uv = 0;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -973,20 +1127,18 @@ __device__ __forceinline__ void blockwise_block(const BlockwiseArgs &a, Blockwis
         float po[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const float m = __fmul_rn(sh.q1[copy][__byte_perm(mc[h], 0u, 0x4440u + j)], am);
-            const float v = __fmul_rn(sh.q2[copy][__byte_perm(vc[h], 0u, 0x4440u + j)], av);
+            const float m = __fmul_rn(sh.q1[copy][__byte_perm(mc[h], 0u, 0x4440u + j)], amv.x);
+            const float v = __fmul_rn(sh.q2[copy][__byte_perm(vc[h], 0u, 0x4440u + j)], amv.y);
             const Moments o = adamw_element(pv[4 * h + j], gv[4 * h + j], m, v, s);
             po[j] = o.p;
-            if (WHOLE || e0 + j < a.n) {
+            float2 x = make_float2(o.m, o.v);
+            if (WHOLE || e0 + j < a.n)
                 bad += any_nonfinite(o);
-                mn[4 * h + j] = o.m;
-                vn[4 * h + j] = o.v;
-            } else {
-                mn[4 * h + j] = 0.0f;  // |0| never raises the block max
-                vn[4 * h + j] = 0.0f;
-            }
-            um = max(um, __float_as_uint(mn[4 * h + j]) & 0x7FFFFFFFu);
-            uv = max(uv, __float_as_uint(vn[4 * h + j]) & 0x7FFFFFFFu);
+            else
+                x = make_float2(0.0f, 0.0f);  // |0| never raises the block max
+            nv[4 * h + j] = x;
+            um = max(um, __float_as_uint(x.x) & 0x7FFFFFFFu);
+            uv = max(uv, __float_as_uint(x.y) & 0x7FFFFFFFu);
         }
         const __nv_bfloat162 lo = __floats2bfloat162_rn(po[0], po[1]);
         const __nv_bfloat162 hi = __floats2bfloat162_rn(po[2], po[3]);
@@ -1019,27 +1171,21 @@ __device__ __forceinline__ void blockwise_block(const BlockwiseArgs &a, Blockwis
     }
     const uint32_t floor_bits = __float_as_uint(1e-30f);
     const uint32_t smb = max(um, floor_bits), svb = max(uv, floor_bits);  // NaN bits stay NaN
-    uint32_t mcode[2], vcode[2];
-    if (scale_in_fast_range(smb)) {  // uniform over the group
-        const uint2 cm = requantise_fast<K>(mn, smb, sh.mid1[copy], sh.bucket1, k1);
-        mcode[0] = cm.x;
-        mcode[1] = cm.y;
-    } else {
-        const uint2 cm = requantise_slow(mn[0], mn[1], mn[2], mn[3], mn[4], mn[5], mn[6], mn[7],
-                                         __uint_as_float(smb), sh.mid1[copy]);
-        mcode[0] = cm.x;
-        mcode[1] = cm.y;
+    float xm[8], xv[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        xm[j] = nv[j].x;
+        xv[j] = nv[j].y;
     }
-    if (scale_in_fast_range(svb)) {
-        const uint2 cv = requantise_fast<K>(vn, svb, sh.mid2[copy], sh.bucket2, k2);
-        vcode[0] = cv.x;
-        vcode[1] = cv.y;
-    } else {
-        const uint2 cv = requantise_slow(vn[0], vn[1], vn[2], vn[3], vn[4], vn[5], vn[6], vn[7],
-                                         __uint_as_float(svb), sh.mid2[copy]);
-        vcode[0] = cv.x;
-        vcode[1] = cv.y;
-    }
+    const uint2 cm = scale_in_fast_range(smb)  // uniform over the group
+                         ? requantise_fast<K>(xm, smb, sh.mid1[copy], sh.bucket1, k1)
+                         : requantise_slow(xm[0], xm[1], xm[2], xm[3], xm[4], xm[5], xm[6], xm[7],
+                                           __uint_as_float(smb), sh.mid1[copy]);
+    const uint2 cv = scale_in_fast_range(svb)
+                         ? requantise_fast<K>(xv, svb, sh.mid2[copy], sh.bucket2, k2)
+                         : requantise_slow(xv[0], xv[1], xv[2], xv[3], xv[4], xv[5], xv[6], xv[7],
+                                           __uint_as_float(svb), sh.mid2[copy]);
+    const uint32_t mcode[2] = {cm.x, cm.y}, vcode[2] = {cv.x, cv.y};
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         const int64_t e0 = base + 1024 * h + 4 * gt;
@@ -1223,6 +1369,10 @@ __device__ __forceinline__ void bw_consume(unsigned char *smem, uint64_t *full, 
         const bool tile = it.nblk > 0;
         const int64_t b = tile ? it.b0 + group : it.b0;
         const bool mine = tile ? group < it.nblk : group == 0;
+        // the block's absmax values first (their loads overlap the copies below)
+        float2 amv = make_float2(0.0f, 0.0f);
+        if (mine)
+            amv = make_float2(a.m_absmax[b], a.v_absmax[b]);
         // this thread's elements and codes, into registers
         float pv[8], gv[8];
         uint32_t mc[2] = {0u, 0u}, vc[2] = {0u, 0u};
@@ -1268,9 +1418,11 @@ __device__ __forceinline__ void bw_consume(unsigned char *smem, uint64_t *full, 
             // whole blocks with at most one midpoint per bucket (the log-linear
             // maps): the specialised body; anything else: the generic one
             if (tile && kmax <= 1)
-                blockwise_block<true, 1>(a, sh, b, group, gt, gpar, pv, gv, mc, vc, s, k1, k2, bad);
+                blockwise_block<true, 1>(a, sh, b, group, gt, gpar, amv, pv, gv, mc, vc, s, k1, k2,
+                                         bad);
             else
-                blockwise_block<false, 0>(a, sh, b, group, gt, gpar, pv, gv, mc, vc, s, k1, k2, bad);
+                blockwise_block<false, 0>(a, sh, b, group, gt, gpar, amv, pv, gv, mc, vc, s, k1, k2,
+                                          bad);
             gpar ^= 1u;
         }
     }
@@ -1488,6 +1640,28 @@ pa_status pipe_grid(const void *kernel, size_t smem, int64_t tiles, int *grid,
     return PA_OK;
 }
 
+// Elements per tile of a staged launch over `elements` parameters in `tiles`
+// tiles of kTile: kTile, unless those tiles would leave SMs idle; then the
+// smallest multiple of 256 (at least 256) that spreads the elements over the
+// SMs, so a small workload runs on many SMs at once instead of one.
+pa_status launch_tile(int64_t tiles, int64_t elements, int32_t *tile)
+{
+    *tile = pa::kTile;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    int sms = 0;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return cuda_fail(e, "cudaDeviceGetAttribute");
+    if (tiles >= sms || sms < 1)
+        return PA_OK;
+    int64_t t = (elements + sms - 1) / sms;
+    t = (t + 255) / 256 * 256;
+    *tile = (int32_t)(t < 256 ? 256 : (t > pa::kTile ? pa::kTile : t));
+    return PA_OK;
+}
+
 pa_status check_launch(const char *what)
 {
     cudaError_t e = cudaGetLastError();
@@ -1571,7 +1745,12 @@ pa_status step_single(const pa_tensor &t, int64_t step, double lr, double beta1,
     if (t.n == 0)
         return ok();
     Desc d;
-    const int64_t tiles = describe(t, MODE, pa::kTile, &d, (int)sizeof(GT));
+    int64_t tiles = describe(t, MODE, pa::kTile, &d, (int)sizeof(GT));
+    int32_t tile = pa::kTile;
+    if ((st = launch_tile(tiles, t.n, &tile)) != PA_OK)
+        return st;
+    if (tile != pa::kTile)
+        tiles = describe(t, MODE, tile, &d, (int)sizeof(GT));
     d.chunk0 = 0;
     const size_t smem = pa::PipeLayout<MODE, GT>::kBytes;  // the kernel's limit
     const size_t used = pa::PipeLayout<MODE, GT>::bytes_for(1);  // the descriptor, by value
@@ -1582,10 +1761,10 @@ pa_status step_single(const pa_tensor &t, int64_t step, double lr, double beta1,
         return st;
     if (s.bc2 == 1.0f)
         pa::adamw_step_pipe_kernel<MODE, true, GT><<<grid, pa::kPipeThreads, used, (cudaStream_t)stream>>>(
-            nullptr, 1, tiles, d, s, nonfinite);
+            nullptr, 1, tiles, d, s, nonfinite, tile);
     else
         pa::adamw_step_pipe_kernel<MODE, false, GT><<<grid, pa::kPipeThreads, used, (cudaStream_t)stream>>>(
-            nullptr, 1, tiles, d, s, nonfinite);
+            nullptr, 1, tiles, d, s, nonfinite, tile);
     return check_launch("adamw_step_pipe_kernel launch");
 }
 
@@ -1718,7 +1897,12 @@ pa_status step_multi(const pa_tensor *list, int32_t ntensors, int64_t step, doub
     Desc none;
     std::memset(&none, 0, sizeof none);
     int64_t tiles = 0;
-    if ((st = table_for(list, ntensors, MODE, pa::kTile, &table, &tiles, (int)sizeof(GT))) != PA_OK)
+    for (int32_t i = 0; i < ntensors; ++i)
+        tiles += (list[i].n + pa::kTile - 1) / pa::kTile;
+    int32_t tile = pa::kTile;
+    if ((st = launch_tile(tiles, total, &tile)) != PA_OK)
+        return st;
+    if ((st = table_for(list, ntensors, MODE, tile, &table, &tiles, (int)sizeof(GT))) != PA_OK)
         return st;
     const size_t smem = pa::PipeLayout<MODE, GT>::kBytes;  // the kernel's limit
     const size_t used = pa::PipeLayout<MODE, GT>::bytes_for(ntensors);
@@ -1729,11 +1913,26 @@ pa_status step_multi(const pa_tensor *list, int32_t ntensors, int64_t step, doub
         return st;
     if (s.bc2 == 1.0f)
         pa::adamw_step_pipe_kernel<MODE, true, GT><<<grid, pa::kPipeThreads, used, (cudaStream_t)stream>>>(
-            table, ntensors, tiles, none, s, nonfinite);
+            table, ntensors, tiles, none, s, nonfinite, tile);
     else
         pa::adamw_step_pipe_kernel<MODE, false, GT><<<grid, pa::kPipeThreads, used, (cudaStream_t)stream>>>(
-            table, ntensors, tiles, none, s, nonfinite);
+            table, ntensors, tiles, none, s, nonfinite, tile);
     return check_launch("adamw_step_pipe_kernel (multi) launch");
+}
+
+// True when m, rms and the words share their address modulo 16 (4-byte
+// aligned each): the vectorised codec kernels then apply, after `head` < 4
+// leading elements.
+bool vector_codec(const void *m, const void *rms, const void *word, int64_t n, int64_t *head)
+{
+    const uintptr_t a = reinterpret_cast<uintptr_t>(m) & 15u;
+    if ((reinterpret_cast<uintptr_t>(rms) & 15u) != a || (reinterpret_cast<uintptr_t>(word) & 15u) != a)
+        return false;
+    const int64_t h = (int64_t)((16u - a) & 15u) / 4;
+    if (n < h + 4)
+        return false;
+    *head = h;
+    return true;
 }
 
 template <int MODE>
@@ -1752,6 +1951,16 @@ pa_status encode(const float *m, const float *rms, uint32_t *word, int64_t n,
     if (st != PA_OK)
         return st;
     int grid = 0;
+    int64_t head = 0;
+    if (vector_codec(m, rms, word, n, &head)) {
+        const int64_t waves = ((n - head) / 4 + pa::kThreads * pa::kUnroll - 1) /
+                              (pa::kThreads * pa::kUnroll);
+        if ((st = grid_for(kSlotCodec, waves, &grid)) != PA_OK)
+            return st;
+        pa::encode_state_vec_kernel<MODE><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
+            m, rms, word, n, head, nonfinite);
+        return check_launch("encode_state_vec_kernel launch");
+    }
     if ((st = grid_for(kSlotCodec, (n + pa::kThreads - 1) / pa::kThreads, &grid)) != PA_OK)
         return st;
     pa::encode_state_kernel<MODE><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(m, rms, word, n, nonfinite);
@@ -1770,8 +1979,18 @@ pa_status decode(const uint32_t *word, float *m, float *rms, int64_t n, pa_strea
     if (!aligned(m, 4) || !aligned(rms, 4) || !aligned(word, 4))
         return fail(PA_ERR_ALIGN, "pointers must be 4-byte aligned");
     int grid = 0;
-    pa_status st = grid_for(kSlotCodec, (n + pa::kThreads - 1) / pa::kThreads, &grid);
-    if (st != PA_OK)
+    pa_status st;
+    int64_t head = 0;
+    if (vector_codec(m, rms, word, n, &head)) {
+        const int64_t waves = ((n - head) / 4 + pa::kThreads * pa::kUnroll - 1) /
+                              (pa::kThreads * pa::kUnroll);
+        if ((st = grid_for(kSlotCodec, waves, &grid)) != PA_OK)
+            return st;
+        pa::decode_state_vec_kernel<MODE><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(
+            word, m, rms, n, head);
+        return check_launch("decode_state_vec_kernel launch");
+    }
+    if ((st = grid_for(kSlotCodec, (n + pa::kThreads - 1) / pa::kThreads, &grid)) != PA_OK)
         return st;
     pa::decode_state_kernel<MODE><<<grid, pa::kThreads, 0, (cudaStream_t)stream>>>(word, m, rms, n);
     return check_launch("decode_state_kernel launch");
@@ -2082,10 +2301,10 @@ extern "C" pa_status pa_adamw_step_packed_e4_multi_noalloc(
     std::memset(&none, 0, sizeof none);
     if (s.bc2 == 1.0f)
         pa::adamw_step_pipe_kernel<pa::kE4, true><<<grid, pa::kPipeThreads, used, (cudaStream_t)stream>>>(
-            table, ntensors, tiles, none, s, nonfinite);
+            table, ntensors, tiles, none, s, nonfinite, pa::kTile);
     else
         pa::adamw_step_pipe_kernel<pa::kE4, false><<<grid, pa::kPipeThreads, used, (cudaStream_t)stream>>>(
-            table, ntensors, tiles, none, s, nonfinite);
+            table, ntensors, tiles, none, s, nonfinite, pa::kTile);
     return check_launch("adamw_step_pipe_kernel (no-alloc multi) launch");
 }
 

@@ -95,3 +95,39 @@ def test_empty_and_errors(pa):
     with pytest.raises(pa.PackedAdamError) as ei:
         pa._check(pa._lib.pa_encode_state(None, None, None, 4, None, None))
     assert ei.value.status == 1
+
+
+@pytest.mark.parametrize("mode", ["e4", "fp16"])
+def test_codecs_at_every_phase_and_size(pa, mode):
+    """Views at each 4-byte phase (the vectorised kernels peel a head of up to 3
+    elements and code a tail of up to 3 one by one) and arrays whose phases
+    differ (the per-element kernels): encode and decode equal the oracle."""
+    import torch
+
+    rng = np.random.default_rng(77)
+    enc = pa.pa_encode_state if mode == "e4" else pa.pa_encode_state_fp16
+    dec = pa.pa_decode_state if mode == "e4" else pa.pa_decode_state_fp16
+    for n in (1, 3, 4, 5, 7, 8, 9, 4097, 100_003):
+        for phases in ((0, 0, 0), (1, 1, 1), (2, 2, 2), (3, 3, 3), (0, 1, 2), (3, 0, 0)):
+            m = rng.normal(0, 1e-3, n).astype(np.float32)
+            r = np.abs(rng.normal(0, 1e-3, n)).astype(np.float32)
+            bufs = [torch.zeros(n + 8, dtype=dt, device="cuda")
+                    for dt in (torch.float32, torch.float32, torch.int32)]
+            dm, dr, dw = (b[o:o + n] for b, o in zip(bufs, phases))
+            dm.copy_(dev(m))
+            dr.copy_(dev(r))
+            bad = torch.zeros(1, dtype=torch.int64, device="cuda")
+            enc(dm, dr, dw, nonfinite=bad)
+            torch.cuda.synchronize()
+            ew, _ = oracle.encode_state(m, r, mode=mode)
+            assert np.array_equal(host_u32(dw), ew), (n, phases)
+            assert int(bad.item()) == 0
+            dm.zero_()
+            dr.zero_()
+            dec(dw, dm, dr)
+            torch.cuda.synchronize()
+            em, er = oracle.decode_state(ew, mode=mode)
+            assert np.array_equal(host_f32(dm).view(np.uint32), em.view(np.uint32)), (n, phases)
+            assert np.array_equal(host_f32(dr).view(np.uint32), er.view(np.uint32)), (n, phases)
+            assert not any(b[:o].any() or b[o + n:].any() for b, o in zip(bufs, phases)), \
+                "write outside the views"
