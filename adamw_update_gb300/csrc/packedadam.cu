@@ -957,23 +957,26 @@ decode_state_vec_kernel(const uint32_t *__restrict__ word, float *__restrict__ m
 }
 
 // ---- 8-bit blockwise mode (KBench quantized_adamw_step, _requantise) -------------
-// One CTA of 256 threads owns one 2048-element block per iteration of a
-// persistent loop.  Thread t holds elements 4t..4t+3 and 1024+4t..1024+4t+3 of
-// the block (16-byte loads of p and g, 4-byte loads of each code array).  The
+// One CTA of 32 warps per SM (blockwise8_pipe_kernel below): a tile of four
+// 2048-element blocks is bulk-copied into a two-stage shared-memory ring, and
+// each group of 8 warps (256 threads) updates one block of the tile.  Thread t
+// of a group holds elements 4t..4t+3 and 1024+4t..1024+4t+3 of its block.  The
 // new block absmax is a warp max (redux.sync on the binary32 bits of |x|,
 // which orders non-negative floats and lets a NaN win) followed by a max over
-// the 8 warp results in shared memory.
+// the group's 8 warp results in shared memory at the group's named barrier.
 //
 // Requantisation, per element: c = x / max(absmax, 1e-30) and code = the
 // number of the map's 255 midpoints strictly below c.
 //  * Division.  When the block scale is a normal number in [2^-100, 2^100),
-//    each thread takes y = RN(1/scale) once per block (__frcp_rn) and forms
-//    c = RN(q0 + r*y) with q0 = RN(x*y) and r = x - scale*q0 (exact by FMA):
-//    Markstein's theorem (P. Markstein, IBM J. Res. Dev. 34(1), 1990) makes
-//    this the correctly rounded quotient when y is the correctly rounded
-//    reciprocal and nothing under- or overflows; here |x| <= scale, so that
-//    holds for |x| >= 2^-100; zeros keep their sign by an OR of the sign bit;
-//    other |x| < 2^-100 use the IEEE divide.
+//    each thread takes y = RN(1/scale) once per block (reciprocal_rn: the
+//    hardware approximation refined by one Newton-Raphson step, equal to the
+//    IEEE reciprocal on that range) and forms c = RN(q0 + r*y) with
+//    q0 = RN(x*y) and r = x - scale*q0 (exact by FMA): Markstein's theorem
+//    (P. Markstein, IBM J. Res. Dev. 34(1), 1990) makes this the correctly
+//    rounded quotient when y is the correctly rounded reciprocal and nothing
+//    under- or overflows; here |x| <= scale, so that holds for |x| above a
+//    floor; zeros keep their sign by an OR of the sign bit; other nonzero |x|
+//    below the floor use the IEEE divide in a rarely entered fix-up.
 //  * Search.  A per-CTA table indexed by the top 14 bits of c's binary32
 //    pattern (32 buckets per binade, either sign) holds the number of
 //    midpoints below every value of the bucket; the code is that count plus K

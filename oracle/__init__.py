@@ -27,23 +27,33 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 SOURCE = os.path.join(_HERE, "oracle.c")
+TURBO_SOURCE = os.path.join(_HERE, "turbo.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 BLOCK = 2048
+TURBO_BLOCK = 128
+TURBO_MEAN = 64
 
 CFLAGS = ["-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
 
 
-def compile_source(src: str, out: str) -> str:
-    """Compile a C oracle source file into a shared library at ``out``."""
+def compile_sources(srcs, out: str) -> str:
+    """Compile C oracle source files into one shared library at ``out``."""
     tmp = out + f".{os.getpid()}.tmp"
-    subprocess.run(["gcc", *CFLAGS, src, "-o", tmp, "-lm"], check=True)
+    subprocess.run(["gcc", *CFLAGS, *srcs, "-o", tmp, "-lm"], check=True)
     os.replace(tmp, out)
     return out
 
 
+def compile_source(src: str, out: str, turbo: str | None = None) -> str:
+    """Compile a copy of oracle.c (``src``) with turbo.c (or ``turbo``, a copy
+    of it) into a shared library at ``out``."""
+    return compile_sources([src, turbo or TURBO_SOURCE], out)
+
+
 def build(force: bool = False) -> str:
-    """Compile oracle.c into liboracle.so (gcc, strict IEEE binary32)."""
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(SOURCE):
+    """Compile oracle.c and turbo.c into liboracle.so (gcc, strict IEEE binary32)."""
+    newest = max(os.path.getmtime(SOURCE), os.path.getmtime(TURBO_SOURCE))
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < newest:
         compile_source(SOURCE, _LIB)
     return _LIB
 
@@ -78,6 +88,23 @@ _SIGNATURES = {
         ctypes.c_uint64,
         [_f32p, _f32p, _u16p, _u8p, _f32p, _u8p, _f32p, _f32p, _f32p, _i64, *_HYP],
     ),
+    # TurboAdam-style state (turbo.c)
+    "oracle_splitmix64_at": (ctypes.c_uint64, [ctypes.c_uint64, ctypes.c_uint64]),
+    "oracle_turbo_uniform_array": (None, [ctypes.c_uint64, _i64, ctypes.c_uint32,
+                                          ctypes.POINTER(ctypes.c_uint64), _f32p, _i64]),
+    "oracle_q1_levels": (None, [ctypes.c_int, ctypes.c_int, ctypes.c_int, _f32p]),
+    "oracle_q1_index_array": (None, [_f32p, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                     _f32p, ctypes.POINTER(ctypes.c_int32)]),
+    "oracle_q1_endpoints_pair": (None, [_f32p, _i64, ctypes.POINTER(ctypes.c_int32)]),
+    "oracle_q1_endpoint_code": (ctypes.c_uint16, [ctypes.c_int]),
+    "oracle_q1_endpoint_value": (ctypes.c_int, [ctypes.c_uint16]),
+    "oracle_ustate_code_array": (None, [_f32p, _i64, ctypes.c_float, _f32p,
+                                        ctypes.POINTER(ctypes.c_int32)]),
+    "oracle_turbo_step": (ctypes.c_uint64, [_f32p, _f32p, _i64, _u8p, _u16p, _f32p, _u8p, _u16p,
+                                            *_HYP, ctypes.c_uint64]),
+    "oracle_turbo_finalize": (None, [_f32p, _i64, _d]),
+    "oracle_turbo_decode": (None, [_i64, _u8p, _u16p, _f32p, _u8p, _u16p, _i64, _d, _d, _d,
+                                   _f32p, _f32p]),
 }
 
 
@@ -289,6 +316,112 @@ class Oracle:
         bad = _run_sliced(run, n, threads, align=BLOCK)
         return out, mc, ma, vc, va, bad
 
+
+def turbo_state_sizes(n: int):
+    """Element counts of the TurboAdam-style state arrays of an n-element tensor:
+    ucode (uint8), umean (uint16 bf16), uscal (float32), vidx (uint8), vend
+    (uint16 fp16)."""
+    return {"ucode": -(-n // 4), "umean": -(-n // TURBO_MEAN), "uscal": 3,
+            "vidx": -(-n // 2), "vend": 2 * -(-n // TURBO_BLOCK)}
+
+
+def turbo_zero_state(n: int):
+    """The initial state (everything zero): decodes to m = v = 0."""
+    z = turbo_state_sizes(n)
+    return {"ucode": np.zeros(z["ucode"], np.uint8), "umean": np.zeros(z["umean"], np.uint16),
+            "uscal": np.zeros(3, np.float32), "vidx": np.zeros(z["vidx"], np.uint8),
+            "vend": np.zeros(z["vend"], np.uint16)}
+
+
+def _turbo_methods():
+    def splitmix64_at(self, seed, counter):
+        return int(self.lib.oracle_splitmix64_at(ctypes.c_uint64(seed), ctypes.c_uint64(counter)))
+
+    def turbo_uniform(self, seed, step, stream, index):
+        idx = _arr(index, np.uint64)
+        out = np.empty(idx.size, np.float32)
+        self.lib.oracle_turbo_uniform_array(ctypes.c_uint64(seed), int(step), int(stream),
+                                            _ptr(idx, ctypes.c_uint64), _ptr(out, ctypes.c_float),
+                                            idx.size)
+        return out
+
+    def q1_levels(self, lo, hi, bits=4):
+        out = np.empty(1 << bits, np.float32)
+        self.lib.oracle_q1_levels(int(lo), int(hi), int(bits), _ptr(out, ctypes.c_float))
+        return out
+
+    def q1_index(self, v, lo, hi, u, bits=4):
+        v = _arr(v, np.float32)
+        u = _arr(u, np.float32)
+        out = np.empty(v.size, np.int32)
+        self.lib.oracle_q1_index_array(_ptr(v, ctypes.c_float), v.size, int(lo), int(hi),
+                                       int(bits), _ptr(u, ctypes.c_float),
+                                       _ptr(out, ctypes.c_int32))
+        return out
+
+    def q1_endpoints(self, v):
+        v = _arr(v, np.float32)
+        out = np.empty(2, np.int32)
+        self.lib.oracle_q1_endpoints_pair(_ptr(v, ctypes.c_float), v.size,
+                                          _ptr(out, ctypes.c_int32))
+        return int(out[0]), int(out[1])
+
+    def q1_endpoint_code(self, e):
+        return int(self.lib.oracle_q1_endpoint_code(int(e)))
+
+    def q1_endpoint_value(self, h):
+        return int(self.lib.oracle_q1_endpoint_value(int(h)))
+
+    def ustate_code(self, r, s, u):
+        r = _arr(r, np.float32)
+        u = _arr(u, np.float32)
+        out = np.empty(r.size, np.int32)
+        self.lib.oracle_ustate_code_array(_ptr(r, ctypes.c_float), r.size, ctypes.c_float(s),
+                                          _ptr(u, ctypes.c_float), _ptr(out, ctypes.c_int32))
+        return out
+
+    def turbo_step(self, p, g, state, step, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8,
+                   wd=0.01, seed=0x12345678):
+        """One TurboAdam-style step of one tensor; returns (p', state', nonfinite)
+        with state a dict of ucode, umean, uscal, vidx, vend (copied)."""
+        p = _arr(p, np.float32)
+        g = _arr(g, np.float32)
+        n = p.size
+        assert g.size == n
+        st = {k: _arr(v, v.dtype) for k, v in state.items()}
+        z = turbo_state_sizes(n)
+        for k, size in z.items():
+            assert st[k].size == size, (k, st[k].size, size)
+        bad = self.lib.oracle_turbo_step(
+            _ptr(p, ctypes.c_float), _ptr(g, ctypes.c_float), n, _ptr(st["ucode"], ctypes.c_uint8),
+            _ptr(st["umean"], ctypes.c_uint16), _ptr(st["uscal"], ctypes.c_float),
+            _ptr(st["vidx"], ctypes.c_uint8), _ptr(st["vend"], ctypes.c_uint16),
+            *_hyp(step, lr, beta1, beta2, eps, wd), ctypes.c_uint64(seed))
+        return p, st, int(bad)
+
+    def turbo_decode(self, state, n, step, beta1=0.9, beta2=0.999, eps=1e-8):
+        """(m_prev, v_dec): the prior moments the step at `step` decodes."""
+        st = {k: _arr(v, v.dtype) for k, v in state.items()}
+        m = np.empty(n, np.float32)
+        v = np.empty(n, np.float32)
+        self.lib.oracle_turbo_decode(
+            int(n), _ptr(st["ucode"], ctypes.c_uint8), _ptr(st["umean"], ctypes.c_uint16),
+            _ptr(st["uscal"], ctypes.c_float), _ptr(st["vidx"], ctypes.c_uint8),
+            _ptr(st["vend"], ctypes.c_uint16), int(step), float(beta1), float(beta2), float(eps),
+            _ptr(m, ctypes.c_float), _ptr(v, ctypes.c_float))
+        return m, v
+
+    def turbo_finalize(self, uscal, n, factor=1.1):
+        s = _arr(uscal, np.float32)
+        self.lib.oracle_turbo_finalize(_ptr(s, ctypes.c_float), int(n), float(factor))
+        return s
+
+    for f in (splitmix64_at, turbo_uniform, q1_levels, q1_index, q1_endpoints, q1_endpoint_code,
+              q1_endpoint_value, ustate_code, turbo_step, turbo_decode, turbo_finalize):
+        setattr(Oracle, f.__name__, f)
+
+
+_turbo_methods()
 
 _default: Oracle | None = None
 _lock = threading.Lock()

@@ -1,0 +1,57 @@
+"""The TurboAdam-style oracle against its pins (CPU only), and planted mistakes
+in copies of turbo.c that the pins must catch."""
+import os
+
+import pytest
+
+import oracle
+import pins_turbo
+
+with open(oracle.TURBO_SOURCE) as _f:
+    _SRC = _f.read()
+
+
+@pytest.mark.parametrize("name", sorted(pins_turbo.ALL_CHECKS))
+def test_turbo_oracle_pin(name):
+    pins_turbo.ALL_CHECKS[name](oracle.default())
+
+
+MUTANTS = [
+    ("grid_intervals_off_by_one", "return float_of((uint32_t)(blo + num / (uint64_t)(K - 1)));",
+     "return float_of((uint32_t)(blo + num / (uint64_t)K));", ["q1_grid_closed_forms"]),
+    ("upper_endpoint_not_rounded_up", "*hi = (mx == ldexpf(1.0f, e)) ? e : e + 1;", "*hi = e;",
+     ["q1_endpoints"]),
+    ("rounds_up_on_large_u", "return (u < p) ? j + 1 : j;", "return (u > p) ? j + 1 : j;",
+     ["q1_rounding"]),
+    ("ustate_rounds_up_on_large_u", "return (u < frac) ? j + 1 : j;",
+     "return (u > frac) ? j + 1 : j;", ["ustate_code"]),
+    ("no_recentring", "float delta = (sdec * (float)S) / (float)(2 * c);", "float delta = 0.0f;",
+     ["means_recentred", "first_moment_reconstructed"]),
+    ("q_normalised_by_exact_v", "float den = sqrtf(vhat[k + j] / h.bc2) + h.ef;",
+     "float den = sqrtf(vnew[k + j] / h.bc2) + h.ef;",
+     ["means_recentred"]),
+    ("scales_not_rotated", "uscal[0] = uscal[1];", "uscal[0] = uscal[0];",
+     ["finalize_rotates_scales"]),
+    ("prior_first_moment_not_rescaled", "m = (q * den) * bc1p;", "m = q * bc1p;",
+     ["step_is_adamw_on_decoded_moments", "first_moment_reconstructed"]),
+    ("mean_not_divided", "float mean = tree_sum64(qv) / (float)c;", "float mean = tree_sum64(qv);",
+     ["means_recentred"]),
+    ("hash_counter_not_advanced", "return oracle_splitmix64_mix(seed + (counter + 1u) * 0x9E3779B97F4A7C15ull);",
+     "return oracle_splitmix64_mix(seed + counter);", ["counter_is_a_splitmix_position"]),
+]
+
+
+@pytest.mark.parametrize("name,old,new,expect", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_turbo_pins_catch_planted_mistake(name, old, new, expect, tmp_path):
+    assert _SRC.count(old) == 1, f"mutation anchor not found once: {old!r}"
+    src = tmp_path / f"{name}.c"
+    src.write_text(_SRC.replace(old, new, 1))
+    lib = oracle.compile_source(oracle.SOURCE, str(tmp_path / f"{name}.so"), turbo=str(src))
+    orc = oracle.Oracle(os.path.abspath(lib))
+    caught = []
+    for pin in expect:
+        try:
+            pins_turbo.ALL_CHECKS[pin](orc)
+        except AssertionError:
+            caught.append(pin)
+    assert caught, f"planted mistake {name} passed every pin in {expect}"
