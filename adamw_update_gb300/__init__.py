@@ -29,7 +29,7 @@ __all__ = [
     "shard_bounds", "pa_adamw_step_packed_e4_multi_noalloc", "pa_adamw_step_packed_e4_host",
     "pa_hyper_table_fill", "pa_adamw_step_packed_e4_multi_graph",
     "pa_adamw_step_packed_e4_bf16g", "pa_adamw_step_packed_e4_multi_bf16g", "pa_shutdown",
-    "pa_adamw_step_blockwise8_multi", "pa_device_fault",
+    "pa_adamw_step_blockwise8_multi", "pa_device_fault", "pa_turbo_step", "turbo_state",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -451,3 +451,45 @@ def pa_device_fault(clear: bool = False) -> int:
     code = ctypes.c_uint32(0)
     _check(_lib.pa_device_fault(ctypes.byref(code), 1 if clear else 0))
     return int(code.value)
+
+
+# ---- TurboAdam-style step (UState first moment, 1Q second moment) -----------------
+
+class PaTurboState(ctypes.Structure):
+    """pa_turbo_state: device pointers of ucode, umean, uscal, vidx, vend."""
+    _fields_ = [("ucode", ctypes.c_void_p), ("umean", ctypes.c_void_p), ("uscal", ctypes.c_void_p),
+                ("vidx", ctypes.c_void_p), ("vend", ctypes.c_void_p)]
+
+
+_lib.pa_turbo_step.restype = _i32
+_lib.pa_turbo_step.argtypes = [_vp, _vp, _i64, ctypes.POINTER(PaTurboState), *_HYP, _d,
+                               ctypes.c_uint64, _vp, _vp]
+
+TURBO_BLOCK = 128
+TURBO_MEAN = 64
+
+
+def turbo_state(n: int, device="cuda"):
+    """Zero TurboAdam-style state of an n-element tensor (the initial state):
+    dict of ucode uint8, umean int16 (bf16 bits), uscal float32[3], vidx uint8,
+    vend int16 (fp16 bits)."""
+    torch = _t()
+    return {"ucode": torch.zeros(-(-n // 4), dtype=torch.uint8, device=device),
+            "umean": torch.zeros(-(-n // TURBO_MEAN), dtype=torch.int16, device=device),
+            "uscal": torch.zeros(3, dtype=torch.float32, device=device),
+            "vidx": torch.zeros(-(-n // 2), dtype=torch.uint8, device=device),
+            "vend": torch.zeros(2 * -(-n // TURBO_BLOCK), dtype=torch.int16, device=device)}
+
+
+def pa_turbo_step(p, g, state, step, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, wd=0.0,
+                  m_step_factor=1.1, seed=0x12345678, nonfinite=None, stream=None):
+    """TurboAdam-style step of one tensor: p updated in place, `state` (from
+    turbo_state) advanced, scales rotated."""
+    torch = _t()
+    st = PaTurboState(_ptr(state["ucode"], torch.uint8), _ptr(state["umean"], torch.int16),
+                      _ptr(state["uscal"], torch.float32), _ptr(state["vidx"], torch.uint8),
+                      _ptr(state["vend"], torch.int16))
+    _check(_lib.pa_turbo_step(_ptr(p, torch.float32), _ptr(g, torch.float32), p.numel(),
+                              ctypes.byref(st), *_hyp(step, lr, beta1, beta2, eps, wd),
+                              float(m_step_factor), ctypes.c_uint64(seed), _ptr(nonfinite),
+                              _stream(stream)))

@@ -1474,6 +1474,8 @@ blockwise8_pipe_kernel(const BwDesc *__restrict__ table, int32_t ntensors, int64
 
 }  // namespace pa
 
+#include "turbo.cuh"
+
 // ===========================================================================
 // Host side
 // ===========================================================================
@@ -1537,7 +1539,7 @@ pa_status make_scalars(int64_t step, double lr, double beta1, double beta2, doub
 // ---- per-device launch geometry --------------------------------------------
 // Kernels launched with kThreads threads and no dynamic shared memory: the
 // register-staged step (on host memory) and the codecs.
-enum KernelSlot { kSlotHostE4, kSlotCodec, kNumSlots };
+enum KernelSlot { kSlotHostE4, kSlotCodec, kSlotTurbo, kNumSlots };
 
 struct DeviceInfo {
     bool ready = false;
@@ -1552,6 +1554,7 @@ const void *kernel_of(int slot)
 {
     switch (slot) {
     case kSlotHostE4: return (const void *)pa::adamw_step_kernel<pa::kE4, false, false, float>;
+    case kSlotTurbo: return (const void *)pa::turbo_step_kernel;
     default: return (const void *)pa::encode_state_kernel<pa::kE4>;
     }
 }
@@ -2755,4 +2758,57 @@ pa_status release_blockwise_tables()
     g_bw_tables.clear();
     cudaSetDevice(cur);
     return PA_OK;
+}
+
+// ===========================================================================
+// TurboAdam-style step (UState first moment, 1Q second moment)
+// ===========================================================================
+extern "C" pa_status pa_turbo_step(float *p, const float *g, int64_t n, const pa_turbo_state *state,
+                                   int64_t step, double lr, double beta1, double beta2, double eps,
+                                   double wd, double m_step_factor, uint64_t seed,
+                                   unsigned long long *nonfinite, pa_stream stream)
+{
+    Scalars s;
+    pa_status st = make_scalars(step, lr, beta1, beta2, eps, wd, &s);
+    if (st != PA_OK)
+        return st;
+    if (!(beta1 * beta1 < beta2))
+        return fail(PA_ERR_ARG, "UState needs beta1^2 < beta2 (got %g, %g)", beta1, beta2);
+    if (!std::isfinite(m_step_factor) || !(m_step_factor > 0.0))
+        return fail(PA_ERR_ARG, "m_step_factor must be finite and > 0 (got %g)", m_step_factor);
+    if (n < 0)
+        return fail(PA_ERR_ARG, "n must be >= 0 (got %lld)", (long long)n);
+    if (n > ((int64_t)1 << 40) || step >= ((int64_t)1 << 22))
+        return fail(PA_ERR_ARG, "n must be <= 2^40 and step < 2^22 (the rounding counter's fields)");
+    if (n == 0)
+        return ok();
+    if (!state)
+        return fail(PA_ERR_NULL, "state is NULL");
+    const pa_turbo_state t = *state;
+    if (!p || !g || !t.ucode || !t.umean || !t.uscal || !t.vidx || !t.vend)
+        return fail(PA_ERR_NULL, "NULL pointer with n = %lld", (long long)n);
+    if (!aligned(p, 16) || !aligned(g, 16))
+        return fail(PA_ERR_ALIGN, "p and g must be 16-byte aligned");
+    if (!aligned(t.umean, 2) || !aligned(t.vidx, 2) || !aligned(t.vend, 2) || !aligned(t.uscal, 4))
+        return fail(PA_ERR_ALIGN, "umean, vidx, vend must be 2-byte and uscal 4-byte aligned");
+    if ((st = check_counter(nonfinite)) != PA_OK)
+        return st;
+    pa::TurboArgs a = {p, g, n, t.ucode, t.umean, t.uscal, t.vidx, t.vend};
+    pa::TurboScalars ts;
+    ts.s = s;
+    ts.bc1 = (float)(1.0 - std::pow(beta1, (double)step));
+    ts.bc1p = (float)(1.0 - std::pow(beta1, (double)(step - 1)));
+    ts.bc2p = (float)(1.0 - std::pow(beta2, (double)(step - 1)));
+    ts.seed = seed;
+    ts.step = step;
+    const int64_t blocks = (n + pa::kTurboBlock - 1) / pa::kTurboBlock;
+    int grid = 0;
+    if ((st = grid_for(kSlotTurbo, (blocks + pa::kTurboWarps - 1) / pa::kTurboWarps, &grid)) != PA_OK)
+        return st;
+    cudaStream_t cs = (cudaStream_t)stream;
+    pa::turbo_step_kernel<<<grid, pa::kTurboThreads, 0, cs>>>(a, ts, nonfinite);
+    if ((st = check_launch("turbo_step_kernel launch")) != PA_OK)
+        return st;
+    pa::turbo_finalize_kernel<<<1, 32, 0, cs>>>(t.uscal, (float)n, (float)m_step_factor);
+    return check_launch("turbo_finalize_kernel launch");
 }

@@ -1,0 +1,349 @@
+// turbo.cuh -- the TurboAdam-style step: the first moment persisted with
+// UState, the second with 1Q ("TurboAdam" README, turboadam 0.2.0, "How it
+// works").  Included at the end of packedadam.cu (one translation unit: it
+// uses that file's host helpers and the FP32 element of codecs.cuh).
+//
+// State of an n-element tensor (the README's memory table: 2 bits + one bf16
+// per 64 values + 12 bytes of UState, 4 bits + two fp16 per 128 values of 1Q):
+//   ucode  uint8[(n+3)/4]    2-bit UState codes, element i at bits 2*(i%4) of byte i/4
+//   umean  uint16[(n+63)/64] bf16 mean of each 64-value mean block
+//   uscal  float[3]          decode scale, encode scale, RMS accumulator
+//   vidx   uint8[(n+1)/2]    4-bit 1Q indices, element i in nibble i%2 of byte i/2
+//   vend   uint16[2*ceil(n/128)] fp16 log endpoints (lo, hi) of each 128-block
+// Readings where the page is silent (listed in the header): the 1Q grid is
+// uniform in the binary32 bit pattern between the integer binary exponents
+// that bracket the block's positive values (exact, no transcendental
+// function); index 0 is 0; stochastic rounding with u from SplitMix64 at a
+// counter (step, stream, element); UState levels {-1.5, -0.5, 0.5, 1.5} times
+// the one-step-lagged encode scale, antithetic pairs (2k, 2k+1) share u and
+// 1-u; block means are pairwise trees rounded to bf16; the finaliser rotates
+// the scales (decode <- encode, encode <- factor * sqrt(acc / n), acc <- 0).
+//
+// Design.  One warp per 128-value storage block, lane l holding values
+// 4l..4l+3 (16-byte loads of p and g; one code byte and one index half-word):
+// the block's endpoints are warp min/max reductions over the binary32 bits of
+// the positive values, the 15 grid levels live one per lane and are read by
+// shuffles in a 4-step binary search, and a mean block's pairwise tree is the
+// lane's own ((q0+q1)+(q2+q3)) followed by xor-shuffles over its 16 lanes --
+// the same tree, since IEEE addition is commutative.  The RMS accumulator is
+// one float atomic per warp (its sum order is the only thing that differs
+// from a sequential evaluation).
+#pragma once
+
+namespace pa {
+
+constexpr int kTurboBlock = 128;  // 1Q storage block
+constexpr int kTurboMean = 64;    // UState mean block
+constexpr int kTurboWarps = 8;    // warps (storage blocks in flight) per CTA
+constexpr int kTurboThreads = kTurboWarps * 32;
+
+struct TurboArgs {
+    float *p;
+    const float *g;
+    int64_t n;
+    uint8_t *ucode;
+    uint16_t *umean;
+    float *uscal;
+    uint8_t *vidx;
+    uint16_t *vend;
+};
+
+struct TurboScalars {
+    Scalars s;        // the step's FP32 scalars (as every mode)
+    float bc1;        // 1 - beta1^step
+    float bc1p, bc2p; // 1 - beta1^(step-1), 1 - beta2^(step-1)
+    uint64_t seed;
+    int64_t step;
+};
+
+// ---- counter hash: SplitMix64 (Steele, Lea, Flood, OOPSLA 2014) at a counter
+__device__ __forceinline__ uint64_t splitmix64_mix(uint64_t z)
+{
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+// u in [0, 1) on the 2^-24 grid for (step, stream, index)
+__device__ __forceinline__ float turbo_uniform(uint64_t seed, int64_t step, uint32_t stream,
+                                               uint64_t index)
+{
+    const uint64_t c = ((uint64_t)step << 42) | ((uint64_t)stream << 40) | index;
+    const uint64_t z = splitmix64_mix(seed + (c + 1u) * 0x9E3779B97F4A7C15ull);
+    return __uint2float_rn((uint32_t)(z >> 40)) * 0x1p-24f;
+}
+
+// ---- 1Q grid ---------------------------------------------------------------------
+__device__ __forceinline__ uint32_t pow2_bits(int e)
+{
+    return e >= -126 ? (uint32_t)(e + 127) << 23 : 1u << (e + 149);
+}
+
+// level k (0..15) of the grid [2^lo, 2^hi] given B(lo), B(hi)
+__device__ __forceinline__ float q1_level(uint32_t blo, uint32_t bhi, int k)
+{
+    if (k <= 0)
+        return 0.0f;
+    const uint64_t num = (uint64_t)(bhi - blo) * (uint64_t)(k - 1) + 7u;
+    return __uint_as_float(blo + (uint32_t)(num / 14u));
+}
+
+// binary exponent of a positive finite float given its bits
+__device__ __forceinline__ int exponent_of_bits(uint32_t b)
+{
+    return b >= 0x00800000u ? (int)(b >> 23) - 127 : (31 - __clz((int)b)) - 149;
+}
+
+__device__ __forceinline__ bool power_of_two_bits(uint32_t b)
+{
+    return b >= 0x00800000u ? (b & 0x007FFFFFu) == 0u : (b & (b - 1u)) == 0u;
+}
+
+// ---- UState code ------------------------------------------------------------------
+__device__ __forceinline__ uint32_t ustate_code(float r, float s, float u)
+{
+    const float y = s > 0.0f ? __fdiv_rn(r, s) : 0.0f;
+    float z = __fadd_rn(y, 1.5f);
+    z = z > 0.0f ? z : 0.0f;  // and NaN -> 0
+    z = z > 3.0f ? 3.0f : z;
+    int j = (int)floorf(z);
+    j = j > 2 ? 2 : j;
+    const float frac = __fsub_rn(z, (float)j);
+    return (uint32_t)(j + (u < frac ? 1 : 0));
+}
+
+__device__ __forceinline__ int ulevel2(uint32_t c)  // 2 * {-1.5, -0.5, 0.5, 1.5}
+{
+    return 2 * (int)c - 3;
+}
+
+__device__ __forceinline__ float ulevel(uint32_t c)
+{
+    return (float)ulevel2(c) * 0.5f;
+}
+
+// Sum over the 16 lanes of this lane's half-warp, by xor-shuffles (a pairwise tree).
+__device__ __forceinline__ float half_warp_tree(float x)
+{
+#pragma unroll
+    for (int off = 1; off < 16; off <<= 1)
+        x = __fadd_rn(x, __shfl_xor_sync(0xFFFFFFFFu, x, off));
+    return x;
+}
+
+__device__ __forceinline__ int half_warp_sum(int x)
+{
+#pragma unroll
+    for (int off = 1; off < 16; off <<= 1)
+        x += __shfl_xor_sync(0xFFFFFFFFu, x, off);
+    return x;
+}
+
+// One storage block (128 values from element i0) by one warp.
+__device__ __forceinline__ void turbo_block(const TurboArgs &a, const TurboScalars &ts,
+                                            float sdec, float senc, int64_t i0, uint32_t &bad,
+                                            float &racc)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t e0 = i0 + 4 * lane;           // this lane's first element
+    const int64_t cnt = a.n - i0 < kTurboBlock ? a.n - i0 : kTurboBlock;
+    const int valid = e0 >= a.n ? 0 : (a.n - e0 >= 4 ? 4 : (int)(a.n - e0));
+    const Scalars &s = ts.s;
+    // ---- loads
+    float p[4] = {0.0f, 0.0f, 0.0f, 0.0f}, g[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    uint32_t cbyte = 0, vhalf = 0;
+    if (valid == 4) {
+        const float4 pv = *reinterpret_cast<const float4 *>(a.p + e0);
+        const float4 gv = __ldg(reinterpret_cast<const float4 *>(a.g + e0));
+        p[0] = pv.x; p[1] = pv.y; p[2] = pv.z; p[3] = pv.w;
+        g[0] = gv.x; g[1] = gv.y; g[2] = gv.z; g[3] = gv.w;
+        cbyte = a.ucode[e0 / 4];
+        vhalf = *reinterpret_cast<const uint16_t *>(a.vidx + e0 / 2);
+    } else if (valid > 0) {
+        for (int j = 0; j < valid; ++j) {
+            p[j] = a.p[e0 + j];
+            g[j] = a.g[e0 + j];
+        }
+        cbyte = a.ucode[e0 / 4];
+        vhalf = a.vidx[e0 / 2] | (valid > 2 ? (uint32_t)a.vidx[e0 / 2 + 1] << 8 : 0u);
+    }
+    const int64_t b = i0 / kTurboBlock;
+    const int lo = __half2int_rn(__ushort_as_half(a.vend[2 * b]));
+    const int hi = __half2int_rn(__ushort_as_half(a.vend[2 * b + 1]));
+    const uint32_t blo = pow2_bits(lo), bhi = pow2_bits(hi);
+    const int half = lane >> 4;  // mean block of this lane within the storage block
+    const int64_t mstart = i0 + kTurboMean * half;
+    const int mcount = mstart >= a.n ? 0 : (a.n - mstart >= kTurboMean ? kTurboMean : (int)(a.n - mstart));
+    // ---- 1. decode UState (recentred means) and 1Q; 2. the prior first moment
+    int S = 0;
+    for (int j = 0; j < valid; ++j)
+        S += ulevel2((cbyte >> (2 * j)) & 3u);
+    S = half_warp_sum(S);
+    float mu = 0.0f;
+    if (mcount > 0)
+        mu = __uint_as_float((uint32_t)a.umean[mstart / kTurboMean] << 16);
+    const float delta = mcount > 0 ? __fdiv_rn(__fmul_rn(sdec, (float)S), (float)(2 * mcount)) : 0.0f;
+    float mprev[4], vdec[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float v = q1_level(blo, bhi, (int)((vhalf >> (4 * j)) & 15u));
+        const float d = __fmul_rn(sdec, ulevel((cbyte >> (2 * j)) & 3u));
+        const float q = __fadd_rn(mu, __fsub_rn(d, delta));
+        float m = 0.0f;
+        if (ts.step > 1) {
+            const float den = __fadd_rn(__fsqrt_rn(__fdiv_rn(v, ts.bc2p)), s.ef);
+            m = __fmul_rn(__fmul_rn(q, den), ts.bc1p);
+        }
+        mprev[j] = m;
+        vdec[j] = v;
+    }
+    // ---- 3. the fp32 moments; 4. the update (the FP32 element of every mode)
+    float mn[4], vn[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const Moments o = adamw_element(p[j], g[j], mprev[j], vdec[j], s);
+        p[j] = o.p;
+        mn[j] = o.m;
+        vn[j] = o.v;
+        if (j < valid)
+            bad += any_nonfinite(o);
+    }
+    // ---- 5. recompress v with 1Q: endpoints from the block's positive values
+    uint32_t pmin = 0xFFFFFFFFu, pmax = 0u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t bits = __float_as_uint(vn[j]);
+        const bool pos = j < valid && vn[j] > 0.0f && bits < 0x7F800000u;
+        pmin = pos ? min(pmin, bits) : pmin;
+        pmax = pos ? max(pmax, bits) : pmax;
+    }
+    pmin = __reduce_min_sync(0xFFFFFFFFu, pmin);
+    pmax = __reduce_max_sync(0xFFFFFFFFu, pmax);
+    int nlo = 0, nhi = 0;
+    if (pmax != 0u) {
+        nlo = exponent_of_bits(pmin);
+        const int e = exponent_of_bits(pmax);
+        nhi = power_of_two_bits(pmax) ? e : e + 1;
+        nhi = nhi > 127 ? 127 : nhi;
+    }
+    const uint32_t nblo = pow2_bits(nlo), nbhi = pow2_bits(nhi);
+    const float mylevel = q1_level(nblo, nbhi, lane < 16 ? lane : 15);  // lane k holds level k
+    uint32_t nvhalf = 0;
+    float vhat[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float v = vn[j];
+        // largest k in 1..15 with level(k) <= v (meaningful for positive v)
+        int k = 1;
+#pragma unroll
+        for (int step = 8; step >= 1; step >>= 1) {
+            const int c = k + step;
+            const float lc = __shfl_sync(0xFFFFFFFFu, mylevel, c > 15 ? 15 : c);
+            k = (c <= 15 && lc <= v) ? c : k;
+        }
+        const float dj = __shfl_sync(0xFFFFFFFFu, mylevel, k);
+        const float dn = __shfl_sync(0xFFFFFFFFu, mylevel, k < 15 ? k + 1 : 15);
+        int idx = 0;
+        if (v > 0.0f) {
+            idx = k;
+            if (!(v == dj || k == 15)) {
+                const float frac = __fdiv_rn(__fsub_rn(v, dj), __fsub_rn(dn, dj));
+                const float u = turbo_uniform(ts.seed, ts.step, 1u, (uint64_t)(e0 + j));
+                idx = u < frac ? k + 1 : k;
+            }
+        }
+        nvhalf |= (uint32_t)idx << (4 * j);
+        vhat[j] = __shfl_sync(0xFFFFFFFFu, mylevel, idx);
+    }
+    // ---- 6. encode the next UState payload
+    float q[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if (j < valid) {
+            const float den = __fadd_rn(__fsqrt_rn(__fdiv_rn(vhat[j], s.bc2)), s.ef);
+            q[j] = __fdiv_rn(__fdiv_rn(mn[j], ts.bc1), den);
+        } else {
+            q[j] = 0.0f;  // missing positions of a short block count as 0
+        }
+    }
+    const float tree = half_warp_tree(__fadd_rn(__fadd_rn(q[0], q[1]), __fadd_rn(q[2], q[3])));
+    const float mean = mcount > 0 ? __fdiv_rn(tree, (float)mcount) : 0.0f;
+    const __nv_bfloat16 mb = __float2bfloat16_rn(mean);
+    uint16_t mbits = *reinterpret_cast<const uint16_t *>(&mb);
+    if (mean != mean)
+        mbits = 0x7FC0u;
+    const float mub = __uint_as_float((uint32_t)mbits << 16);
+    uint32_t ncbyte = cbyte;
+    float rsum = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if (j < valid) {
+            const float r = __fsub_rn(q[j], mub);
+            const uint64_t e = (uint64_t)(e0 + j);
+            float u = turbo_uniform(ts.seed, ts.step, 2u, e >> 1);
+            if (e & 1u)
+                u = __fsub_rn(1.0f, u);
+            const uint32_t c = ustate_code(r, senc, u);
+            ncbyte = (ncbyte & ~(3u << (2 * j))) | (c << (2 * j));
+            rsum = __fadd_rn(rsum, __fmul_rn(r, r));
+        }
+    }
+    // ---- stores
+    if (valid == 4) {
+        *reinterpret_cast<float4 *>(a.p + e0) = make_float4(p[0], p[1], p[2], p[3]);
+        a.ucode[e0 / 4] = (uint8_t)ncbyte;
+        *reinterpret_cast<uint16_t *>(a.vidx + e0 / 2) = (uint16_t)nvhalf;
+    } else if (valid > 0) {
+        for (int j = 0; j < valid; ++j)
+            a.p[e0 + j] = p[j];
+        a.ucode[e0 / 4] = (uint8_t)ncbyte;
+        // indices of elements past n keep their old nibbles
+        const uint32_t keep = valid >= 4 ? 0u : (0xFFFFu << (4 * valid)) & 0xFFFFu;
+        const uint32_t nv = (nvhalf & ~keep) | (vhalf & keep);
+        a.vidx[e0 / 2] = (uint8_t)nv;
+        if (valid > 2)
+            a.vidx[e0 / 2 + 1] = (uint8_t)(nv >> 8);
+    }
+    if ((lane & 15) == 0 && mcount > 0)
+        a.umean[mstart / kTurboMean] = mbits;
+    if (lane == 0) {
+        a.vend[2 * b] = __half_as_ushort(__int2half_rn(nlo));
+        a.vend[2 * b + 1] = __half_as_ushort(__int2half_rn(nhi));
+    }
+    racc = __fadd_rn(racc, rsum);
+    (void)cnt;
+}
+
+__global__ void __launch_bounds__(kTurboThreads)
+turbo_step_kernel(const TurboArgs a, const TurboScalars ts, unsigned long long *nonfinite)
+{
+    const float sdec = a.uscal[0], senc = a.uscal[1];
+    const int64_t nblocks = (a.n + kTurboBlock - 1) / kTurboBlock;
+    const int64_t warp = (int64_t)blockIdx.x * kTurboWarps + (threadIdx.x >> 5);
+    const int64_t warps = (int64_t)gridDim.x * kTurboWarps;
+    uint32_t bad = 0;
+    float racc = 0.0f;
+    for (int64_t b = warp; b < nblocks; b += warps)  // uniform per warp
+        turbo_block(a, ts, sdec, senc, b * kTurboBlock, bad, racc);
+    // the RMS accumulator: one atomic per warp
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1)
+        racc = __fadd_rn(racc, __shfl_xor_sync(0xFFFFFFFFu, racc, off));
+    if ((threadIdx.x & 31) == 0 && racc != 0.0f)
+        atomicAdd(a.uscal + 2, racc);
+    flush_nonfinite(bad, nonfinite);
+}
+
+// The finaliser: decode scale <- encode scale, encode scale <- factor *
+// sqrt(acc / n), acc <- 0.
+__global__ void turbo_finalize_kernel(float *uscal, float nf, float factor)
+{
+    if (threadIdx.x == 0 && blockIdx.x == 0) {
+        const float acc = uscal[2];
+        uscal[0] = uscal[1];
+        uscal[1] = __fmul_rn(factor, __fsqrt_rn(__fdiv_rn(acc, nf)));
+        uscal[2] = 0.0f;
+    }
+}
+
+}  // namespace pa

@@ -327,6 +327,49 @@ pa_status pa_adamw_step_packed_e4_multi_graph(const pa_tensor *list, int32_t nte
                                               int32_t *status, unsigned long long *nonfinite,
                                               pa_stream stream);
 
+/* ---------------------------------------------------------------------------
+ * TurboAdam-style step ("TurboAdam" README, turboadam 0.2.0, "How it works"):
+ * the AdamW update from FP32 transient moments, with the first moment
+ * persisted by UState (normalised Adam update units q = (m/(1-beta1^t)) /
+ * (sqrt(v_persisted/(1-beta2^t)) + eps), a 2-bit four-level code per value, a
+ * bf16 mean per 64 values, a one-step-lagged tensor scale) and the second
+ * moment by 1Q (a 4-bit index per value on a logarithmic grid between two fp16
+ * log endpoints per 128 values), both with stochastic rounding from a counter
+ * hash.  One call: decode both states, rebuild the prior first moment in the
+ * persisted second-moment frame, form m and v, update p in place, recompress
+ * v, encode the next UState payload, then rotate the scales (the page's
+ * "Fused CUDA path" and finaliser).  Readings where the page is silent (grid,
+ * levels, hash, rounding, means) are stated in the library's design notes and
+ * in csrc/turbo.cuh.
+ *
+ * pa_turbo_state (device arrays, caller-owned, all zero before the first step):
+ *   ucode  uint8[(n+3)/4]        2-bit codes, element i at bits 2*(i%4) of byte i/4
+ *   umean  uint16[(n+63)/64]     bf16 mean per 64 values
+ *   uscal  float[3]              decode scale, encode scale, RMS accumulator
+ *   vidx   uint8[(n+1)/2]        4-bit indices, element i in nibble i%2 of byte i/2
+ *   vend   uint16[2*ceil(n/128)] fp16 endpoints (lo, hi) per 128 values
+ * p, g: float[n], 16-byte aligned; umean, vidx and vend 2-byte aligned.
+ * m_step_factor: the UState scale factor (1.1 on the page); seed: the
+ * counter hash's seed (rounding for step t and element i depends only on
+ * seed, t and i).  beta1^2 < beta2 is required (the page's finite coordinate
+ * bound), else PA_ERR_ARG; so are step >= 2^22 and n > 2^40.  Other errors as
+ * for the other steps.  The RMS accumulator is a parallel float sum, so the
+ * next encode scale can differ from a sequential sum in its last bits (the
+ * page says the same of its own CUDA path); everything else is exact.
+ * ------------------------------------------------------------------------- */
+typedef struct pa_turbo_state {
+    uint8_t *ucode;
+    uint16_t *umean;
+    float *uscal;
+    uint8_t *vidx;
+    uint16_t *vend;
+} pa_turbo_state;
+
+pa_status pa_turbo_step(float *p, const float *g, int64_t n, const pa_turbo_state *state,
+                        int64_t step, double lr, double beta1, double beta2, double eps, double wd,
+                        double m_step_factor, uint64_t seed, unsigned long long *nonfinite,
+                        pa_stream stream);
+
 /* Device fault flag of the staged step kernels (current device): *code = 0
  * when no bounded wait has run out since the flag was last cleared, else 1 (the
  * copying warp found a stage still in use after 2 s), 2 (a copy had not landed

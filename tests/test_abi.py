@@ -97,6 +97,21 @@ def test_host_validation_without_gpu(lib):
                                       4, 1, *hy, None, None) == 3  # g not 16-byte aligned
     assert L.pa_encode_state(None, None, None, 0, None, None) == 0
     assert L.pa_decode_state(None, None, None, 3, None) == 1
+    # the TurboAdam-style step
+    T = lib.PaTurboState
+    st = T(0x1000, 0x2000, 0x3000, 0x4000, 0x5000)
+    sd = (1.1, ctypes.c_uint64(7), None, None)
+    assert L.pa_turbo_step(al, al, 4, ctypes.byref(st), 1, 1e-3, 0.9, 0.8, 1e-8, 0.0, *sd) == 2
+    assert b"beta1^2 < beta2" in L.pa_last_error()
+    assert L.pa_turbo_step(al, al, -1, ctypes.byref(st), 1, *hy, *sd) == 2
+    assert L.pa_turbo_step(al, al, 4, ctypes.byref(st), 1 << 22, *hy, *sd) == 2
+    assert L.pa_turbo_step(al, al, 4, ctypes.byref(st), 1, *hy, 0.0, ctypes.c_uint64(7), None,
+                           None) == 2  # scale factor
+    assert L.pa_turbo_step(al, al, 0, None, 1, *hy, *sd) == 0  # empty: no-op
+    assert L.pa_turbo_step(al, al, 4, None, 1, *hy, *sd) == 1
+    assert L.pa_turbo_step(ctypes.c_void_p(0x1004), al, 4, ctypes.byref(st), 1, *hy, *sd) == 3
+    odd = T(0x1000, 0x2001, 0x3000, 0x4000, 0x5000)
+    assert L.pa_turbo_step(al, al, 4, ctypes.byref(odd), 1, *hy, *sd) == 3
 
 
 def test_oracle_and_cuda_path_share_no_source():
