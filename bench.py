@@ -28,8 +28,9 @@ The default line (flat-7e9, packed E4, N = 1) also carries `configs`: every
 workload of the benchmark measured the same way after the headline, each with
 its own buffers, warm-up, timed steps and oracle baseline -- single-4096 (10
 steps), gpt-52 packed E4 and FP32 (100 steps each), gpt2-148 packed E4 and FP16
-(50 steps each), flat-7e9 (the headline's numbers) and the 8-bit blockwise
-mode on 1e9 parameters (20 steps).
+(50 steps each), flat-7e9 (the headline's numbers), the 8-bit blockwise
+mode on 1e9 parameters (20 steps) and the TurboAdam-style step on GPT-2
+small's 124M parameters (20 steps).
 
 --impl reference times the CPU oracle, as it stands, on this machine's cores on a
 bounded sample of the same workload (rank 0 only).
@@ -52,9 +53,14 @@ sys.path.insert(0, ROOT)
 
 import workloads as wl  # noqa: E402
 
-BYTES_PER_PARAM = {"e4": 20, "fp16": 20, "fp32": 28, "blockwise": 14 + 16 / 2048}
+# TurboAdam-style: read p, g, 2-bit codes, 4-bit indices, a bf16 mean per 64 and two
+# fp16 endpoints per 128; write all but g
+TURBO_BYTES = 4 + 4 + 0.25 + 0.5 + 2 / 64 + 4 / 128 + 4 + 0.25 + 0.5 + 2 / 64 + 4 / 128
+BYTES_PER_PARAM = {"e4": 20, "fp16": 20, "fp32": 28, "blockwise": 14 + 16 / 2048,
+                   "turbo": TURBO_BYTES}
 KERNEL_NAME = {"e4": "adamw_step_pipe_kernel<0>", "fp16": "adamw_step_pipe_kernel<1>",
-               "fp32": "adamw_step_pipe_kernel<2>", "blockwise": "blockwise8_pipe_kernel<false>"}
+               "fp32": "adamw_step_pipe_kernel<2>", "blockwise": "blockwise8_pipe_kernel<false>",
+               "turbo": "turbo_step_kernel"}
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_HBM_GBS = 6800.0
 
@@ -241,6 +247,15 @@ class Workload:
         self.n = sum(self.sizes)
         n = self.n
         f32 = torch.float32
+        if name == "turbo-124m":
+            import adamw_update_gb300 as pa
+
+            self.mode = "turbo"
+            self.p = wl.fill_normal_(torch.empty(n, dtype=f32, device=device), 0.02, seed)
+            self.g = wl.fill_turbo_grads_(torch.empty(n, dtype=f32, device=device), seed)
+            self.st = pa.turbo_state(n, device)
+            self.fresh_g = None
+            return
         if name == "blockwise-1e9":
             self.mode = mode = "blockwise"
             q1, q2 = wl.dynamic_qmap_signed(), wl.dynamic_qmap_unsigned()
@@ -293,6 +308,10 @@ def step_fn(pa, w, hy, nonfinite):
         def run(t):
             pa.pa_adamw_step_blockwise8(w.p, w.g, w.p_bf16, w.m_code, w.m_absmax, w.v_code,
                                         w.v_absmax, w.q1, w.q2, t, nonfinite=nonfinite, **hy)
+        return run
+    if w.mode == "turbo":
+        def run(t):
+            pa.pa_turbo_step(w.p, w.g, w.st, t, nonfinite=nonfinite, **hy)
         return run
     fn = {"e4": pa.pa_adamw_step_packed_e4_multi, "fp16": pa.pa_adamw_step_packed_fp16_multi,
           "fp32": pa.pa_adamw_step_fp32_multi}[w.mode]
@@ -352,10 +371,16 @@ def oracle_sample_rate(arrays, mode, seconds, threads, q=None):
     hy = wl.HYPER
     n = arrays[0].size
     passes, t0 = 0, time.perf_counter()
-    st = [a.copy() for a in arrays]
+    st = [a.copy() if isinstance(a, np.ndarray) else {k: v.copy() for k, v in a.items()}
+          for a in arrays]
     while True:
         passes += 1
-        if mode == "blockwise":
+        if mode == "turbo":  # one thread: the oracle's step is sequential
+            p, g, ts = st
+            p, ts, _ = oracle.turbo_step(p, g, ts, passes, **hy)
+            ts["uscal"] = oracle.turbo_finalize(ts["uscal"], p.size)
+            st = [p, g, ts]
+        elif mode == "blockwise":
             p, g, mc, ma, vc, va = st
             ob, mc, ma, vc, va, _ = oracle.step_blockwise8(p, g, mc, ma, vc, va, q[0], q[1],
                                                            passes, threads=threads, **hy)
@@ -380,8 +405,13 @@ def sample_size(mode, seconds, threads, total):
     rng = np.random.default_rng(0)
     p = rng.normal(0, 0.02, k).astype(np.float32)
     g = rng.normal(0, 1e-3, k).astype(np.float32)
+    if mode == "turbo":
+        k = 1 << 16
+        p, g = p[:k], g[:k]
     t0 = time.perf_counter()
-    if mode == "fp32":
+    if mode == "turbo":
+        oracle.turbo_step(p, g, oracle.turbo_zero_state(k), 1)
+    elif mode == "fp32":
         z = np.zeros(k, np.float32)
         oracle.step_fp32(p, g, z, z, 1, threads=threads)
     elif mode == "blockwise":
@@ -392,7 +422,7 @@ def sample_size(mode, seconds, threads, total):
     else:
         oracle.step_packed(p, g, np.zeros(k, np.uint32), 1, mode=mode, threads=threads)
     rate = k / max(time.perf_counter() - t0, 1e-6)
-    s = int(min(total, 1 << 27, max(1 << 20, rate * seconds)))
+    s = int(min(total, 1 << 27, max(1 << 16 if mode == "turbo" else 1 << 20, rate * seconds)))
     return (s // 2048) * 2048 if s >= 2048 else s
 
 
@@ -415,6 +445,10 @@ def sample_gradient(name, s, seed):
 
 def host_sample(w, s):
     """First s elements of the workload's inputs, as host numpy arrays."""
+    if w.mode == "turbo":
+        import oracle
+
+        return [w.p[:s].cpu().numpy(), w.g[:s].cpu().numpy(), oracle.turbo_zero_state(s)], None
     if w.mode == "blockwise":
         nb = wl.blocks(s)
         arrays = [w.p[:s].cpu().numpy(), w.g[:s].cpu().numpy(), w.m_code[:s].cpu().numpy(),
@@ -446,13 +480,17 @@ def prefix_sample(arrays, mode, s):
         nb = wl.blocks(s)
         p, g, mc, ma, vc, va = arrays
         return [p[:s], g[:s], mc[:s], ma[:nb], vc[:s], va[:nb]]
+    if mode == "turbo":
+        import oracle
+
+        return [arrays[0][:s], arrays[1][:s], oracle.turbo_zero_state(s)]
     return [a[:s] for a in arrays]
 
 
 def cpu_baseline(w, seconds):
     """The oracle on all host cores for `seconds`, then on one thread for a
     quarter of that on a prefix of the same sample."""
-    cores = host_cores()
+    cores = host_cores() if w.mode != "turbo" else 1
     s = sample_size(w.mode, seconds / 4, cores, w.n)
     arrays, q = host_sample(w, s)
     rate, n, passes = oracle_sample_rate(arrays, w.mode, seconds, cores, q)
@@ -696,6 +734,7 @@ CONFIGS = [
     ("gpt2-148", "fp16", 50),
     ("flat-7e9", "e4", None),
     ("blockwise-1e9", "blockwise", 20),
+    ("turbo-124m", "turbo", 20),
 ]
 
 
@@ -753,7 +792,11 @@ def measure_config(lib, name, mode, steps, warmup, device, cpu_seconds):
              "gb_s": gbs, "frac": gbs / peak, "peak_source": peak_kind,
              "kernel": kernel_name(w), "kernel_ms": kernel_ms,
              "kernel_ms_median": statistics.median(launch_ms), "l2": l2_policy(w, flush),
-             "gpu_launches": steps, "nonfinite": int(nonfinite.item())}
+             "gpu_launches": steps * (2 if w.mode == "turbo" else 1),
+             "nonfinite": int(nonfinite.item())}
+    if w.mode == "turbo":
+        entry["note"] = ("TurboAdam-style step (UState first moment, 1Q second moment); "
+                         "the oracle baseline runs on one thread")
     if name == "single-4096":
         entry["note"] = "launch-latency bound: the fraction of peak is not meaningful here"
     entry["cpu_baseline"] = cpu_baseline(w, cpu_seconds)
@@ -834,15 +877,16 @@ def run_reference(args):
         return
     import torch
 
-    mode = "blockwise" if args.workload == "blockwise-1e9" else args.mode
-    cores = host_cores()
+    mode = {"blockwise-1e9": "blockwise", "turbo-124m": "turbo"}.get(args.workload, args.mode)
+    cores = host_cores() if mode != "turbo" else 1
     total = tensor_sizes(args.workload)[0] if args.workload in ("flat-7e9", "blockwise-1e9") \
         else wl.WORKLOADS[args.workload]["n"]
+    g_fill = wl.fill_turbo_grads_ if mode == "turbo" else None
     budget = 150.0  # seconds for the whole run
     per_step = min(10.0, budget / max(1, args.steps + args.warmup))
     s = sample_size(mode, per_step, cores, total)
     p = wl.fill_normal_(torch.empty(s, dtype=torch.float32), 0.02, 1234)
-    g = sample_gradient(args.workload, s, 1234)
+    g = g_fill(torch.empty(s), 1234) if g_fill else sample_gradient(args.workload, s, 1234)
     p, g = p.numpy(), g.numpy()
     import oracle
 
@@ -854,12 +898,18 @@ def run_reference(args):
               np.full(s, wl.nearest_zero_code(q2), np.uint8), np.zeros(nb, np.float32)]
     elif mode == "fp32":
         st = [np.zeros(s, np.float32), np.zeros(s, np.float32)]
+    elif mode == "turbo":
+        st = [oracle.turbo_zero_state(s)]
     else:
         st = [np.zeros(s, np.uint32)]
 
     def one(t):
         nonlocal p, st
-        if mode == "blockwise":
+        if mode == "turbo":
+            p, ts, _ = oracle.turbo_step(p, g, st[0], t, **hy)
+            ts["uscal"] = oracle.turbo_finalize(ts["uscal"], s)
+            st = [ts]
+        elif mode == "blockwise":
             _, mc, ma, vc, va, _ = oracle.step_blockwise8(p, g, st[0], st[1], st[2], st[3], q1, q2,
                                                           t, threads=cores, **hy)
             st = [mc, ma, vc, va]

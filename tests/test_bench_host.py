@@ -117,7 +117,7 @@ def test_configs_cover_every_benchmark_workload(bench):
     got = {(name, mode): steps for name, mode, steps in bench.CONFIGS}
     assert got == {("single-4096", "e4"): 10, ("gpt-52", "e4"): 100, ("gpt-52", "fp32"): 100,
                    ("gpt2-148", "e4"): 50, ("gpt2-148", "fp16"): 50, ("flat-7e9", "e4"): None,
-                   ("blockwise-1e9", "blockwise"): 20}
+                   ("blockwise-1e9", "blockwise"): 20, ("turbo-124m", "turbo"): 20}
     assert {name for name, _, _ in bench.CONFIGS} == set(wl.WORKLOADS)
 
 

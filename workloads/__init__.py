@@ -22,6 +22,10 @@ The workloads (synthetic stand-ins; the pages' token tapes are not available):
                  1e-4 fraction of entries scaled by 1e4.
   blockwise-1e9  1e9 parameters for the 8-bit blockwise mode, g ~ N(0, 1e-3),
                  codes start at the map entry nearest 0 and absmax at 0.
+  turbo-124m     the TurboAdam-style step on one tensor of GPT-2 small's
+                 124,439,808 parameters (the TurboAdam page's language-model
+                 runs are GPT-2 124M), g ~ N(0, 1e-3) with half the entries
+                 scaled by 10, zero state.
 """
 from __future__ import annotations
 
@@ -69,6 +73,7 @@ WORKLOADS = {
     "gpt2-148": dict(n=sum(s for _, s in GPT2_148_SHAPES), steps=50),
     "flat-7e9": dict(n=7_000_000_000, steps=20),
     "blockwise-1e9": dict(n=1_000_000_000, steps=1),
+    "turbo-124m": dict(n=sum(s for _, s in GPT2_148_SHAPES), steps=20),
 }
 
 HYPER = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, wd=0.01)
@@ -193,3 +198,17 @@ def normal_np(n: int, std: float, seed: int) -> np.ndarray:
 
 def blocks(n: int, block: int = 2048) -> int:
     return math.ceil(n / block)
+
+
+def fill_turbo_grads_(t, seed: int, stream: int = 3):
+    """g ~ N(0, 1e-3), half the entries (a seeded coin) scaled by 10."""
+    import torch
+
+    n = t.numel()
+    for k, lo in enumerate(range(0, n, _CHUNK)):
+        hi = min(n, lo + _CHUNK)
+        g = _gen(seed, stream, k, t.device)
+        x = torch.randn(hi - lo, generator=g, device=t.device, dtype=torch.float32) * 1e-3
+        big = torch.rand(hi - lo, generator=g, device=t.device, dtype=torch.float32) < 0.5
+        t[lo:hi].copy_(torch.where(big, x * 10.0, x))
+    return t
