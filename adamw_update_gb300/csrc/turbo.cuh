@@ -145,8 +145,7 @@ __device__ __forceinline__ void turbo_block(const TurboArgs &a, const TurboScala
                                             float &racc)
 {
     const int lane = threadIdx.x & 31;
-    const int64_t e0 = i0 + 4 * lane;           // this lane's first element
-    const int64_t cnt = a.n - i0 < kTurboBlock ? a.n - i0 : kTurboBlock;
+    const int64_t e0 = i0 + 4 * lane;  // this lane's first element
     const int valid = e0 >= a.n ? 0 : (a.n - e0 >= 4 ? 4 : (int)(a.n - e0));
     const Scalars &s = ts.s;
     // ---- loads
@@ -311,10 +310,11 @@ __device__ __forceinline__ void turbo_block(const TurboArgs &a, const TurboScala
         a.vend[2 * b + 1] = __half_as_ushort(__int2half_rn(nhi));
     }
     racc = __fadd_rn(racc, rsum);
-    (void)cnt;
 }
 
-__global__ void __launch_bounds__(kTurboThreads)
+// (64 registers, four CTAs per SM: 4 % faster on GB300 than the 80 registers
+// and three CTAs the compiler picks unbounded; five CTAs lost it again.)
+__global__ void __launch_bounds__(kTurboThreads, 4)
 turbo_step_kernel(const TurboArgs a, const TurboScalars ts, unsigned long long *nonfinite)
 {
     const float sdec = a.uscal[0], senc = a.uscal[1];

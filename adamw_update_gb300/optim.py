@@ -17,6 +17,19 @@ class keeps that contract:
   ``load_state_dict()`` restores them bit for bit, so training continues exactly
   as if uninterrupted (``save_checkpoint`` / ``load_checkpoint`` write and read
   a latest-only checkpoint file atomically).
+
+Cost of moving gradients.  The step hands the library the list of (p, g,
+state) pointers; the library keeps one device descriptor table per distinct
+list (64 at most, least recently used freed first).  A list it has not seen
+costs a cudaMalloc and a synchronous upload, and past 64 lists each new one
+also a cudaFree, which waits for the device.  Gradients that move between
+steps -- ``zero_grad(set_to_none=True)``, torch's default, lets backward
+allocate new ones, which the caching allocator often but not always puts at
+the same addresses -- can therefore make a step synchronise the host.  Keep
+gradients in place (``zero_grad(set_to_none=False)``, or gradient buckets)
+to pay the upload once; in mode "e4" with up to 1024 parameters on one
+stream, ``pa_adamw_step_packed_e4_multi_noalloc`` is a step that never
+allocates or waits, whatever the pointers.
 """
 from __future__ import annotations
 

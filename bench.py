@@ -127,7 +127,8 @@ def kernel_code_digest_input() -> str:
 
     src = os.path.join(ROOT, "adamw_update_gb300", "csrc")
     out = []
-    for name in ("packedadam.cu", "codecs.cuh", "blockwise.cuh", "pipeline.cuh"):
+    for name in ("packedadam.cu", "codecs.cuh", "blockwise.cuh", "pipeline.cuh", "f32x2.cuh",
+                 "turbo.cuh"):
         with open(os.path.join(src, name)) as f:
             for line in f:
                 code = re.sub(r"//.*$", "", line).rstrip()
@@ -947,7 +948,7 @@ def run_reference(args):
 def main():
     args = parse()
     if args.params is not None:
-        if args.workload not in ("flat-7e9", "blockwise-1e9"):
+        if args.workload not in ("flat-7e9", "blockwise-1e9", "turbo-124m"):
             raise SystemExit("--params applies to the one-tensor workloads only")
         PARAMS_OVERRIDE[args.workload] = args.params
     if args.impl == "reference":

@@ -11,7 +11,8 @@ import pytest
 import workloads as wl
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-SOURCES = ("packedadam.cu", "codecs.cuh", "blockwise.cuh", "pipeline.cuh")
+SOURCES = ("packedadam.cu", "codecs.cuh", "blockwise.cuh", "pipeline.cuh", "f32x2.cuh",
+           "turbo.cuh")
 
 
 @pytest.fixture(scope="module")
