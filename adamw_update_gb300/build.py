@@ -27,7 +27,7 @@ ROOT = os.path.dirname(HERE)
 SRC = os.path.join(HERE, "csrc", "packedadam.cu")
 DEPS = [SRC, os.path.join(ROOT, "include", "packedadam.h")] + [
     os.path.join(HERE, "csrc", f) for f in ("codecs.cuh", "blockwise.cuh", "pipeline.cuh",
-                                              "f32x2.cuh", "turbo.cuh")]
+                                              "f32x2.cuh", "turbo.cuh", "exact.cuh")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-lineinfo", "-std=c++17", "-I", os.path.join(ROOT, "include"),
           "-Xcompiler", "-fPIC,-ffp-contract=off", "-shared"]

@@ -100,25 +100,25 @@ __device__ __forceinline__ void store_stream(uint32_t *a, uint4 x) { __stcs(rein
 // ---- one element of a packed step -------------------------------------------
 // Decode the prior state, v = r*r, FP32 update, encode m' and sqrt(v') into the
 // next word ("Release scope": the state is stored only after the update).
-template <int MODE, bool UNIT_BC2, bool ZS = false>
+template <int MODE, bool UNIT_BC2>
 __device__ __forceinline__ uint32_t packed_element(float &p, float g, uint32_t w,
-                                                   const Scalars &s, uint32_t &bad,
-                                                   const ZeroSafe *zs = nullptr)
+                                                   const Scalars &s, uint32_t &bad)
 {
     const float m = MODE == kE4 ? decode_m_lane(w) : decode_fp16_low(w);
     const float r = MODE == kE4 ? decode_rms_lane(w) : decode_fp16_high(w);
     float rn = 0.0f;
-    const Moments o = adamw_element<UNIT_BC2, ZS>(p, g, m, __fmul_rn(r, r), s, &rn, zs);
+    const Moments o = adamw_element<UNIT_BC2>(p, g, m, __fmul_rn(r, r), s, &rn);
     bad += any_nonfinite(o);
     p = o.p;
     if (!UNIT_BC2)
-        rn = ZS ? sqrt_zero_safe(o.v) : __fsqrt_rn(o.v);  // bc2 == 1: the update took sqrt(v')
+        rn = __fsqrt_rn(o.v);  // bc2 == 1: the update took sqrt(v')
     return MODE == kE4 ? encode_step_word_e4(o.m, o.v, rn) : encode_word_fp16(o.m, rn);
 }
 
-// Two elements of packed_element (lanes x and y) with packed arithmetic: the
-// exact rebias multiplies of the E4 decode, v = r*r and the update's multiplies
-// and adds are one instruction per pair (adamw_element2); same bits.
+// Four elements of packed_element (one staged vector) with packed arithmetic:
+// the exact rebias multiplies of the E4 decode, v = r*r and the update's
+// multiplies and adds one instruction per pair, the quotients and roots as
+// adamw_vector chooses them for the warp; same bits.  Warp-collective.
 __device__ __forceinline__ float2 decode_m_pair(uint32_t w0, uint32_t w1)
 {
     const uint32_t b0 = ((w0 & 0x7FFFu) << 12) | ((w0 & 0x8000u) << 16);
@@ -132,26 +132,38 @@ __device__ __forceinline__ float2 decode_rms_pair(uint32_t w0, uint32_t w1)
     return mul2(make_float2(__uint_as_float(b0), __uint_as_float(b1)), make_float2(0x1p112f, 0x1p112f));
 }
 
-template <int MODE, bool UNIT_BC2, bool ZS = false>
-__device__ __forceinline__ uint2 packed_element2(float2 &p, float2 g, uint32_t w0, uint32_t w1,
-                                                 const Scalars &s, const Pairs &k, uint32_t &bad,
-                                                 const ZeroSafe *zs = nullptr)
+template <int MODE, bool UNIT_BC2>
+__device__ __forceinline__ uint4 packed_vector(float pp[4], const float gg[4], const uint4 w,
+                                               const Scalars &s, const Pairs &k, const ZeroSafe &zs,
+                                               uint32_t &bad)
 {
-    const float2 m = MODE == kE4 ? decode_m_pair(w0, w1)
-                                 : make_float2(decode_fp16_low(w0), decode_fp16_low(w1));
-    const float2 r = MODE == kE4 ? decode_rms_pair(w0, w1)
-                                 : make_float2(decode_fp16_high(w0), decode_fp16_high(w1));
-    float2 rn = make_float2(0.0f, 0.0f);
-    const Moments2 o = adamw_element2<UNIT_BC2, ZS>(p, g, m, mul2(r, r), s, k, &rn, zs);
-    bad += any_nonfinite(Moments{o.p.x, o.m.x, o.v.x}) + any_nonfinite(Moments{o.p.y, o.m.y, o.v.y});
-    p = o.p;
-    if (!UNIT_BC2) {  // bc2 == 1: the update took sqrt(v')
-        rn.x = ZS ? sqrt_zero_safe(o.v.x) : __fsqrt_rn(o.v.x);
-        rn.y = ZS ? sqrt_zero_safe(o.v.y) : __fsqrt_rn(o.v.y);
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+    float2 p[2], g[2], m[2], v[2], rn[2];
+    Moments2 o[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        p[j] = make_float2(pp[2 * j], pp[2 * j + 1]);
+        g[j] = make_float2(gg[2 * j], gg[2 * j + 1]);
+        m[j] = MODE == kE4 ? decode_m_pair(ww[2 * j], ww[2 * j + 1])
+                           : make_float2(decode_fp16_low(ww[2 * j]), decode_fp16_low(ww[2 * j + 1]));
+        const float2 r = MODE == kE4 ? decode_rms_pair(ww[2 * j], ww[2 * j + 1])
+                                     : make_float2(decode_fp16_high(ww[2 * j]), decode_fp16_high(ww[2 * j + 1]));
+        v[j] = mul2(r, r);
     }
-    return MODE == kE4 ? make_uint2(encode_step_word_e4(o.m.x, o.v.x, rn.x),
-                                    encode_step_word_e4(o.m.y, o.v.y, rn.y))
-                       : make_uint2(encode_word_fp16(o.m.x, rn.x), encode_word_fp16(o.m.y, rn.y));
+    adamw_vector<UNIT_BC2, true>(p, g, m, v, s, k, zs, o, rn);
+    uint32_t out[4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        bad += any_nonfinite(Moments{o[j].p.x, o[j].m.x, o[j].v.x}) +
+               any_nonfinite(Moments{o[j].p.y, o[j].m.y, o[j].v.y});
+        pp[2 * j] = o[j].p.x;
+        pp[2 * j + 1] = o[j].p.y;
+        out[2 * j] = MODE == kE4 ? encode_step_word_e4(o[j].m.x, o[j].v.x, rn[j].x)
+                                 : encode_word_fp16(o[j].m.x, rn[j].x);
+        out[2 * j + 1] = MODE == kE4 ? encode_step_word_e4(o[j].m.y, o[j].v.y, rn[j].y)
+                                     : encode_word_fp16(o[j].m.y, rn[j].y);
+    }
+    return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
 // Element i of tensor d with 4-byte accesses (heads, tails, unaligned tensors).
@@ -498,9 +510,8 @@ __device__ __forceinline__ void pipe_produce(unsigned char *smem, uint64_t *full
 }
 
 // One staged 16-byte vector: elements e..e+3 of the stage buffer, which are
-// elements base+e.. of the tensor.  A warp with an exactly-zero gradient among
-// its lanes' elements takes the zero-safe arithmetic (same results).
-template <int MODE, bool U1, bool ZS, typename GT>
+// elements base+e.. of the tensor (warp-collective: adamw_vector).
+template <int MODE, bool U1, typename GT>
 __device__ __forceinline__ void pipe_vector_math(const unsigned char *buf, int e, const Desc &d,
                                                  int64_t base, float pp[4], const float gg[4],
                                                  const Scalars &s, const ZeroSafe &zs,
@@ -511,43 +522,31 @@ __device__ __forceinline__ void pipe_vector_math(const unsigned char *buf, int e
     if constexpr (MODE == kF32) {
         const float4 mv = *reinterpret_cast<const float4 *>(buf + L::kS1 + 4 * e);
         const float4 vv = *reinterpret_cast<const float4 *>(buf + L::kS2 + 4 * e);
-        float mm[4] = {mv.x, mv.y, mv.z, mv.w};
-        float vq[4] = {vv.x, vv.y, vv.z, vv.w};
+        const float2 p[2] = {make_float2(pp[0], pp[1]), make_float2(pp[2], pp[3])};
+        const float2 g[2] = {make_float2(gg[0], gg[1]), make_float2(gg[2], gg[3])};
+        const float2 m[2] = {make_float2(mv.x, mv.y), make_float2(mv.z, mv.w)};
+        const float2 v[2] = {make_float2(vv.x, vv.y), make_float2(vv.z, vv.w)};
+        Moments2 o[2];
+        float2 unused[2];
+        adamw_vector<U1, false>(p, g, m, v, s, k, zs, o, unused);
 #pragma unroll
-        for (int j = 0; j < 4; j += 2) {
-            const Moments2 o = adamw_element2<U1, ZS>(make_float2(pp[j], pp[j + 1]),
-                                                      make_float2(gg[j], gg[j + 1]),
-                                                      make_float2(mm[j], mm[j + 1]),
-                                                      make_float2(vq[j], vq[j + 1]), s, k, nullptr,
-                                                      &zs);
-            bad += any_nonfinite(Moments{o.p.x, o.m.x, o.v.x}) +
-                   any_nonfinite(Moments{o.p.y, o.m.y, o.v.y});
-            pp[j] = o.p.x;
-            pp[j + 1] = o.p.y;
-            mm[j] = o.m.x;
-            mm[j + 1] = o.m.y;
-            vq[j] = o.v.x;
-            vq[j + 1] = o.v.y;
+        for (int j = 0; j < 2; ++j) {
+            bad += any_nonfinite(Moments{o[j].p.x, o[j].m.x, o[j].v.x}) +
+                   any_nonfinite(Moments{o[j].p.y, o[j].m.y, o[j].v.y});
+            pp[2 * j] = o[j].p.x;
+            pp[2 * j + 1] = o[j].p.y;
         }
-        store_stream(static_cast<float *>(d.s1) + base + e, make_float4(mm[0], mm[1], mm[2], mm[3]));
-        store_stream(static_cast<float *>(d.s2) + base + e, make_float4(vq[0], vq[1], vq[2], vq[3]));
+        store_stream(static_cast<float *>(d.s1) + base + e, make_float4(o[0].m.x, o[0].m.y, o[1].m.x, o[1].m.y));
+        store_stream(static_cast<float *>(d.s2) + base + e, make_float4(o[0].v.x, o[0].v.y, o[1].v.x, o[1].v.y));
     } else {
         const uint4 wv = *reinterpret_cast<const uint4 *>(buf + L::kS1 + 4 * e);
-        float2 p01 = make_float2(pp[0], pp[1]), p23 = make_float2(pp[2], pp[3]);
-        const uint2 w01 = packed_element2<MODE, U1, ZS>(p01, make_float2(gg[0], gg[1]), wv.x, wv.y,
-                                                        s, k, bad, &zs);
-        const uint2 w23 = packed_element2<MODE, U1, ZS>(p23, make_float2(gg[2], gg[3]), wv.z, wv.w,
-                                                        s, k, bad, &zs);
-        pp[0] = p01.x;
-        pp[1] = p01.y;
-        pp[2] = p23.x;
-        pp[3] = p23.y;
-        store_stream(static_cast<uint32_t *>(d.s1) + base + e, make_uint4(w01.x, w01.y, w23.x, w23.y));
+        store_stream(static_cast<uint32_t *>(d.s1) + base + e,
+                     packed_vector<MODE, U1>(pp, gg, wv, s, k, zs, bad));
     }
 }
 
 // One staged vector whose gradients gv are already loaded.
-template <int MODE, bool U1, bool ZS, typename GT>
+template <int MODE, bool U1, typename GT>
 __device__ __forceinline__ void pipe_vector_g(const unsigned char *buf, int e, const Desc &d,
                                               int64_t base, const float4 gv, const Scalars &s,
                                               const ZeroSafe &zs, uint32_t &bad)
@@ -555,7 +554,7 @@ __device__ __forceinline__ void pipe_vector_g(const unsigned char *buf, int e, c
     const float4 pv = *reinterpret_cast<const float4 *>(buf + 4 * e);
     float pp[4] = {pv.x, pv.y, pv.z, pv.w};
     const float gg[4] = {gv.x, gv.y, gv.z, gv.w};
-    pipe_vector_math<MODE, U1, ZS, GT>(buf, e, d, base, pp, gg, s, zs, bad);
+    pipe_vector_math<MODE, U1, GT>(buf, e, d, base, pp, gg, s, zs, bad);
     store_stream(d.p + base + e, make_float4(pp[0], pp[1], pp[2], pp[3]));
 }
 
@@ -680,9 +679,10 @@ __device__ __forceinline__ void pipe_consume(const unsigned char *smem, uint64_t
             const unsigned char *buf = smem + (size_t)st * L::kStageBytes;
             // Whole tile without a zero gradient in this warp: every vector
             // on the plain path, unrolled.  Otherwise one vector at a time,
-            // each warp-vector choosing the plain or the zero-safe arithmetic
-            // (one copy of each: the E4 element is large, and more inlined
-            // copies missed in the instruction cache on GB300).
+            // each warp-vector choosing the branch-free or the zero-safe
+            // arithmetic (adamw_vector; one copy of each: the E4 element is
+            // large, and more inlined copies missed in the instruction cache
+            // on GB300).
             bool fast = sp.staged == kTile;  // uniform over the CTA
             float4 gv[kTileVecs];
             if (fast) {
@@ -712,19 +712,15 @@ __device__ __forceinline__ void pipe_consume(const unsigned char *smem, uint64_t
             } else if (fast) {
 #pragma unroll
                 for (int v = 0; v < kTileVecs; ++v)
-                    pipe_vector_g<MODE, U1, false, GT>(buf, 4 * (ct + v * kConsumers), d, sp.base,
-                                                       gv[v], s, zs, bad);
+                    pipe_vector_g<MODE, U1, GT>(buf, 4 * (ct + v * kConsumers), d, sp.base,
+                                                gv[v], s, zs, bad);
             } else {
 #pragma unroll 1
                 for (int v = 0; v < kTileVecs; ++v) {
                     const int e = 4 * (ct + v * kConsumers);
-                    if (e < sp.staged) {
-                        const float4 g = staged_grad<GT>(buf, e);
-                        if (__any_sync(__activemask(), has_zero(g)))
-                            pipe_vector_g<MODE, U1, true, GT>(buf, e, d, sp.base, g, s, zs, bad);
-                        else
-                            pipe_vector_g<MODE, U1, false, GT>(buf, e, d, sp.base, g, s, zs, bad);
-                    }
+                    if (e < sp.staged)
+                        pipe_vector_g<MODE, U1, GT>(buf, e, d, sp.base, staged_grad<GT>(buf, e), s,
+                                                    zs, bad);
                 }
             }
             // the <= 3 elements before the 16-byte body (first tile) and the

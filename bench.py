@@ -128,7 +128,7 @@ def kernel_code_digest_input() -> str:
     src = os.path.join(ROOT, "adamw_update_gb300", "csrc")
     out = []
     for name in ("packedadam.cu", "codecs.cuh", "blockwise.cuh", "pipeline.cuh", "f32x2.cuh",
-                 "turbo.cuh"):
+                 "turbo.cuh", "exact.cuh"):
         with open(os.path.join(src, name)) as f:
             for line in f:
                 code = re.sub(r"//.*$", "", line).rstrip()

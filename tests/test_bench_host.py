@@ -12,7 +12,7 @@ import workloads as wl
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SOURCES = ("packedadam.cu", "codecs.cuh", "blockwise.cuh", "pipeline.cuh", "f32x2.cuh",
-           "turbo.cuh")
+           "turbo.cuh", "exact.cuh")
 
 
 @pytest.fixture(scope="module")

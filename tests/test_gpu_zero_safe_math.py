@@ -8,7 +8,11 @@ with every 64th divisor significand (all 2^46 pairs with
 PA_EXHAUSTIVE_DIVISION=1, about 45 s on a GB300), and whole elements
 (adamw_element, zero-safe against plain) on 2^30 random elements whose
 values, scalars and hyperparameters include zeros, subnormals, extremes, Inf
-and NaN."""
+and NaN.  The per-vector path's branch-free arithmetic: the residual-corrected
+square root against __fsqrt_rn for every binary32 in [2^-100, 2^126), and
+adamw_vector (the warp's vote between the branch-free and the zero-safe
+arithmetic) against adamw_element on 2^29 elements per bias-correction case,
+with warps at the edges of the branch-free ranges; both arms must run."""
 import ctypes
 import os
 import shutil
@@ -46,3 +50,23 @@ def test_zero_safe_element_equals_plain(lib):
     assert lib.run_elements(ctypes.c_uint64(1 << 30), ctypes.c_uint64(17), ctypes.byref(count),
                             first) == 0
     assert count.value == 0, (count.value, [hex(x) for x in first])
+
+
+def test_residual_root_equals_ieee_on_its_range(lib):
+    count = ctypes.c_ulonglong(0)
+    first = (ctypes.c_uint32 * 4)()
+    assert lib.run_roots(ctypes.byref(count), first) == 0
+    assert count.value == 0, (count.value, [hex(x) for x in first])
+
+
+@pytest.mark.parametrize("unit_bc2", [0, 1])
+def test_vector_arithmetic_equals_element(lib, unit_bc2):
+    nwarps = 1 << 22
+    count = ctypes.c_ulonglong(0)
+    branch_free = ctypes.c_ulonglong(0)
+    first = (ctypes.c_uint32 * 4)()
+    assert lib.run_vectors(ctypes.c_int(unit_bc2), ctypes.c_uint64(nwarps), ctypes.c_uint64(23),
+                           ctypes.byref(count), first, ctypes.byref(branch_free)) == 0
+    assert count.value == 0, (count.value, [hex(x) for x in first])
+    # both arms ran: about half of the warps are drawn in range
+    assert nwarps // 5 < branch_free.value < nwarps * 4 // 5, branch_free.value
