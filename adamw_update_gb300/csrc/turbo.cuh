@@ -22,12 +22,15 @@
 // Design.  One warp per 128-value storage block, lane l holding values
 // 4l..4l+3 (16-byte loads of p and g; one code byte and one index half-word):
 // the block's endpoints are warp min/max reductions over the binary32 bits of
-// the positive values, the 15 grid levels live one per lane and are read by
-// shuffles in a 4-step binary search, and a mean block's pairwise tree is the
+// the positive values, the 15 levels of the old grid (decode) and of the new
+// one live one per lane and are read by shuffles (the new one in a 4-step
+// binary search), and a mean block's pairwise tree is the
 // lane's own ((q0+q1)+(q2+q3)) followed by xor-shuffles over its 16 lanes --
 // the same tree, since IEEE addition is commutative.  The RMS accumulator is
 // one float atomic per warp (its sum order is the only thing that differs
-// from a sequential evaluation).
+// from a sequential evaluation).  Whole blocks take a body without bounds
+// logic; a warp whose operands allow it takes the branch-free quotients and
+// roots described above TurboFast; each pair of elements draws one hash.
 #pragma once
 
 namespace pa {
@@ -64,12 +67,24 @@ __device__ __forceinline__ uint64_t splitmix64_mix(uint64_t z)
     return z ^ (z >> 31);
 }
 
-// u in [0, 1) on the 2^-24 grid for (step, stream, index)
-__device__ __forceinline__ float turbo_uniform(uint64_t seed, int64_t step, uint32_t stream,
-                                               uint64_t index)
+constexpr uint64_t kGolden = 0x9E3779B97F4A7C15ull;  // SplitMix64's counter increment
+
+// seed + (c + 1) * golden for the counter c of (step, stream, index): the
+// input of the mix; index + j adds j * golden (index + j < 2^40 never carries
+// into the stream and step fields)
+__device__ __forceinline__ uint64_t turbo_counter(uint64_t seed, int64_t step, uint32_t stream,
+                                                  uint64_t index)
 {
     const uint64_t c = ((uint64_t)step << 42) | ((uint64_t)stream << 40) | index;
-    const uint64_t z = splitmix64_mix(seed + (c + 1u) * 0x9E3779B97F4A7C15ull);
+    return seed + (c + 1u) * kGolden;
+}
+
+// u in [0, 1) on the 2^-24 grid: the top 24 bits of the mix of z.  The mix's
+// last step, z ^ (z >> 31), leaves bits 40..63 as they are, so it is not taken.
+__device__ __forceinline__ float turbo_uniform_of(uint64_t z)
+{
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
     return __uint2float_rn((uint32_t)(z >> 40)) * 0x1p-24f;
 }
 
@@ -100,9 +115,9 @@ __device__ __forceinline__ bool power_of_two_bits(uint32_t b)
 }
 
 // ---- UState code ------------------------------------------------------------------
-__device__ __forceinline__ uint32_t ustate_code(float r, float s, float u)
+// code of y = r / s (0 when s <= 0) with the uniform u
+__device__ __forceinline__ uint32_t ustate_code_of(float y, float u)
 {
-    const float y = s > 0.0f ? __fdiv_rn(r, s) : 0.0f;
     float z = __fadd_rn(y, 1.5f);
     z = z > 0.0f ? z : 0.0f;  // and NaN -> 0
     z = z > 3.0f ? 3.0f : z;
@@ -139,85 +154,103 @@ __device__ __forceinline__ int half_warp_sum(int x)
     return x;
 }
 
-// One storage block (128 values from element i0) by one warp.
-__device__ __forceinline__ void turbo_block(const TurboArgs &a, const TurboScalars &ts,
-                                            float sdec, float senc, int64_t i0, uint32_t &bad,
-                                            float &racc)
+// ---- branch-free quotients ----------------------------------------------------------
+// The step divides and takes roots of values whose ranges are mostly fixed per
+// storage block.  A warp replaces CUDA's correctly rounded divide and square
+// root by the exact FMA forms of exact.cuh (Markstein's corrections, the
+// residual root), same bits, where every operand lies in their ranges:
+//  * launch (TurboFast::ok): bc2, bc2p in [2^-24, 1] (bc2p only after step 1),
+//    bc1 in [2^-4, 1], ss = lr/bc1 in [2^-20, 2^20], eps in [2^-40, 2^60];
+//  * the old grid (decode): endpoints lo >= -100 and hi <= 99, so v is 0 or in
+//    [2^-100, 2^99], v/bc2p below 2^123;
+//  * the block's v' (every v' finite, the positive ones in [2^-76, 2^99]) and so
+//    the new grid [2^nlo, 2^nhi] with nlo >= -76, nhi <= 99: v'/bc2 and
+//    vhat/bc2 below 2^123, their roots in [2^-38, 2^62), den = root + eps in
+//    [2^-40, 2^63); the 1Q fraction (v - dj)/(dn - dj) has v - dj >= ulp(dj)
+//    >= 2^-99 and, the grid's levels being at most 254/14 binades apart, a
+//    quotient above 2^-43;
+//  * each lane's |m'|, which is 0 or NaN or in [2^-40, 2^40): u = ss*m' is 0 or
+//    in [2^-60, 2^60] and u/den in [2^-123, 2^120]; t = m'/bc1 in [2^-40, 2^44)
+//    and t/den in [2^-103, 2^84].  (A NaN operand gives NaN either way.)
+//  * y = r/senc (TurboFast::sok, senc in [2^-20, 2^20]): |r| < 2^86 by the
+//    bounds on t/den and on their bf16 mean, so nothing overflows; for
+//    |r| >= 2^-100 the quotient is exact, and for smaller |r| both quotients
+//    are below 2^-40 in magnitude, where RN(y + 1.5) = 1.5 for both and the
+//    code is the same.
+// Zero-signed quotients keep the dividend's sign (the divisors are positive).
+struct TurboFast {
+    float rb2, rb2p, rb1, rs;  // RN(1/bc2), RN(1/bc2p), RN(1/bc1), RN(1/senc)
+    bool ok, sok;
+};
+
+__device__ __forceinline__ TurboFast turbo_fast_of(const TurboScalars &ts, float senc)
+{
+    const Scalars &s = ts.s;
+    TurboFast f;
+    const bool b2 = s.bc2 >= 0x1p-24f && s.bc2 <= 1.0f;
+    const bool b2p = ts.step == 1 || (ts.bc2p >= 0x1p-24f && ts.bc2p <= 1.0f);
+    const bool b1 = ts.bc1 >= 0x1p-4f && ts.bc1 <= 1.0f;
+    f.ok = b2 && b2p && b1 && s.ss >= 0x1p-20f && s.ss <= 0x1p20f && s.ef >= 0x1p-40f &&
+           s.ef <= 0x1p60f;
+    f.sok = senc >= 0x1p-20f && senc <= 0x1p20f;
+    f.rb2 = reciprocal_rn(b2 ? s.bc2 : 1.0f);
+    f.rb2p = reciprocal_rn(b2p && ts.step > 1 ? ts.bc2p : 1.0f);
+    f.rb1 = reciprocal_rn(b1 ? ts.bc1 : 1.0f);
+    f.rs = reciprocal_rn(f.sok ? senc : 1.0f);
+    return f;
+}
+
+// sqrt(x / b) (rb = RN(1/b)), IEEE or branch-free
+template <bool BF>
+__device__ __forceinline__ float root_of_quotient(float x, float b, float rb)
+{
+    if (BF)
+        return sqrt_branch_free(quotient_by_reciprocal(x, b, rb));  // x = +0: +0
+    return __fsqrt_rn(__fdiv_rn(x, b));
+}
+
+// a / den for den > 0, IEEE or branch-free (the sign of a zero a kept)
+template <bool BF>
+__device__ __forceinline__ float over_den(float a, float den)
+{
+    if (BF) {
+        const float c = quotient_by_reciprocal(a, den, reciprocal_rn(den));
+        return __uint_as_float(__float_as_uint(c) | (__float_as_uint(a) & 0x80000000u));
+    }
+    return __fdiv_rn(a, den);
+}
+
+// What turbo_block carries from the moments to the recompression.
+struct TurboLane {
+    float p[4], mn[4], vn[4];
+};
+
+// The second half of a storage block (the update, 1Q and UState encode,
+// stores), with the IEEE or the branch-free quotients.
+template <bool WHOLE, bool BF>
+__device__ __forceinline__ void turbo_encode(const TurboArgs &a, const TurboScalars &ts,
+                                             const TurboFast &f, float senc, TurboLane &L,
+                                             int64_t i0, int64_t e0, int valid, int mcount,
+                                             int64_t mstart, uint32_t cbyte, uint32_t vhalf,
+                                             uint32_t pmin, uint32_t pmax, uint32_t &bad,
+                                             float &racc)
 {
     const int lane = threadIdx.x & 31;
-    const int64_t e0 = i0 + 4 * lane;  // this lane's first element
-    const int valid = e0 >= a.n ? 0 : (a.n - e0 >= 4 ? 4 : (int)(a.n - e0));
     const Scalars &s = ts.s;
-    // ---- loads
-    float p[4] = {0.0f, 0.0f, 0.0f, 0.0f}, g[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    uint32_t cbyte = 0, vhalf = 0;
-    if (valid == 4) {
-        const float4 pv = *reinterpret_cast<const float4 *>(a.p + e0);
-        const float4 gv = __ldg(reinterpret_cast<const float4 *>(a.g + e0));
-        p[0] = pv.x; p[1] = pv.y; p[2] = pv.z; p[3] = pv.w;
-        g[0] = gv.x; g[1] = gv.y; g[2] = gv.z; g[3] = gv.w;
-        cbyte = a.ucode[e0 / 4];
-        vhalf = *reinterpret_cast<const uint16_t *>(a.vidx + e0 / 2);
-    } else if (valid > 0) {
-        for (int j = 0; j < valid; ++j) {
-            p[j] = a.p[e0 + j];
-            g[j] = a.g[e0 + j];
-        }
-        cbyte = a.ucode[e0 / 4];
-        vhalf = a.vidx[e0 / 2] | (valid > 2 ? (uint32_t)a.vidx[e0 / 2 + 1] << 8 : 0u);
-    }
-    const int64_t b = i0 / kTurboBlock;
-    const int lo = __half2int_rn(__ushort_as_half(a.vend[2 * b]));
-    const int hi = __half2int_rn(__ushort_as_half(a.vend[2 * b + 1]));
-    const uint32_t blo = pow2_bits(lo), bhi = pow2_bits(hi);
-    const int half = lane >> 4;  // mean block of this lane within the storage block
-    const int64_t mstart = i0 + kTurboMean * half;
-    const int mcount = mstart >= a.n ? 0 : (a.n - mstart >= kTurboMean ? kTurboMean : (int)(a.n - mstart));
-    // ---- 1. decode UState (recentred means) and 1Q; 2. the prior first moment
-    int S = 0;
-    for (int j = 0; j < valid; ++j)
-        S += ulevel2((cbyte >> (2 * j)) & 3u);
-    S = half_warp_sum(S);
-    float mu = 0.0f;
-    if (mcount > 0)
-        mu = __uint_as_float((uint32_t)a.umean[mstart / kTurboMean] << 16);
-    const float delta = mcount > 0 ? __fdiv_rn(__fmul_rn(sdec, (float)S), (float)(2 * mcount)) : 0.0f;
-    float mprev[4], vdec[4];
+    // ---- 4. the update (the FP32 element of every mode)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const float v = q1_level(blo, bhi, (int)((vhalf >> (4 * j)) & 15u));
-        const float d = __fmul_rn(sdec, ulevel((cbyte >> (2 * j)) & 3u));
-        const float q = __fadd_rn(mu, __fsub_rn(d, delta));
-        float m = 0.0f;
-        if (ts.step > 1) {
-            const float den = __fadd_rn(__fsqrt_rn(__fdiv_rn(v, ts.bc2p)), s.ef);
-            m = __fmul_rn(__fmul_rn(q, den), ts.bc1p);
-        }
-        mprev[j] = m;
-        vdec[j] = v;
-    }
-    // ---- 3. the fp32 moments; 4. the update (the FP32 element of every mode)
-    float mn[4], vn[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const Moments o = adamw_element(p[j], g[j], mprev[j], vdec[j], s);
-        p[j] = o.p;
-        mn[j] = o.m;
-        vn[j] = o.v;
-        if (j < valid)
-            bad += any_nonfinite(o);
+        const float den = __fadd_rn(root_of_quotient<BF>(L.vn[j], s.bc2, f.rb2), s.ef);
+        const float nupd = over_den<BF>(__fmul_rn(-s.ss, L.mn[j]), den);
+#ifndef PA_FAST_MATH
+        L.p[j] = __fadd_rn(__fmul_rn(L.p[j], s.dk), nupd);
+#else
+        L.p[j] = __fmaf_rn(L.p[j], s.dk, nupd);  // as adamw_element in this build
+#endif
+        if (WHOLE || j < valid)
+            bad += any_nonfinite(Moments{L.p[j], L.mn[j], L.vn[j]});
     }
     // ---- 5. recompress v with 1Q: endpoints from the block's positive values
-    uint32_t pmin = 0xFFFFFFFFu, pmax = 0u;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const uint32_t bits = __float_as_uint(vn[j]);
-        const bool pos = j < valid && vn[j] > 0.0f && bits < 0x7F800000u;
-        pmin = pos ? min(pmin, bits) : pmin;
-        pmax = pos ? max(pmax, bits) : pmax;
-    }
-    pmin = __reduce_min_sync(0xFFFFFFFFu, pmin);
-    pmax = __reduce_max_sync(0xFFFFFFFFu, pmax);
     int nlo = 0, nhi = 0;
     if (pmax != 0u) {
         nlo = exponent_of_bits(pmin);
@@ -227,11 +260,12 @@ __device__ __forceinline__ void turbo_block(const TurboArgs &a, const TurboScala
     }
     const uint32_t nblo = pow2_bits(nlo), nbhi = pow2_bits(nhi);
     const float mylevel = q1_level(nblo, nbhi, lane < 16 ? lane : 15);  // lane k holds level k
+    const uint64_t z1 = turbo_counter(ts.seed, ts.step, 1u, (uint64_t)e0);
     uint32_t nvhalf = 0;
     float vhat[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const float v = vn[j];
+        const float v = L.vn[j];
         // largest k in 1..15 with level(k) <= v (meaningful for positive v)
         int k = 1;
 #pragma unroll
@@ -246,8 +280,10 @@ __device__ __forceinline__ void turbo_block(const TurboArgs &a, const TurboScala
         if (v > 0.0f) {
             idx = k;
             if (!(v == dj || k == 15)) {
-                const float frac = __fdiv_rn(__fsub_rn(v, dj), __fsub_rn(dn, dj));
-                const float u = turbo_uniform(ts.seed, ts.step, 1u, (uint64_t)(e0 + j));
+                const float b = __fsub_rn(dn, dj);
+                const float frac = BF ? quotient_by_reciprocal(__fsub_rn(v, dj), b, reciprocal_rn(b))
+                                      : __fdiv_rn(__fsub_rn(v, dj), b);
+                const float u = turbo_uniform_of(z1 + (uint64_t)j * kGolden);
                 idx = u < frac ? k + 1 : k;
             }
         }
@@ -258,43 +294,53 @@ __device__ __forceinline__ void turbo_block(const TurboArgs &a, const TurboScala
     float q[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        if (j < valid) {
-            const float den = __fadd_rn(__fsqrt_rn(__fdiv_rn(vhat[j], s.bc2)), s.ef);
-            q[j] = __fdiv_rn(__fdiv_rn(mn[j], ts.bc1), den);
+        if (WHOLE || j < valid) {
+            const float den = __fadd_rn(root_of_quotient<BF>(vhat[j], s.bc2, f.rb2), s.ef);
+            const float t = BF ? __uint_as_float(__float_as_uint(quotient_by_reciprocal(L.mn[j], ts.bc1, f.rb1)) |
+                                                 (__float_as_uint(L.mn[j]) & 0x80000000u))
+                               : __fdiv_rn(L.mn[j], ts.bc1);
+            q[j] = over_den<BF>(t, den);
         } else {
             q[j] = 0.0f;  // missing positions of a short block count as 0
         }
     }
     const float tree = half_warp_tree(__fadd_rn(__fadd_rn(q[0], q[1]), __fadd_rn(q[2], q[3])));
-    const float mean = mcount > 0 ? __fdiv_rn(tree, (float)mcount) : 0.0f;
+    // (dividing by 64 = multiplying by 2^-6: the same rounded result)
+    const float mean = WHOLE ? __fmul_rn(tree, 0x1p-6f)
+                             : (mcount > 0 ? __fdiv_rn(tree, (float)mcount) : 0.0f);
     const __nv_bfloat16 mb = __float2bfloat16_rn(mean);
     uint16_t mbits = *reinterpret_cast<const uint16_t *>(&mb);
     if (mean != mean)
         mbits = 0x7FC0u;
     const float mub = __uint_as_float((uint32_t)mbits << 16);
+    // antithetic pairs (2k, 2k+1) share u and 1-u; e0 is a multiple of 4
+    const uint64_t z2 = turbo_counter(ts.seed, ts.step, 2u, (uint64_t)e0 >> 1);
+    const float upair[2] = {turbo_uniform_of(z2), turbo_uniform_of(z2 + kGolden)};
     uint32_t ncbyte = cbyte;
     float rsum = 0.0f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        if (j < valid) {
+        if (WHOLE || j < valid) {
             const float r = __fsub_rn(q[j], mub);
-            const uint64_t e = (uint64_t)(e0 + j);
-            float u = turbo_uniform(ts.seed, ts.step, 2u, e >> 1);
-            if (e & 1u)
-                u = __fsub_rn(1.0f, u);
-            const uint32_t c = ustate_code(r, senc, u);
+            const float u = (j & 1) ? __fsub_rn(1.0f, upair[j >> 1]) : upair[j >> 1];
+            float y;
+            if (BF && f.sok)  // uniform over the launch (|r| < 2^86 needs the BF bounds)
+                y = quotient_by_reciprocal(r, senc, f.rs);
+            else
+                y = senc > 0.0f ? __fdiv_rn(r, senc) : 0.0f;
+            const uint32_t c = ustate_code_of(y, u);
             ncbyte = (ncbyte & ~(3u << (2 * j))) | (c << (2 * j));
             rsum = __fadd_rn(rsum, __fmul_rn(r, r));
         }
     }
     // ---- stores
-    if (valid == 4) {
-        *reinterpret_cast<float4 *>(a.p + e0) = make_float4(p[0], p[1], p[2], p[3]);
+    if (WHOLE || valid == 4) {
+        *reinterpret_cast<float4 *>(a.p + e0) = make_float4(L.p[0], L.p[1], L.p[2], L.p[3]);
         a.ucode[e0 / 4] = (uint8_t)ncbyte;
         *reinterpret_cast<uint16_t *>(a.vidx + e0 / 2) = (uint16_t)nvhalf;
     } else if (valid > 0) {
         for (int j = 0; j < valid; ++j)
-            a.p[e0 + j] = p[j];
+            a.p[e0 + j] = L.p[j];
         a.ucode[e0 / 4] = (uint8_t)ncbyte;
         // indices of elements past n keep their old nibbles
         const uint32_t keep = valid >= 4 ? 0u : (0xFFFFu << (4 * valid)) & 0xFFFFu;
@@ -303,13 +349,116 @@ __device__ __forceinline__ void turbo_block(const TurboArgs &a, const TurboScala
         if (valid > 2)
             a.vidx[e0 / 2 + 1] = (uint8_t)(nv >> 8);
     }
-    if ((lane & 15) == 0 && mcount > 0)
+    if ((lane & 15) == 0 && (WHOLE || mcount > 0))
         a.umean[mstart / kTurboMean] = mbits;
     if (lane == 0) {
+        const int64_t b = i0 / kTurboBlock;
         a.vend[2 * b] = __half_as_ushort(__int2half_rn(nlo));
         a.vend[2 * b + 1] = __half_as_ushort(__int2half_rn(nhi));
     }
     racc = __fadd_rn(racc, rsum);
+}
+
+// One storage block (128 values from element i0) by one warp.  WHOLE: all 128
+// values lie below n.
+template <bool WHOLE>
+__device__ __forceinline__ void turbo_block(const TurboArgs &a, const TurboScalars &ts,
+                                            const TurboFast &f, float sdec, float senc, int64_t i0,
+                                            uint32_t &bad, float &racc)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t e0 = i0 + 4 * lane;  // this lane's first element
+    const int valid = WHOLE ? 4 : (e0 >= a.n ? 0 : (a.n - e0 >= 4 ? 4 : (int)(a.n - e0)));
+    const Scalars &s = ts.s;
+    TurboLane L;
+    // ---- loads
+    float g[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    uint32_t cbyte = 0, vhalf = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        L.p[j] = 0.0f;
+    if (WHOLE || valid == 4) {
+        const float4 pv = *reinterpret_cast<const float4 *>(a.p + e0);
+        const float4 gv = __ldg(reinterpret_cast<const float4 *>(a.g + e0));
+        L.p[0] = pv.x; L.p[1] = pv.y; L.p[2] = pv.z; L.p[3] = pv.w;
+        g[0] = gv.x; g[1] = gv.y; g[2] = gv.z; g[3] = gv.w;
+        cbyte = a.ucode[e0 / 4];
+        vhalf = *reinterpret_cast<const uint16_t *>(a.vidx + e0 / 2);
+    } else if (valid > 0) {
+        for (int j = 0; j < valid; ++j) {
+            L.p[j] = a.p[e0 + j];
+            g[j] = a.g[e0 + j];
+        }
+        cbyte = a.ucode[e0 / 4];
+        vhalf = a.vidx[e0 / 2] | (valid > 2 ? (uint32_t)a.vidx[e0 / 2 + 1] << 8 : 0u);
+    }
+    const int64_t b = i0 / kTurboBlock;
+    const int lo = __half2int_rn(__ushort_as_half(a.vend[2 * b]));
+    const int hi = __half2int_rn(__ushort_as_half(a.vend[2 * b + 1]));
+    const uint32_t blo = pow2_bits(lo), bhi = pow2_bits(hi);
+    const int half = lane >> 4;  // mean block of this lane within the storage block
+    const int64_t mstart = i0 + kTurboMean * half;
+    const int mcount = WHOLE ? kTurboMean
+                             : (mstart >= a.n ? 0 : (a.n - mstart >= kTurboMean ? kTurboMean : (int)(a.n - mstart)));
+    // ---- 1. decode UState (recentred means) and 1Q (lane k holds old level k);
+    //      2. the prior first moment
+    int S = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        if (WHOLE || j < valid)
+            S += ulevel2((cbyte >> (2 * j)) & 3u);
+    S = half_warp_sum(S);
+    float mu = 0.0f;
+    if (WHOLE || mcount > 0)
+        mu = __uint_as_float((uint32_t)a.umean[mstart / kTurboMean] << 16);
+    const float delta = WHOLE ? __fmul_rn(__fmul_rn(sdec, (float)S), 0x1p-7f)  // / 128
+                              : (mcount > 0 ? __fdiv_rn(__fmul_rn(sdec, (float)S), (float)(2 * mcount)) : 0.0f);
+    const float oldlevel = q1_level(blo, bhi, lane < 16 ? lane : 15);
+    const bool old_bf = f.ok && lo >= -100 && hi <= 99;  // uniform over the warp
+    float mprev[4], vdec[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float v = __shfl_sync(0xFFFFFFFFu, oldlevel, (int)((vhalf >> (4 * j)) & 15u));
+        const float d = __fmul_rn(sdec, ulevel((cbyte >> (2 * j)) & 3u));
+        const float q = __fadd_rn(mu, __fsub_rn(d, delta));
+        float m = 0.0f;
+        if (ts.step > 1) {
+            const float root = old_bf ? root_of_quotient<true>(v, ts.bc2p, f.rb2p)
+                                      : root_of_quotient<false>(v, ts.bc2p, f.rb2p);
+            m = __fmul_rn(__fmul_rn(q, __fadd_rn(root, s.ef)), ts.bc1p);
+        }
+        mprev[j] = m;
+        vdec[j] = v;
+    }
+    // ---- 3. the fp32 moments; the block's v' range; each lane's |m'| range
+    uint32_t pmin = 0xFFFFFFFFu, pmax = 0u, vall = 0u;
+    float mlo = INFINITY, mhi = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        L.mn[j] = __fadd_rn(__fmul_rn(s.b1, mprev[j]), __fmul_rn(s.c1, g[j]));
+        L.vn[j] = __fadd_rn(__fmul_rn(s.b2, vdec[j]), __fmul_rn(__fmul_rn(s.c2, g[j]), g[j]));
+        const uint32_t bits = __float_as_uint(L.vn[j]);
+        if (WHOLE || j < valid) {
+            const bool pos = L.vn[j] > 0.0f && bits < 0x7F800000u;
+            pmin = pos ? min(pmin, bits) : pmin;
+            pmax = pos ? max(pmax, bits) : pmax;
+            vall = max(vall, bits);
+            mlo = fminf(mlo, fabsf(L.mn[j]));  // NaN ignored (NaN is NaN either way)
+            mhi = fmaxf(mhi, fabsf(L.mn[j]));
+        }
+    }
+    pmin = __reduce_min_sync(0xFFFFFFFFu, pmin);
+    pmax = __reduce_max_sync(0xFFFFFFFFu, pmax);
+    vall = __reduce_max_sync(0xFFFFFFFFu, vall);
+    // positive v' in [2^-76, 2^99], none non-finite or negative; |m'| range
+    const bool lane_ok = f.ok && (pmax == 0u || (pmin >= 0x19800000u && pmax <= 0x71000000u)) &&
+                         vall <= 0x71000000u && mlo >= 0x1p-40f && mhi < 0x1p40f;
+    if (__all_sync(0xFFFFFFFFu, lane_ok))
+        turbo_encode<WHOLE, true>(a, ts, f, senc, L, i0, e0, valid, mcount, mstart, cbyte, vhalf,
+                                  pmin, pmax, bad, racc);
+    else
+        turbo_encode<WHOLE, false>(a, ts, f, senc, L, i0, e0, valid, mcount, mstart, cbyte, vhalf,
+                                   pmin, pmax, bad, racc);
 }
 
 // (64 registers, four CTAs per SM: 4 % faster on GB300 than the 80 registers
@@ -321,10 +470,15 @@ turbo_step_kernel(const TurboArgs a, const TurboScalars ts, unsigned long long *
     const int64_t nblocks = (a.n + kTurboBlock - 1) / kTurboBlock;
     const int64_t warp = (int64_t)blockIdx.x * kTurboWarps + (threadIdx.x >> 5);
     const int64_t warps = (int64_t)gridDim.x * kTurboWarps;
+    const TurboFast f = turbo_fast_of(ts, senc);
     uint32_t bad = 0;
     float racc = 0.0f;
-    for (int64_t b = warp; b < nblocks; b += warps)  // uniform per warp
-        turbo_block(a, ts, sdec, senc, b * kTurboBlock, bad, racc);
+    for (int64_t b = warp; b < nblocks; b += warps) {  // uniform per warp
+        if ((b + 1) * kTurboBlock <= a.n)
+            turbo_block<true>(a, ts, f, sdec, senc, b * kTurboBlock, bad, racc);
+        else
+            turbo_block<false>(a, ts, f, sdec, senc, b * kTurboBlock, bad, racc);
+    }
     // the RMS accumulator: one atomic per warp
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1)

@@ -99,7 +99,8 @@ __global__ void reciprocal_all(unsigned long long *count, uint32_t *first)
     }
 }
 
-// whole codes as the requantiser forms them, against count_below(IEEE quotient)
+// whole codes as the requantiser forms them (pairs of quotients, zeros as +0),
+// against count_below(IEEE quotient)
 __global__ void codes_random(const float *qmap, uint64_t n, uint64_t seed, unsigned long long *count,
                              uint32_t *first)
 {
@@ -124,15 +125,22 @@ __global__ void codes_random(const float *qmap, uint64_t n, uint64_t seed, unsig
         if ((r2 & 0xFFu) == 0u) xb = 0u;
         xb |= r2 & 0x80000000u;
         const float x = __uint_as_float(xb), s = __uint_as_float(sb);
-        uint32_t got;
-        if (fabsf(x) < __uint_as_float(fast_quotient_floor(sb)) && needs_ieee_divide(x, fast_quotient_floor(sb)))
-            got = (uint32_t)count_below(mid, __fdiv_rn(x, s));
-        else
-            got = k <= 2 ? code_by_bucket<2>(mid, table, divide_by_scale_fma(x, s, reciprocal_rn(s)), k)
-                         : code_by_bucket<0>(mid, table, divide_by_scale_fma(x, s, reciprocal_rn(s)), k);
-        const uint32_t want = (uint32_t)count_below(mid, __fdiv_rn(x, s));
-        if (got != want)
-            note(count, first, xb, sb, got, want);
+        // the pair form, x beside a second value of the same block (|x'| <= scale)
+        const float x2 = __uint_as_float((r2 >> 8) % (sb + 1u) | (r0 & 0x80000000u));
+        const float2 c = divide_pair_for_code(make_float2(x, x2), make_float2(-s, -s),
+                                              make_float2(reciprocal_rn(s), reciprocal_rn(s)));
+        const float xs[2] = {x, x2}, cs[2] = {c.x, c.y};
+        for (int j = 0; j < 2; ++j) {
+            uint32_t got;
+            if (fabsf(xs[j]) < __uint_as_float(fast_quotient_floor(sb)) &&
+                needs_ieee_divide(xs[j], fast_quotient_floor(sb)))
+                got = (uint32_t)count_below(mid, __fdiv_rn(xs[j], s));
+            else
+                got = k <= 2 ? code_by_bucket<2>(mid, table, cs[j], k) : code_by_bucket<0>(mid, table, cs[j], k);
+            const uint32_t want = (uint32_t)count_below(mid, __fdiv_rn(xs[j], s));
+            if (got != want)
+                note(count, first, __float_as_uint(xs[j]), sb, got, want);
+        }
     }
 }
 
