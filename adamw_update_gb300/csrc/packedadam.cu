@@ -583,28 +583,35 @@ __device__ __forceinline__ RegVec<MODE> load_vec(const unsigned char *buf, int e
     return r;
 }
 
-// (One element at a time: packed pairs here measured 1.3 % slower on the
-// 7e9-parameter flat workload, all of whose tiles take this path, though 3 %
-// faster on 2^28 parameters; the per-vector paths below keep the pairs.)
+// The FP32 mode takes adamw_vector (packed pairs, the warp's vote for the
+// branch-free quotients): on GB300 3 % faster than one element at a time on
+// the gpt-52 list.  The packed modes keep one element at a time with the IEEE
+// arithmetic: adamw_vector here measured 2.6 % slower on the 7e9-parameter
+// flat workload, all of whose tiles take this path.
 template <int MODE, bool U1>
 __device__ __forceinline__ void compute_vec(const RegVec<MODE> &r, int e, const Desc &d,
-                                            int64_t base, const Scalars &s, uint32_t &bad)
+                                            int64_t base, const Scalars &s, const ZeroSafe &zs,
+                                            uint32_t &bad)
 {
     float pp[4] = {r.p.x, r.p.y, r.p.z, r.p.w};
     const float gg[4] = {r.g.x, r.g.y, r.g.z, r.g.w};
     if constexpr (MODE == kF32) {
-        float mm[4] = {r.m.x, r.m.y, r.m.z, r.m.w};
-        float vq[4] = {r.v.x, r.v.y, r.v.z, r.v.w};
+        const float2 p[2] = {make_float2(pp[0], pp[1]), make_float2(pp[2], pp[3])};
+        const float2 g[2] = {make_float2(gg[0], gg[1]), make_float2(gg[2], gg[3])};
+        const float2 m[2] = {make_float2(r.m.x, r.m.y), make_float2(r.m.z, r.m.w)};
+        const float2 v[2] = {make_float2(r.v.x, r.v.y), make_float2(r.v.z, r.v.w)};
+        Moments2 o[2];
+        float2 unused[2];
+        adamw_vector<U1, false>(p, g, m, v, s, pairs_of(s), zs, o, unused);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const Moments o = adamw_element<U1>(pp[j], gg[j], mm[j], vq[j], s);
-            bad += any_nonfinite(o);
-            pp[j] = o.p;
-            mm[j] = o.m;
-            vq[j] = o.v;
+        for (int j = 0; j < 2; ++j) {
+            bad += any_nonfinite(Moments{o[j].p.x, o[j].m.x, o[j].v.x}) +
+                   any_nonfinite(Moments{o[j].p.y, o[j].m.y, o[j].v.y});
+            pp[2 * j] = o[j].p.x;
+            pp[2 * j + 1] = o[j].p.y;
         }
-        store_stream(static_cast<float *>(d.s1) + base + e, make_float4(mm[0], mm[1], mm[2], mm[3]));
-        store_stream(static_cast<float *>(d.s2) + base + e, make_float4(vq[0], vq[1], vq[2], vq[3]));
+        store_stream(static_cast<float *>(d.s1) + base + e, make_float4(o[0].m.x, o[0].m.y, o[1].m.x, o[1].m.y));
+        store_stream(static_cast<float *>(d.s2) + base + e, make_float4(o[0].v.x, o[0].v.y, o[1].v.x, o[1].v.y));
     } else {
         uint32_t ww[4] = {r.w.x, r.w.y, r.w.z, r.w.w};
 #pragma unroll
@@ -682,7 +689,9 @@ __device__ __forceinline__ void pipe_consume(const unsigned char *smem, uint64_t
             // each warp-vector choosing the branch-free or the zero-safe
             // arithmetic (adamw_vector; one copy of each: the E4 element is
             // large, and more inlined copies missed in the instruction cache
-            // on GB300).
+            // on GB300).  (Whole tiles of a runtime size below kTile, with the
+            // vectors past the tile's end skipped, measured 3-9 % slower on
+            // GB300 everywhere, also at kTile.)
             bool fast = sp.staged == kTile;  // uniform over the CTA
             float4 gv[kTileVecs];
             if (fast) {
@@ -708,7 +717,7 @@ __device__ __forceinline__ void pipe_consume(const unsigned char *smem, uint64_t
                 released = true;
 #pragma unroll
                 for (int v = 0; v < kTileVecs; ++v)
-                    compute_vec<MODE, U1>(rv[v], 4 * (ct + v * kConsumers), d, sp.base, s, bad);
+                    compute_vec<MODE, U1>(rv[v], 4 * (ct + v * kConsumers), d, sp.base, s, zs, bad);
             } else if (fast) {
 #pragma unroll
                 for (int v = 0; v < kTileVecs; ++v)

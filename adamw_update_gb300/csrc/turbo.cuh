@@ -155,20 +155,20 @@ __device__ __forceinline__ int half_warp_sum(int x)
 }
 
 // ---- branch-free quotients ----------------------------------------------------------
-// The step divides and takes roots of values whose ranges are mostly fixed per
-// storage block.  A warp replaces CUDA's correctly rounded divide and square
-// root by the exact FMA forms of exact.cuh (Markstein's corrections, the
-// residual root), same bits, where every operand lies in their ranges:
-//  * launch (TurboFast::ok): bc2, bc2p in [2^-24, 1] (bc2p only after step 1),
-//    bc1 in [2^-4, 1], ss = lr/bc1 in [2^-20, 2^20], eps in [2^-40, 2^60];
-//  * the old grid (decode): endpoints lo >= -100 and hi <= 99, so v is 0 or in
-//    [2^-100, 2^99], v/bc2p below 2^123;
+// The denominators sqrt(level / bc2p) + eps (decode) and sqrt(level / bc2) +
+// eps (encode) depend only on a grid level, so each lane forms the one of its
+// level with the IEEE operations and elements fetch theirs by shuffle.  For
+// the rest a warp replaces CUDA's correctly rounded divide and square root by
+// the exact FMA forms of exact.cuh (Markstein's corrections, the residual
+// root), same bits, where every operand lies in their ranges:
+//  * launch (TurboFast::ok): bc2 in [2^-24, 1], bc1 in [2^-4, 1],
+//    ss = lr/bc1 in [2^-20, 2^20], eps in [2^-40, 2^60];
 //  * the block's v' (every v' finite, the positive ones in [2^-76, 2^99]) and so
-//    the new grid [2^nlo, 2^nhi] with nlo >= -76, nhi <= 99: v'/bc2 and
-//    vhat/bc2 below 2^123, their roots in [2^-38, 2^62), den = root + eps in
-//    [2^-40, 2^63); the 1Q fraction (v - dj)/(dn - dj) has v - dj >= ulp(dj)
-//    >= 2^-99 and, the grid's levels being at most 254/14 binades apart, a
-//    quotient above 2^-43;
+//    the new grid [2^nlo, 2^nhi] with nlo >= -76, nhi <= 99: v'/bc2 below
+//    2^123, its root in [2^-38, 2^62), den = root + eps in [2^-40, 2^63), the
+//    encode's denominators in the same range; the 1Q fraction
+//    (v - dj)/(dn - dj) has v - dj >= ulp(dj) >= 2^-99 and, the grid's levels
+//    being at most 254/14 binades apart, a quotient above 2^-43;
 //  * each lane's |m'|, which is 0 or NaN or in [2^-40, 2^40): u = ss*m' is 0 or
 //    in [2^-60, 2^60] and u/den in [2^-123, 2^120]; t = m'/bc1 in [2^-40, 2^44)
 //    and t/den in [2^-103, 2^84].  (A NaN operand gives NaN either way.)
@@ -179,7 +179,7 @@ __device__ __forceinline__ int half_warp_sum(int x)
 //    code is the same.
 // Zero-signed quotients keep the dividend's sign (the divisors are positive).
 struct TurboFast {
-    float rb2, rb2p, rb1, rs;  // RN(1/bc2), RN(1/bc2p), RN(1/bc1), RN(1/senc)
+    float rb2, rb1, rs;  // RN(1/bc2), RN(1/bc1), RN(1/senc)
     bool ok, sok;
 };
 
@@ -188,13 +188,10 @@ __device__ __forceinline__ TurboFast turbo_fast_of(const TurboScalars &ts, float
     const Scalars &s = ts.s;
     TurboFast f;
     const bool b2 = s.bc2 >= 0x1p-24f && s.bc2 <= 1.0f;
-    const bool b2p = ts.step == 1 || (ts.bc2p >= 0x1p-24f && ts.bc2p <= 1.0f);
     const bool b1 = ts.bc1 >= 0x1p-4f && ts.bc1 <= 1.0f;
-    f.ok = b2 && b2p && b1 && s.ss >= 0x1p-20f && s.ss <= 0x1p20f && s.ef >= 0x1p-40f &&
-           s.ef <= 0x1p60f;
+    f.ok = b2 && b1 && s.ss >= 0x1p-20f && s.ss <= 0x1p20f && s.ef >= 0x1p-40f && s.ef <= 0x1p60f;
     f.sok = senc >= 0x1p-20f && senc <= 0x1p20f;
     f.rb2 = reciprocal_rn(b2 ? s.bc2 : 1.0f);
-    f.rb2p = reciprocal_rn(b2p && ts.step > 1 ? ts.bc2p : 1.0f);
     f.rb1 = reciprocal_rn(b1 ? ts.bc1 : 1.0f);
     f.rs = reciprocal_rn(f.sok ? senc : 1.0f);
     return f;
@@ -259,20 +256,23 @@ __device__ __forceinline__ void turbo_encode(const TurboArgs &a, const TurboScal
         nhi = nhi > 127 ? 127 : nhi;
     }
     const uint32_t nblo = pow2_bits(nlo), nbhi = pow2_bits(nhi);
-    const float mylevel = q1_level(nblo, nbhi, lane < 16 ? lane : 15);  // lane k holds level k
+    // lane k holds level k of the new grid and the encode's denominator for it,
+    // sqrt(level / bc2) + eps (the same value for every element that takes it)
+    const float mylevel = q1_level(nblo, nbhi, lane < 16 ? lane : 15);
+    const float myden = __fadd_rn(__fsqrt_rn(__fdiv_rn(mylevel, s.bc2)), s.ef);
     const uint64_t z1 = turbo_counter(ts.seed, ts.step, 1u, (uint64_t)e0);
     uint32_t nvhalf = 0;
-    float vhat[4];
+    float den5[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const float v = L.vn[j];
-        // largest k in 1..15 with level(k) <= v (meaningful for positive v)
-        int k = 1;
+        // k = the number of levels 1..15 at most v: for positive v (>= level
+        // 1) the largest such level; the probes stay within 1..15
+        int k = 0;
 #pragma unroll
         for (int step = 8; step >= 1; step >>= 1) {
             const int c = k + step;
-            const float lc = __shfl_sync(0xFFFFFFFFu, mylevel, c > 15 ? 15 : c);
-            k = (c <= 15 && lc <= v) ? c : k;
+            k = __shfl_sync(0xFFFFFFFFu, mylevel, c) <= v ? c : k;
         }
         const float dj = __shfl_sync(0xFFFFFFFFu, mylevel, k);
         const float dn = __shfl_sync(0xFFFFFFFFu, mylevel, k < 15 ? k + 1 : 15);
@@ -288,14 +288,14 @@ __device__ __forceinline__ void turbo_encode(const TurboArgs &a, const TurboScal
             }
         }
         nvhalf |= (uint32_t)idx << (4 * j);
-        vhat[j] = __shfl_sync(0xFFFFFFFFu, mylevel, idx);
+        den5[j] = __shfl_sync(0xFFFFFFFFu, myden, idx);
     }
     // ---- 6. encode the next UState payload
     float q[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         if (WHOLE || j < valid) {
-            const float den = __fadd_rn(root_of_quotient<BF>(vhat[j], s.bc2, f.rb2), s.ef);
+            const float den = den5[j];
             const float t = BF ? __uint_as_float(__float_as_uint(quotient_by_reciprocal(L.mn[j], ts.bc1, f.rb1)) |
                                                  (__float_as_uint(L.mn[j]) & 0x80000000u))
                                : __fdiv_rn(L.mn[j], ts.bc1);
@@ -359,42 +359,69 @@ __device__ __forceinline__ void turbo_encode(const TurboArgs &a, const TurboScal
     racc = __fadd_rn(racc, rsum);
 }
 
-// One storage block (128 values from element i0) by one warp.  WHOLE: all 128
-// values lie below n.
+// A lane's inputs for one storage block: its values, their codes and indices,
+// the block's endpoints and its mean block's bf16 mean.
+struct TurboIn {
+    float p[4], g[4];
+    uint32_t cbyte, vhalf;
+    uint16_t vlo, vhi, mean;
+};
+
+template <bool WHOLE>
+__device__ __forceinline__ TurboIn turbo_load(const TurboArgs &a, int64_t i0)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t e0 = i0 + 4 * lane;
+    const int valid = WHOLE ? 4 : (e0 >= a.n ? 0 : (a.n - e0 >= 4 ? 4 : (int)(a.n - e0)));
+    TurboIn in;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        in.p[j] = in.g[j] = 0.0f;
+    in.cbyte = in.vhalf = 0u;
+    if (WHOLE || valid == 4) {
+        const float4 pv = *reinterpret_cast<const float4 *>(a.p + e0);
+        const float4 gv = __ldg(reinterpret_cast<const float4 *>(a.g + e0));
+        in.p[0] = pv.x; in.p[1] = pv.y; in.p[2] = pv.z; in.p[3] = pv.w;
+        in.g[0] = gv.x; in.g[1] = gv.y; in.g[2] = gv.z; in.g[3] = gv.w;
+        in.cbyte = a.ucode[e0 / 4];
+        in.vhalf = *reinterpret_cast<const uint16_t *>(a.vidx + e0 / 2);
+    } else if (valid > 0) {
+        for (int j = 0; j < valid; ++j) {
+            in.p[j] = a.p[e0 + j];
+            in.g[j] = a.g[e0 + j];
+        }
+        in.cbyte = a.ucode[e0 / 4];
+        in.vhalf = a.vidx[e0 / 2] | (valid > 2 ? (uint32_t)a.vidx[e0 / 2 + 1] << 8 : 0u);
+    }
+    const int64_t b = i0 / kTurboBlock;
+    in.vlo = a.vend[2 * b];
+    in.vhi = a.vend[2 * b + 1];
+    const int64_t mstart = i0 + kTurboMean * (lane >> 4);
+    in.mean = (WHOLE || mstart < a.n) ? a.umean[mstart / kTurboMean] : (uint16_t)0;
+    return in;
+}
+
+// One storage block (128 values from element i0) by one warp, from its loaded
+// inputs.  WHOLE: all 128 values lie below n.
 template <bool WHOLE>
 __device__ __forceinline__ void turbo_block(const TurboArgs &a, const TurboScalars &ts,
                                             const TurboFast &f, float sdec, float senc, int64_t i0,
-                                            uint32_t &bad, float &racc)
+                                            const TurboIn &in, uint32_t &bad, float &racc)
 {
     const int lane = threadIdx.x & 31;
     const int64_t e0 = i0 + 4 * lane;  // this lane's first element
     const int valid = WHOLE ? 4 : (e0 >= a.n ? 0 : (a.n - e0 >= 4 ? 4 : (int)(a.n - e0)));
     const Scalars &s = ts.s;
     TurboLane L;
-    // ---- loads
-    float g[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    uint32_t cbyte = 0, vhalf = 0;
+    float g[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-        L.p[j] = 0.0f;
-    if (WHOLE || valid == 4) {
-        const float4 pv = *reinterpret_cast<const float4 *>(a.p + e0);
-        const float4 gv = __ldg(reinterpret_cast<const float4 *>(a.g + e0));
-        L.p[0] = pv.x; L.p[1] = pv.y; L.p[2] = pv.z; L.p[3] = pv.w;
-        g[0] = gv.x; g[1] = gv.y; g[2] = gv.z; g[3] = gv.w;
-        cbyte = a.ucode[e0 / 4];
-        vhalf = *reinterpret_cast<const uint16_t *>(a.vidx + e0 / 2);
-    } else if (valid > 0) {
-        for (int j = 0; j < valid; ++j) {
-            L.p[j] = a.p[e0 + j];
-            g[j] = a.g[e0 + j];
-        }
-        cbyte = a.ucode[e0 / 4];
-        vhalf = a.vidx[e0 / 2] | (valid > 2 ? (uint32_t)a.vidx[e0 / 2 + 1] << 8 : 0u);
+    for (int j = 0; j < 4; ++j) {
+        L.p[j] = in.p[j];
+        g[j] = in.g[j];
     }
-    const int64_t b = i0 / kTurboBlock;
-    const int lo = __half2int_rn(__ushort_as_half(a.vend[2 * b]));
-    const int hi = __half2int_rn(__ushort_as_half(a.vend[2 * b + 1]));
+    const uint32_t cbyte = in.cbyte, vhalf = in.vhalf;
+    const int lo = __half2int_rn(__ushort_as_half(in.vlo));
+    const int hi = __half2int_rn(__ushort_as_half(in.vhi));
     const uint32_t blo = pow2_bits(lo), bhi = pow2_bits(hi);
     const int half = lane >> 4;  // mean block of this lane within the storage block
     const int64_t mstart = i0 + kTurboMean * half;
@@ -408,26 +435,22 @@ __device__ __forceinline__ void turbo_block(const TurboArgs &a, const TurboScala
         if (WHOLE || j < valid)
             S += ulevel2((cbyte >> (2 * j)) & 3u);
     S = half_warp_sum(S);
-    float mu = 0.0f;
-    if (WHOLE || mcount > 0)
-        mu = __uint_as_float((uint32_t)a.umean[mstart / kTurboMean] << 16);
+    const float mu = (WHOLE || mcount > 0) ? __uint_as_float((uint32_t)in.mean << 16) : 0.0f;
     const float delta = WHOLE ? __fmul_rn(__fmul_rn(sdec, (float)S), 0x1p-7f)  // / 128
                               : (mcount > 0 ? __fdiv_rn(__fmul_rn(sdec, (float)S), (float)(2 * mcount)) : 0.0f);
+    // lane k holds level k of the old grid and the prior denominator for it,
+    // sqrt(level / bc2p) + eps
     const float oldlevel = q1_level(blo, bhi, lane < 16 ? lane : 15);
-    const bool old_bf = f.ok && lo >= -100 && hi <= 99;  // uniform over the warp
+    const float oldden = ts.step > 1 ? __fadd_rn(__fsqrt_rn(__fdiv_rn(oldlevel, ts.bc2p)), s.ef) : 0.0f;
     float mprev[4], vdec[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const float v = __shfl_sync(0xFFFFFFFFu, oldlevel, (int)((vhalf >> (4 * j)) & 15u));
+        const int idx = (int)((vhalf >> (4 * j)) & 15u);
+        const float v = __shfl_sync(0xFFFFFFFFu, oldlevel, idx);
+        const float den = __shfl_sync(0xFFFFFFFFu, oldden, idx);
         const float d = __fmul_rn(sdec, ulevel((cbyte >> (2 * j)) & 3u));
         const float q = __fadd_rn(mu, __fsub_rn(d, delta));
-        float m = 0.0f;
-        if (ts.step > 1) {
-            const float root = old_bf ? root_of_quotient<true>(v, ts.bc2p, f.rb2p)
-                                      : root_of_quotient<false>(v, ts.bc2p, f.rb2p);
-            m = __fmul_rn(__fmul_rn(q, __fadd_rn(root, s.ef)), ts.bc1p);
-        }
-        mprev[j] = m;
+        mprev[j] = ts.step > 1 ? __fmul_rn(__fmul_rn(q, den), ts.bc1p) : 0.0f;
         vdec[j] = v;
     }
     // ---- 3. the fp32 moments; the block's v' range; each lane's |m'| range
@@ -471,14 +494,18 @@ turbo_step_kernel(const TurboArgs a, const TurboScalars ts, unsigned long long *
     const int64_t warp = (int64_t)blockIdx.x * kTurboWarps + (threadIdx.x >> 5);
     const int64_t warps = (int64_t)gridDim.x * kTurboWarps;
     const TurboFast f = turbo_fast_of(ts, senc);
+    const int64_t nwhole = a.n / kTurboBlock;
     uint32_t bad = 0;
     float racc = 0.0f;
-    for (int64_t b = warp; b < nblocks; b += warps) {  // uniform per warp
-        if ((b + 1) * kTurboBlock <= a.n)
-            turbo_block<true>(a, ts, f, sdec, senc, b * kTurboBlock, bad, racc);
-        else
-            turbo_block<false>(a, ts, f, sdec, senc, b * kTurboBlock, bad, racc);
-    }
+    // (Loading a warp's next block before computing the current one measured
+    // 6 % slower on GB300.)
+    int64_t b = warp;
+    for (; b < nwhole; b += warps)  // uniform per warp
+        turbo_block<true>(a, ts, f, sdec, senc, b * kTurboBlock, turbo_load<true>(a, b * kTurboBlock),
+                          bad, racc);
+    if (b < nblocks)  // the short last block
+        turbo_block<false>(a, ts, f, sdec, senc, b * kTurboBlock, turbo_load<false>(a, b * kTurboBlock),
+                           bad, racc);
     // the RMS accumulator: one atomic per warp
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1)

@@ -17,7 +17,9 @@ from gpu_helpers import assert_same_bits, dev, host_f32, host_u32
 pytestmark = pytest.mark.gpu
 
 HY = wl.HYPER
-SIZES = [1, 3, 4, 5, 255, 4095, 4096, 4097, 3 * 4096 + 7, 6143, 6144, 6147, 2 * 6144 + 5, 100_003]
+# 1_500_007: a launch of a few full tiles per SM with a ragged tail
+SIZES = [1, 3, 4, 5, 255, 4095, 4096, 4097, 3 * 4096 + 7, 6143, 6144, 6147, 2 * 6144 + 5, 100_003,
+         1_500_007]
 
 
 @pytest.fixture(scope="module")
