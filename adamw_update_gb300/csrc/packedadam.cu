@@ -152,10 +152,9 @@ __device__ __forceinline__ uint4 packed_vector(float pp[4], const float gg[4], c
     }
     adamw_vector<UNIT_BC2, true>(p, g, m, v, s, k, zs, o, rn);
     uint32_t out[4];
+    bad += nonfinite_count4(o);
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-        bad += any_nonfinite(Moments{o[j].p.x, o[j].m.x, o[j].v.x}) +
-               any_nonfinite(Moments{o[j].p.y, o[j].m.y, o[j].v.y});
         pp[2 * j] = o[j].p.x;
         pp[2 * j + 1] = o[j].p.y;
         out[2 * j] = MODE == kE4 ? encode_step_word_e4(o[j].m.x, o[j].v.x, rn[j].x)
@@ -529,10 +528,9 @@ __device__ __forceinline__ void pipe_vector_math(const unsigned char *buf, int e
         Moments2 o[2];
         float2 unused[2];
         adamw_vector<U1, false>(p, g, m, v, s, k, zs, o, unused);
+        bad += nonfinite_count4(o);
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            bad += any_nonfinite(Moments{o[j].p.x, o[j].m.x, o[j].v.x}) +
-                   any_nonfinite(Moments{o[j].p.y, o[j].m.y, o[j].v.y});
             pp[2 * j] = o[j].p.x;
             pp[2 * j + 1] = o[j].p.y;
         }
@@ -603,10 +601,9 @@ __device__ __forceinline__ void compute_vec(const RegVec<MODE> &r, int e, const 
         Moments2 o[2];
         float2 unused[2];
         adamw_vector<U1, false>(p, g, m, v, s, pairs_of(s), zs, o, unused);
+        bad += nonfinite_count4(o);
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            bad += any_nonfinite(Moments{o[j].p.x, o[j].m.x, o[j].v.x}) +
-                   any_nonfinite(Moments{o[j].p.y, o[j].m.y, o[j].v.y});
             pp[2 * j] = o[j].p.x;
             pp[2 * j + 1] = o[j].p.y;
         }
@@ -1161,6 +1158,8 @@ __device__ __forceinline__ void blockwise_block(const BlockwiseArgs &a, Blockwis
             Moments2 o2[2];
             float2 unused[2];
             adamw_vector<false, false>(P2, G2, M2, V2, s, pairs_of(s), zs, o2, unused);
+            if (WHOLE)
+                bad += nonfinite_count4(o2);
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 o[2 * j] = Moments{o2[j].p.x, o2[j].m.x, o2[j].v.x};
@@ -1171,10 +1170,12 @@ __device__ __forceinline__ void blockwise_block(const BlockwiseArgs &a, Blockwis
         for (int j = 0; j < 4; ++j) {
             po[j] = o[j].p;
             float2 x = make_float2(o[j].m, o[j].v);
-            if (WHOLE || e0 + j < a.n)
-                bad += any_nonfinite(o[j]);
-            else
-                x = make_float2(0.0f, 0.0f);  // |0| never raises the block max
+            if (!WHOLE) {
+                if (e0 + j < a.n)
+                    bad += any_nonfinite(o[j]);
+                else
+                    x = make_float2(0.0f, 0.0f);  // |0| never raises the block max
+            }
             nv[4 * h + j] = x;
             um = max(um, __float_as_uint(x.x) & 0x7FFFFFFFu);
             uv = max(uv, __float_as_uint(x.y) & 0x7FFFFFFFu);

@@ -9,7 +9,8 @@ PA_EXHAUSTIVE_DIVISION=1, about 45 s on a GB300), and whole elements
 (adamw_element, zero-safe against plain) on 2^30 random elements whose
 values, scalars and hyperparameters include zeros, subnormals, extremes, Inf
 and NaN.  The per-vector path's branch-free arithmetic: the residual-corrected
-square root against __fsqrt_rn for every binary32 in [2^-100, 2^126), and
+square roots against __fsqrt_rn for every binary32 in [2^-100, 2^126) (and the
+zero-safe one at +-0), and
 adamw_vector (the warp's vote between the branch-free and the zero-safe
 arithmetic) against adamw_element on 2^29 elements per bias-correction case,
 with warps at the edges of the branch-free ranges; both arms must run."""
