@@ -100,21 +100,15 @@ __device__ __forceinline__ void store_stream(uint32_t *a, uint4 x) { __stcs(rein
 // ---- one element of a packed step -------------------------------------------
 // Decode the prior state, v = r*r, FP32 update, encode m' and sqrt(v') into the
 // next word ("Release scope": the state is stored only after the update).
-// (`vout`: receives v' and the element is not counted, for callers that count
-// four at once.)
 template <int MODE, bool UNIT_BC2>
 __device__ __forceinline__ uint32_t packed_element(float &p, float g, uint32_t w,
-                                                   const Scalars &s, uint32_t &bad,
-                                                   float *vout = nullptr)
+                                                   const Scalars &s, uint32_t &bad)
 {
     const float m = MODE == kE4 ? decode_m_lane(w) : decode_fp16_low(w);
     const float r = MODE == kE4 ? decode_rms_lane(w) : decode_fp16_high(w);
     float rn = 0.0f;
     const Moments o = adamw_element<UNIT_BC2>(p, g, m, __fmul_rn(r, r), s, &rn);
-    if (vout)
-        *vout = o.v;
-    else
-        bad += any_nonfinite(o);
+    bad += any_nonfinite(o);
     p = o.p;
     if (!UNIT_BC2)
         rn = __fsqrt_rn(o.v);  // bc2 == 1: the update took sqrt(v')
@@ -587,11 +581,13 @@ __device__ __forceinline__ RegVec<MODE> load_vec(const unsigned char *buf, int e
     return r;
 }
 
-// The FP32 mode takes adamw_vector (packed pairs, the warp's vote for the
-// branch-free quotients): on GB300 3 % faster than one element at a time on
-// the gpt-52 list.  The packed modes keep one element at a time with the IEEE
-// arithmetic: adamw_vector here measured 2.6 % slower on the 7e9-parameter
-// flat workload, all of whose tiles take this path.
+// Every mode takes adamw_vector here (packed pairs, the warp's vote for the
+// branch-free quotients and roots).  Measured on GB300 against one element at
+// a time with the IEEE arithmetic: FP32 3 % faster on the gpt-52 list; packed
+// E4 +0.2 % on the 7e9-parameter flat workload and +2.2 % with bfloat16
+// gradients (that step is issue-bound), once the roots took their zero case
+// by an add and the non-finite count went to packed FMAs (before that, 2.6 %
+// slower on the flat workload).
 template <int MODE, bool U1>
 __device__ __forceinline__ void compute_vec(const RegVec<MODE> &r, int e, const Desc &d,
                                             int64_t base, const Scalars &s, const ZeroSafe &zs,
@@ -616,15 +612,8 @@ __device__ __forceinline__ void compute_vec(const RegVec<MODE> &r, int e, const 
         store_stream(static_cast<float *>(d.s1) + base + e, make_float4(o[0].m.x, o[0].m.y, o[1].m.x, o[1].m.y));
         store_stream(static_cast<float *>(d.s2) + base + e, make_float4(o[0].v.x, o[0].v.y, o[1].v.x, o[1].v.y));
     } else {
-        uint32_t ww[4] = {r.w.x, r.w.y, r.w.z, r.w.w};
-        float vn[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            ww[j] = packed_element<MODE, U1>(pp[j], gg[j], ww[j], s, bad, &vn[j]);
-        const Moments2 o[2] = {{make_float2(pp[0], pp[1]), make_float2(0.0f, 0.0f), make_float2(vn[0], vn[1])},
-                               {make_float2(pp[2], pp[3]), make_float2(0.0f, 0.0f), make_float2(vn[2], vn[3])}};
-        bad += nonfinite_count4(o);
-        store_stream(static_cast<uint32_t *>(d.s1) + base + e, make_uint4(ww[0], ww[1], ww[2], ww[3]));
+        store_stream(static_cast<uint32_t *>(d.s1) + base + e,
+                     packed_vector<MODE, U1>(pp, gg, r.w, s, pairs_of(s), zs, bad));
     }
     store_stream(d.p + base + e, make_float4(pp[0], pp[1], pp[2], pp[3]));
 }
