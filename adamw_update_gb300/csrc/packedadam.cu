@@ -10,7 +10,11 @@
 //
 // Design.  The step is elementwise and bound by HBM bandwidth (20 bytes per
 // parameter for the packed modes) and by instruction issue (the correctly
-// rounded divisions and square roots).  The step kernels are staged: one CTA
+// rounded divisions and square roots, the codecs' integer work).  The
+// consumers update 16-byte vectors four elements at a time with packed f32x2
+// arithmetic, one warp vote choosing branch-free correctly rounded quotients
+// and roots (exact.cuh) where every lane's operands allow them, the zero-safe
+// IEEE arithmetic otherwise (codecs.cuh).  The step kernels are staged: one CTA
 // per SM, whose producer warp streams tiles of every input into a two-stage
 // shared-memory ring with bulk (TMA) copies and mbarriers, while 24 consumer
 // warps update the staged tiles and store the results straight to global
