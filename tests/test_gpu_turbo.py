@@ -107,3 +107,57 @@ def test_turbo_special_blocks():
                                 dict(lr=3e-4, beta1=0.95, beta2=0.9999, eps=1e-8, wd=0.0)])
 def test_turbo_other_hyperparameters(hy):
     assert _run(5000, 4, _normal, seed=99, hy=hy, factor=1.3) == 0
+
+
+def test_turbo_branch_free_range_edges():
+    """Blocks at the edges of the ranges where the step takes the branch-free
+    quotients: v' around 2^-76 at step 1 (gradients near 2^-33 on zero state),
+    then |m'| just inside and just outside 2^-40 and 2^40 at step 2 (the
+    gradient built from the decoded first moment, m' = b1*m + c1*g landing on
+    the chosen magnitude), then an ordinary step from those states.  Blocks
+    that straddle an edge take the IEEE arithmetic, the others the FMA forms;
+    both must equal the oracle bit for bit."""
+    import torch
+
+    import adamw_update_gb300 as pa
+
+    nb = 16
+    n = 128 * nb
+    b1, c1 = float(np.float32(HY["beta1"])), float(np.float32(1.0 - HY["beta1"]))
+    rng = np.random.default_rng(404)
+    p = torch.from_numpy(rng.normal(0, 0.02, n).astype(np.float32)).cuda()
+    st = pa.turbo_state(n)
+    bad = torch.zeros(1, dtype=torch.int64, device="cuda")
+    scale = rng.uniform(0.95, 1.05, n)
+    sign = rng.choice([-1.0, 1.0], n)
+    # per block: the step-1 gradient magnitude and the step-2 |m'| target
+    # (2^-33: v' = c2*g^2 straddles 2^-76 over the block's +-5 %; 1.06 * 2^-33:
+    # every v' just above it)
+    g1_mag = [2.0 ** -33] * 2 + [1.06 * 2.0 ** -33] * 2 + [1e-9] * 6 + [1e-3] * 6
+    m2_target = ([None] * 4 + [2.0 ** -40 * f for f in (0.5, 0.999, 1.001, 2.0, 1.0, 1.0)] +
+                 [2.0 ** 40 * f for f in (0.5, 0.999, 1.001, 2.0)] + [None] * 2)
+    for t in (1, 2, 3):
+        before = _host_state(st)
+        p_before = p.cpu().numpy()
+        if t == 1:
+            g = np.concatenate([sign[128 * b:128 * (b + 1)] * scale[128 * b:128 * (b + 1)] * g1_mag[b]
+                                for b in range(nb)])
+        elif t == 2:
+            m_dec, _ = oracle.turbo_decode(before, n, 2, HY["beta1"], HY["beta2"], HY["eps"])
+            g = np.empty(n)
+            for b in range(nb):
+                s = slice(128 * b, 128 * (b + 1))
+                if m2_target[b] is None:
+                    g[s] = rng.normal(0, 1e-3, 128)
+                else:
+                    target = sign[s] * scale[s] * m2_target[b]
+                    g[s] = (target - b1 * m_dec[s].astype(np.float64)) / c1
+        else:
+            g = rng.normal(0, 1e-3, n)
+        g = g.astype(np.float32)
+        pa.pa_turbo_step(p, torch.from_numpy(g).cuda(), st, t, nonfinite=bad, **HY)
+        torch.cuda.synchronize()
+        ep, est, eb = oracle.turbo_step(p_before, g, before, t, **HY)
+        est["uscal"] = oracle.turbo_finalize(est["uscal"], n, 1.1)
+        _compare(n, p, st, ep, est, f"range edges, step {t}")
+    assert int(bad.item()) == 0
