@@ -136,7 +136,7 @@ __device__ __forceinline__ float2 decode_rms_pair(uint32_t w0, uint32_t w1)
     return mul2(make_float2(__uint_as_float(b0), __uint_as_float(b1)), make_float2(0x1p112f, 0x1p112f));
 }
 
-template <int MODE, bool UNIT_BC2>
+template <int MODE, bool UNIT_BC2, bool DEFER_NAN>
 __device__ __forceinline__ uint4 packed_vector(float pp[4], const float gg[4], const uint4 w,
                                                const Scalars &s, const Pairs &k, const ZeroSafe &zs,
                                                uint32_t &bad)
@@ -155,16 +155,44 @@ __device__ __forceinline__ uint4 packed_vector(float pp[4], const float gg[4], c
         v[j] = mul2(r, r);
     }
     adamw_vector<UNIT_BC2, true>(p, g, m, v, s, k, zs, o, rn);
-    uint32_t out[4];
-    bad += nonfinite_count4(o);
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
         pp[2 * j] = o[j].p.x;
         pp[2 * j + 1] = o[j].p.y;
-        out[2 * j] = MODE == kE4 ? encode_step_word_e4(o[j].m.x, o[j].v.x, rn[j].x)
-                                 : encode_word_fp16(o[j].m.x, rn[j].x);
-        out[2 * j + 1] = MODE == kE4 ? encode_step_word_e4(o[j].m.y, o[j].v.y, rn[j].y)
-                                     : encode_word_fp16(o[j].m.y, rn[j].y);
+    }
+    uint32_t out[4];
+    // DEFER_NAN: encode without the NaN tests and only when the non-finite
+    // count is nonzero encode again with them.  A NaN m' makes p' NaN and a
+    // NaN RMS comes from a NaN v', so a lane whose code needs the NaN rules
+    // always makes that count nonzero.  Same words either way.
+    const uint32_t nf = DEFER_NAN ? 0u : nonfinite_count4(o);
+    bad += nf;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        if (DEFER_NAN) {
+            out[2 * j] = MODE == kE4 ? encode_step_word_e4_finite(o[j].m.x, rn[j].x)
+                                     : encode_word_fp16_finite(o[j].m.x, rn[j].x);
+            out[2 * j + 1] = MODE == kE4 ? encode_step_word_e4_finite(o[j].m.y, rn[j].y)
+                                         : encode_word_fp16_finite(o[j].m.y, rn[j].y);
+        } else {
+            out[2 * j] = MODE == kE4 ? encode_step_word_e4(o[j].m.x, o[j].v.x, rn[j].x)
+                                     : encode_word_fp16(o[j].m.x, rn[j].x);
+            out[2 * j + 1] = MODE == kE4 ? encode_step_word_e4(o[j].m.y, o[j].v.y, rn[j].y)
+                                         : encode_word_fp16(o[j].m.y, rn[j].y);
+        }
+    }
+    if (DEFER_NAN) {
+        const uint32_t nfd = nonfinite_count4(o);
+        if (nfd != 0) {
+            bad += nfd;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                out[2 * j] = MODE == kE4 ? encode_step_word_e4(o[j].m.x, o[j].v.x, rn[j].x)
+                                         : encode_word_fp16(o[j].m.x, rn[j].x);
+                out[2 * j + 1] = MODE == kE4 ? encode_step_word_e4(o[j].m.y, o[j].v.y, rn[j].y)
+                                             : encode_word_fp16(o[j].m.y, rn[j].y);
+            }
+        }
     }
     return make_uint4(out[0], out[1], out[2], out[3]);
 }
@@ -542,8 +570,10 @@ __device__ __forceinline__ void pipe_vector_math(const unsigned char *buf, int e
         store_stream(static_cast<float *>(d.s2) + base + e, make_float4(o[0].v.x, o[0].v.y, o[1].v.x, o[1].v.y));
     } else {
         const uint4 wv = *reinterpret_cast<const uint4 *>(buf + L::kS1 + 4 * e);
+        // (the E4 vectors here are issue-bound: NaN tests deferred, 2 % faster
+        // on gpt2-148; the FP16 mode measured no gain)
         store_stream(static_cast<uint32_t *>(d.s1) + base + e,
-                     packed_vector<MODE, U1>(pp, gg, wv, s, k, zs, bad));
+                     packed_vector<MODE, U1, MODE == kE4>(pp, gg, wv, s, k, zs, bad));
     }
 }
 
@@ -592,7 +622,7 @@ __device__ __forceinline__ RegVec<MODE> load_vec(const unsigned char *buf, int e
 // gradients (that step is issue-bound), once the roots took their zero case
 // by an add and the non-finite count went to packed FMAs (before that, 2.6 %
 // slower on the flat workload).
-template <int MODE, bool U1>
+template <int MODE, bool U1, typename GT>
 __device__ __forceinline__ void compute_vec(const RegVec<MODE> &r, int e, const Desc &d,
                                             int64_t base, const Scalars &s, const ZeroSafe &zs,
                                             uint32_t &bad)
@@ -616,8 +646,11 @@ __device__ __forceinline__ void compute_vec(const RegVec<MODE> &r, int e, const 
         store_stream(static_cast<float *>(d.s1) + base + e, make_float4(o[0].m.x, o[0].m.y, o[1].m.x, o[1].m.y));
         store_stream(static_cast<float *>(d.s2) + base + e, make_float4(o[0].v.x, o[0].v.y, o[1].v.x, o[1].v.y));
     } else {
+        // (NaN tests deferred with bfloat16 gradients, whose whole tiles are
+        // issue-bound: 4 % faster; with FP32 gradients, bound by HBM, the same
+        // measured 3-5 % slower on the 7e9-parameter flat workload)
         store_stream(static_cast<uint32_t *>(d.s1) + base + e,
-                     packed_vector<MODE, U1>(pp, gg, r.w, s, pairs_of(s), zs, bad));
+                     packed_vector<MODE, U1, sizeof(GT) == 2>(pp, gg, r.w, s, pairs_of(s), zs, bad));
     }
     store_stream(d.p + base + e, make_float4(pp[0], pp[1], pp[2], pp[3]));
 }
@@ -717,7 +750,7 @@ __device__ __forceinline__ void pipe_consume(const unsigned char *smem, uint64_t
                 released = true;
 #pragma unroll
                 for (int v = 0; v < kTileVecs; ++v)
-                    compute_vec<MODE, U1>(rv[v], 4 * (ct + v * kConsumers), d, sp.base, s, zs, bad);
+                    compute_vec<MODE, U1, GT>(rv[v], 4 * (ct + v * kConsumers), d, sp.base, s, zs, bad);
             } else if (fast) {
 #pragma unroll
                 for (int v = 0; v < kTileVecs; ++v)
