@@ -14,7 +14,8 @@
 // uniform in the binary32 bit pattern between the integer binary exponents
 // that bracket the block's positive values (exact, no transcendental
 // function); index 0 is 0; stochastic rounding with u from SplitMix64 at a
-// counter (step, stream, element); UState levels {-1.5, -0.5, 0.5, 1.5} times
+// counter (step, stream, index / 2), each output's bits 40..63 serving the
+// even index and bits 16..39 the odd one; UState levels {-1.5, -0.5, 0.5, 1.5} times
 // the one-step-lagged encode scale, antithetic pairs (2k, 2k+1) share u and
 // 1-u; block means are pairwise trees rounded to bf16; the finaliser rotates
 // the scales (decode <- encode, encode <- factor * sqrt(acc / n), acc <- 0).
@@ -30,7 +31,7 @@
 // one float atomic per warp (its sum order is the only thing that differs
 // from a sequential evaluation).  Whole blocks take a body without bounds
 // logic; a warp whose operands allow it takes the branch-free quotients and
-// roots described above TurboFast; each pair of elements draws one hash.
+// roots described above TurboFast.
 #pragma once
 
 namespace pa {
@@ -69,9 +70,9 @@ __device__ __forceinline__ uint64_t splitmix64_mix(uint64_t z)
 
 constexpr uint64_t kGolden = 0x9E3779B97F4A7C15ull;  // SplitMix64's counter increment
 
-// seed + (c + 1) * golden for the counter c of (step, stream, index): the
-// input of the mix; index + j adds j * golden (index + j < 2^40 never carries
-// into the stream and step fields)
+// seed + (c + 1) * golden for the counter c of (step, stream, k), k the
+// output's number in its stream (an index / 2): the input of the mix; k + j
+// adds j * golden (k + j < 2^40 never carries into the stream and step fields)
 __device__ __forceinline__ uint64_t turbo_counter(uint64_t seed, int64_t step, uint32_t stream,
                                                   uint64_t index)
 {
@@ -79,13 +80,13 @@ __device__ __forceinline__ uint64_t turbo_counter(uint64_t seed, int64_t step, u
     return seed + (c + 1u) * kGolden;
 }
 
-// u in [0, 1) on the 2^-24 grid: the top 24 bits of the mix of z.  The mix's
-// last step, z ^ (z >> 31), leaves bits 40..63 as they are, so it is not taken.
-__device__ __forceinline__ float turbo_uniform_of(uint64_t z)
+// The two uniforms in [0, 1) on the 2^-24 grid that one output serves: bits
+// 40..63 of the mix of z for the even index, bits 16..39 for the odd one.
+__device__ __forceinline__ float2 turbo_uniform_pair(uint64_t z)
 {
-    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
-    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
-    return __uint2float_rn((uint32_t)(z >> 40)) * 0x1p-24f;
+    const uint64_t h = splitmix64_mix(z);
+    return make_float2(__uint2float_rn((uint32_t)(h >> 40)) * 0x1p-24f,
+                       __uint2float_rn((uint32_t)(h >> 16) & 0xFFFFFFu) * 0x1p-24f);
 }
 
 // ---- 1Q grid ---------------------------------------------------------------------
@@ -409,18 +410,22 @@ __device__ __forceinline__ void turbo_block(const TurboArgs &a, const TurboScala
     const Scalars &s = ts.s;
     // The rounding uniforms depend on the counters alone: formed here, where
     // they overlap the block's loads (2 % faster on GB300 than where they are
-    // used; builds without the two hashes ran 19 % faster).  1Q: one per value;
-    // UState: one per antithetic pair (2k, 2k+1), which share u and 1-u (e0 is
-    // a multiple of 4).
+    // used; builds without the hashes ran 19 % faster).  Each hash output
+    // serves two indices.  1Q: one uniform per value, two outputs for the
+    // lane's four; UState: one per antithetic pair (2k, 2k+1), which share u
+    // and 1-u, one output for the lane's two pairs (e0 is a multiple of 4).
     float u1[4], upair[2];
     {
-        const uint64_t z1 = turbo_counter(ts.seed, ts.step, 1u, (uint64_t)e0);
-        const uint64_t z2 = turbo_counter(ts.seed, ts.step, 2u, (uint64_t)e0 >> 1);
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            u1[j] = turbo_uniform_of(z1 + (uint64_t)j * kGolden);
-        upair[0] = turbo_uniform_of(z2);
-        upair[1] = turbo_uniform_of(z2 + kGolden);
+        const uint64_t z1 = turbo_counter(ts.seed, ts.step, 1u, (uint64_t)e0 >> 1);
+        const uint64_t z2 = turbo_counter(ts.seed, ts.step, 2u, (uint64_t)e0 >> 2);
+        const float2 a = turbo_uniform_pair(z1), b = turbo_uniform_pair(z1 + kGolden);
+        const float2 c = turbo_uniform_pair(z2);
+        u1[0] = a.x;
+        u1[1] = a.y;
+        u1[2] = b.x;
+        u1[3] = b.y;
+        upair[0] = c.x;
+        upair[1] = c.y;
     }
     TurboLane L;
     float g[4];

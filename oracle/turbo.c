@@ -49,9 +49,11 @@
  *   T3  Counter hash.  SplitMix64 (G. Steele, D. Lea, C. Flood, "Fast
  *       splittable pseudorandom number generators", OOPSLA 2014; the public
  *       splitmix64 generator): output number c+1 of the generator seeded with
- *       `seed`, at counter c = step << 42 | stream << 40 | index, is
- *       mix64(seed + (c + 1) * 0x9E3779B97F4A7C15); u = (output >> 40) *
- *       2^-24 in [0, 1).  Stream 1 rounds 1Q, stream 2 UState.
+ *       `seed`, at counter c = step << 42 | stream << 40 | (index >> 1), is
+ *       mix64(seed + (c + 1) * 0x9E3779B97F4A7C15); each output serves two
+ *       indices: u = (bits 40..63 of it) * 2^-24 for an even index, (bits
+ *       16..39) * 2^-24 for the odd one after it, in [0, 1).  Stream 1
+ *       rounds 1Q, stream 2 UState.
  *   T4  UState code.  Four levels L = {-1.5, -0.5, 0.5, 1.5} in units of the
  *       encode scale s: y = r / s (0 when s = 0), z = clamp(y + 1.5, 0, 3),
  *       j = min(floor(z), 2), code = j + 1 when u < z - j, else j.  Antithetic:
@@ -101,8 +103,10 @@ uint64_t oracle_splitmix64_at(uint64_t seed, uint64_t counter)
 
 float oracle_turbo_uniform(uint64_t seed, int64_t step, uint32_t stream, uint64_t index)
 {
-    uint64_t c = ((uint64_t)step << 42) | ((uint64_t)stream << 40) | index;
-    return (float)(oracle_splitmix64_at(seed, c) >> 40) * 0x1p-24f;
+    uint64_t c = ((uint64_t)step << 42) | ((uint64_t)stream << 40) | (index >> 1);
+    uint64_t h = oracle_splitmix64_at(seed, c);
+    uint64_t field = (index & 1u) ? (h >> 16) & 0xFFFFFFu : h >> 40;
+    return (float)field * 0x1p-24f;
 }
 
 /* ---- 1Q (T1, T2) ------------------------------------------------------------ */

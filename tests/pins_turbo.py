@@ -50,6 +50,21 @@ def check_uniform_statistics(orc):
             assert abs(c) < 6 / np.sqrt(n), (keys[a], keys[b], c)
 
 
+def check_two_uniforms_per_output(orc):
+    """Indices 2k and 2k+1 of a stream take bits 40..63 and 16..39 of the one
+    SplitMix64 output at counter (step, stream, k): both on the 2^-24 grid,
+    and together they are 48 bits of that output."""
+    rng = np.random.default_rng(9)
+    for _ in range(300):
+        seed = int(rng.integers(0, 2 ** 63))
+        step, stream, k = int(rng.integers(1, 2 ** 20)), int(rng.integers(1, 3)), int(rng.integers(0, 2 ** 38))
+        c = (step << 42) | (stream << 40) | k
+        h = orc.splitmix64_at(seed, c)
+        u = orc.turbo_uniform(seed, step, stream, np.array([2 * k, 2 * k + 1], np.uint64))
+        assert int(np.float64(u[0]) * 2 ** 24) == h >> 40
+        assert int(np.float64(u[1]) * 2 ** 24) == (h >> 16) & 0xFFFFFF
+
+
 def check_counter_is_a_splitmix_position(orc):
     """Counter c of seed s is output number c+1 of the generator whose state
     starts at s and advances by the golden-ratio increment: moving one step
@@ -310,6 +325,7 @@ def check_finalize_rotates_scales(orc):
 ALL_CHECKS = {
     "uniform_statistics": check_uniform_statistics,
     "counter_is_a_splitmix_position": check_counter_is_a_splitmix_position,
+    "two_uniforms_per_output": check_two_uniforms_per_output,
     "q1_grid_closed_forms": check_q1_grid_closed_forms,
     "q1_endpoints": check_q1_endpoints,
     "q1_rounding": check_q1_rounding,

@@ -38,6 +38,10 @@ MUTANTS = [
      ["means_recentred"]),
     ("hash_counter_not_advanced", "return oracle_splitmix64_mix(seed + (counter + 1u) * 0x9E3779B97F4A7C15ull);",
      "return oracle_splitmix64_mix(seed + counter);", ["counter_is_a_splitmix_position"]),
+    ("odd_index_repeats_the_even_uniform", "uint64_t field = (index & 1u) ? (h >> 16) & 0xFFFFFFu : h >> 40;",
+     "uint64_t field = h >> 40;", ["two_uniforms_per_output", "uniform_statistics"]),
+    ("pair_counter_not_halved", "((uint64_t)stream << 40) | (index >> 1);",
+     "((uint64_t)stream << 40) | index;", ["two_uniforms_per_output"]),
 ]
 
 
