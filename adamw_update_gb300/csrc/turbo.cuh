@@ -158,8 +158,9 @@ __device__ __forceinline__ int half_warp_sum(int x)
 // ---- branch-free quotients ----------------------------------------------------------
 // The denominators sqrt(level / bc2p) + eps (decode) and sqrt(level / bc2) +
 // eps (encode) depend only on a grid level, so each lane forms the one of its
-// level with the IEEE operations and elements fetch theirs by shuffle.  For
-// the rest a warp replaces CUDA's correctly rounded divide and square root by
+// level and elements fetch theirs by shuffle; a lane forms them branch-free
+// too where the grid and bc2p (bc2) lie in the ranges below.  For the rest a
+// warp replaces CUDA's correctly rounded divide and square root by
 // the exact FMA forms of exact.cuh (Markstein's corrections, the residual
 // root), same bits, where every operand lies in their ranges:
 //  * launch (TurboFast::ok): bc2 in [2^-24, 1], bc1 in [2^-4, 1],
@@ -180,8 +181,8 @@ __device__ __forceinline__ int half_warp_sum(int x)
 //    code is the same.
 // Zero-signed quotients keep the dividend's sign (the divisors are positive).
 struct TurboFast {
-    float rb2, rb1, rs;  // RN(1/bc2), RN(1/bc1), RN(1/senc)
-    bool ok, sok;
+    float rb2, rb2p, rb1, rs;  // RN(1/bc2), RN(1/bc2p), RN(1/bc1), RN(1/senc)
+    bool ok, sok, okp;         // okp: bc2p in [2^-24, 1] (the decode's levels)
 };
 
 __device__ __forceinline__ TurboFast turbo_fast_of(const TurboScalars &ts, float senc)
@@ -192,7 +193,9 @@ __device__ __forceinline__ TurboFast turbo_fast_of(const TurboScalars &ts, float
     const bool b1 = ts.bc1 >= 0x1p-4f && ts.bc1 <= 1.0f;
     f.ok = b2 && b1 && s.ss >= 0x1p-20f && s.ss <= 0x1p20f && s.ef >= 0x1p-40f && s.ef <= 0x1p60f;
     f.sok = senc >= 0x1p-20f && senc <= 0x1p20f;
+    f.okp = ts.step > 1 && ts.bc2p >= 0x1p-24f && ts.bc2p <= 1.0f;
     f.rb2 = reciprocal_rn(b2 ? s.bc2 : 1.0f);
+    f.rb2p = reciprocal_rn(f.okp ? ts.bc2p : 1.0f);
     f.rb1 = reciprocal_rn(b1 ? ts.bc1 : 1.0f);
     f.rs = reciprocal_rn(f.sok ? senc : 1.0f);
     return f;
@@ -260,7 +263,7 @@ __device__ __forceinline__ void turbo_encode(const TurboArgs &a, const TurboScal
     // lane k holds level k of the new grid and the encode's denominator for it,
     // sqrt(level / bc2) + eps (the same value for every element that takes it)
     const float mylevel = q1_level(nblo, nbhi, lane < 16 ? lane : 15);
-    const float myden = __fadd_rn(__fsqrt_rn(__fdiv_rn(mylevel, s.bc2)), s.ef);
+    const float myden = __fadd_rn(root_of_quotient<BF>(mylevel, s.bc2, f.rb2), s.ef);
     uint32_t nvhalf = 0;
     float den5[4];
 #pragma unroll
@@ -456,7 +459,13 @@ __device__ __forceinline__ void turbo_block(const TurboArgs &a, const TurboScala
     // lane k holds level k of the old grid and the prior denominator for it,
     // sqrt(level / bc2p) + eps
     const float oldlevel = q1_level(blo, bhi, lane < 16 ? lane : 15);
-    const float oldden = ts.step > 1 ? __fadd_rn(__fsqrt_rn(__fdiv_rn(oldlevel, ts.bc2p)), s.ef) : 0.0f;
+    // (branch-free when the old grid lies in [2^-100, 2^99]: the level over
+    // bc2p below 2^123, its root in the residual root's range)
+    float oldden = 0.0f;
+    if (ts.step > 1)
+        oldden = __fadd_rn(f.okp && lo >= -100 && hi <= 99 ? root_of_quotient<true>(oldlevel, ts.bc2p, f.rb2p)
+                                                            : root_of_quotient<false>(oldlevel, ts.bc2p, f.rb2p),
+                           s.ef);
     float mprev[4], vdec[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
