@@ -95,13 +95,17 @@ __device__ __forceinline__ uint32_t pow2_bits(int e)
     return e >= -126 ? (uint32_t)(e + 127) << 23 : 1u << (e + 149);
 }
 
-// level k (0..15) of the grid [2^lo, 2^hi] given B(lo), B(hi)
+// level k (0..15) of the grid [2^lo, 2^hi] given B(lo), B(hi): the bits
+// B(lo) + floor((D (k-1) + 7) / 14), D = B(hi) - B(lo), in 32-bit arithmetic:
+// with D = 14 Q + R the floor is Q (k-1) + floor((R (k-1) + 7) / 14), whose
+// numerator is at most 13 * 14 + 7 = 189, where floor(t / 14) equals
+// (t * 4682) >> 16 (checked for every t of that range).
 __device__ __forceinline__ float q1_level(uint32_t blo, uint32_t bhi, int k)
 {
     if (k <= 0)
         return 0.0f;
-    const uint64_t num = (uint64_t)(bhi - blo) * (uint64_t)(k - 1) + 7u;
-    return __uint_as_float(blo + (uint32_t)(num / 14u));
+    const uint32_t d = bhi - blo, q = d / 14u, r = d - 14u * q, j = (uint32_t)(k - 1);
+    return __uint_as_float(blo + q * j + (((r * j + 7u) * 4682u) >> 16));
 }
 
 // binary exponent of a positive finite float given its bits
