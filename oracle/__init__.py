@@ -102,6 +102,8 @@ _SIGNATURES = {
                                         ctypes.POINTER(ctypes.c_int32)]),
     "oracle_turbo_step": (ctypes.c_uint64, [_f32p, _f32p, _i64, _u8p, _u16p, _f32p, _u8p, _u16p,
                                             *_HYP, ctypes.c_uint64]),
+    "oracle_turbo_step_at": (ctypes.c_uint64, [_f32p, _f32p, _i64, _u8p, _u16p, _f32p, _u8p, _u16p,
+                                               *_HYP, ctypes.c_uint64, ctypes.c_uint64]),
     "oracle_turbo_finalize": (None, [_f32p, _i64, _d]),
     "oracle_turbo_decode": (None, [_i64, _u8p, _u16p, _f32p, _u8p, _u16p, _i64, _d, _d, _d,
                                    _f32p, _f32p]),
@@ -381,9 +383,12 @@ def _turbo_methods():
         return out
 
     def turbo_step(self, p, g, state, step, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8,
-                   wd=0.01, seed=0x12345678):
+                   wd=0.01, seed=0x12345678, index0=0):
         """One TurboAdam-style step of one tensor; returns (p', state', nonfinite)
-        with state a dict of ucode, umean, uscal, vidx, vend (copied)."""
+        with state a dict of ucode, umean, uscal, vidx, vend (copied).  index0:
+        the arrays are the slice of a larger tensor from element index0 (a
+        multiple of 128) on, whose rounding counters take the tensor's indices."""
+        assert index0 % TURBO_BLOCK == 0
         p = _arr(p, np.float32)
         g = _arr(g, np.float32)
         n = p.size
@@ -392,11 +397,11 @@ def _turbo_methods():
         z = turbo_state_sizes(n)
         for k, size in z.items():
             assert st[k].size == size, (k, st[k].size, size)
-        bad = self.lib.oracle_turbo_step(
+        bad = self.lib.oracle_turbo_step_at(
             _ptr(p, ctypes.c_float), _ptr(g, ctypes.c_float), n, _ptr(st["ucode"], ctypes.c_uint8),
             _ptr(st["umean"], ctypes.c_uint16), _ptr(st["uscal"], ctypes.c_float),
             _ptr(st["vidx"], ctypes.c_uint8), _ptr(st["vend"], ctypes.c_uint16),
-            *_hyp(step, lr, beta1, beta2, eps, wd), ctypes.c_uint64(seed))
+            *_hyp(step, lr, beta1, beta2, eps, wd), ctypes.c_uint64(seed), ctypes.c_uint64(index0))
         return p, st, int(bad)
 
     def turbo_decode(self, state, n, step, beta1=0.9, beta2=0.999, eps=1e-8):

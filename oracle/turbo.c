@@ -332,10 +332,30 @@ static turbo_hyper make_hyper(int64_t step, double lr, double beta1, double beta
  * p is updated in place; returns the number of elements whose p', m or v is
  * not finite.  uscal[2] accumulates; call oracle_turbo_finalize after the step.
  */
+/* The step over elements index0 .. index0+n-1 of a tensor (index0 a multiple
+ * of the 128-value block; p, g and the state arrays start at element index0,
+ * block index0 / 128 and mean block index0 / 64): the rounding counters take
+ * the tensor's element indices.  Whole blocks are independent given the
+ * scales, so a slice is updated as in the whole tensor, except the RMS
+ * accumulator, which gathers the slice's squares only. */
+uint64_t oracle_turbo_step_at(float *p, const float *g, int64_t n, uint8_t *ucode, uint16_t *umean,
+                              float *uscal, uint8_t *vidx, uint16_t *vend, int64_t step,
+                              double lr, double beta1, double beta2, double eps, double wd,
+                              uint64_t seed, uint64_t index0);
+
 uint64_t oracle_turbo_step(float *p, const float *g, int64_t n, uint8_t *ucode, uint16_t *umean,
                            float *uscal, uint8_t *vidx, uint16_t *vend, int64_t step,
                            double lr, double beta1, double beta2, double eps, double wd,
                            uint64_t seed)
+{
+    return oracle_turbo_step_at(p, g, n, ucode, umean, uscal, vidx, vend, step, lr, beta1, beta2,
+                                eps, wd, seed, 0u);
+}
+
+uint64_t oracle_turbo_step_at(float *p, const float *g, int64_t n, uint8_t *ucode, uint16_t *umean,
+                              float *uscal, uint8_t *vidx, uint16_t *vend, int64_t step,
+                              double lr, double beta1, double beta2, double eps, double wd,
+                              uint64_t seed, uint64_t index0)
 {
     const int bits = 4;
     turbo_hyper h = make_hyper(step, lr, beta1, beta2, eps, wd);
@@ -380,7 +400,7 @@ uint64_t oracle_turbo_step(float *p, const float *g, int64_t n, uint8_t *ucode, 
         vend[2 * b + 1] = fp16_of_int(nhi);
         for (int64_t j = 0; j < cnt; ++j) {
             int64_t i = i0 + j;
-            float u = oracle_turbo_uniform(seed, step, 1, (uint64_t)i);
+            float u = oracle_turbo_uniform(seed, step, 1, index0 + (uint64_t)i);
             int vi = oracle_q1_index(vnew[j], nlo, nhi, bits, u);
             vidx[i / 2] = (uint8_t)((vidx[i / 2] & ~(15u << (4 * (i % 2)))) | ((unsigned)vi << (4 * (i % 2))));
             vhat[j] = oracle_q1_level(nlo, nhi, bits, vi);
@@ -404,7 +424,7 @@ uint64_t oracle_turbo_step(float *p, const float *g, int64_t n, uint8_t *ucode, 
             for (int64_t j = 0; j < c; ++j) {
                 int64_t i = i0 + k + j;
                 float r = qv[j] - mu;
-                float u = oracle_turbo_uniform(seed, step, 2, (uint64_t)i >> 1);
+                float u = oracle_turbo_uniform(seed, step, 2, (index0 + (uint64_t)i) >> 1);
                 if (i & 1)
                     u = 1.0f - u;
                 int code = oracle_ustate_code(r, senc, u);

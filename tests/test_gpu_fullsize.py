@@ -9,6 +9,7 @@ independent).  A full-array device check counts non-finite values and the
 state codes at the finite bound.
 gpt2-148: all 124,439,808 parameters, packed E4 and FP16, two steps, in full.
 blockwise-1e9: 64 sampled 2048-blocks (the short last block included).
+turbo-124m: 48 sampled slices of eight 128-value blocks over three steps.
 """
 import numpy as np
 import pytest
@@ -121,3 +122,51 @@ def test_blockwise_1e9_sampled(pa):
             assert_same_f32_nan_aware(w.v_absmax[blk:blk + 1].cpu().numpy(), va)
     del w
     torch.cuda.empty_cache()
+
+
+def test_turbo_124m_sampled(pa):
+    """turbo-124m (GPT-2 small's 124,439,808 parameters): three TurboAdam-style
+    steps at full size, the bench's launch; 48 sampled slices of eight
+    128-value blocks (the first and the short last one included) against the
+    oracle's step over each slice, its rounding counters at the tensor's
+    element indices (whole blocks are independent given the tensor's scales,
+    which every slice takes from the GPU's state before the step)."""
+    import torch
+
+    b = _bench()
+    w = b.Workload("turbo-124m", "turbo", torch.device("cuda"), seed=11)
+    n = w.n
+    run = b.step_fn(pa, w, wl.HYPER, None)
+    nb = -(-n // 128)
+    rng = np.random.default_rng(8)
+    starts = sorted(set((rng.integers(0, nb - 8, 46) * 128).tolist()) | {0, (nb - 1) * 128})
+
+    def host_state():
+        out = {}
+        for k in ("ucode", "umean", "uscal", "vidx", "vend"):
+            a = w.st[k].cpu().numpy()
+            out[k] = a.view(np.uint16) if a.dtype == np.int16 else a.copy()
+        return out
+
+    def cut(st, s0, length):
+        return {"ucode": st["ucode"][s0 // 4:(s0 + length + 3) // 4],
+                "umean": st["umean"][s0 // 64:(s0 + length + 63) // 64],
+                "vidx": st["vidx"][s0 // 2:(s0 + length + 1) // 2],
+                "vend": st["vend"][2 * (s0 // 128):2 * ((s0 + length + 127) // 128)]}
+
+    g = w.g.cpu().numpy()
+    for t in (1, 2, 3):
+        before, p = host_state(), w.p.cpu().numpy()
+        run(t)
+        torch.cuda.synchronize()
+        after, p_gpu = host_state(), w.p.cpu().numpy()
+        for s0 in starts:
+            length = min(1024, n - s0)
+            sl = cut(before, s0, length)
+            sl["uscal"] = before["uscal"].copy()
+            ps, sts, _ = oracle.turbo_step(p[s0:s0 + length], g[s0:s0 + length], sl, t,
+                                           index0=s0, **wl.HYPER)
+            assert_same_bits(p_gpu[s0:s0 + length], ps, f"turbo p, step {t}, slice {s0}")
+            got = cut(after, s0, length)
+            for k in got:
+                assert np.array_equal(got[k], sts[k]), (t, s0, k)

@@ -2,6 +2,7 @@
 in copies of turbo.c that the pins must catch."""
 import os
 
+import numpy as np
 import pytest
 
 import oracle
@@ -59,3 +60,34 @@ def test_turbo_pins_catch_planted_mistake(name, old, new, expect, tmp_path):
         except AssertionError:
             caught.append(pin)
     assert caught, f"planted mistake {name} passed every pin in {expect}"
+
+
+def test_turbo_slice_steps_as_in_the_whole_tensor():
+    """Whole 128-value blocks are independent given the tensor's scales: the
+    oracle's step over a slice (its rounding counters at the tensor's element
+    indices) gives the slice of the whole-tensor step, p and every state
+    array; only the RMS accumulator gathers the slice's squares alone."""
+    n = 128 * 40 + 45
+    rng = np.random.default_rng(21)
+    orc = oracle.Oracle()
+    p = rng.normal(0, 0.02, n).astype(np.float32)
+    st = oracle.turbo_zero_state(n)
+    for t in (1, 2, 3):
+        g = (rng.normal(0, 1e-3, n) * rng.choice([1.0, 10.0], n)).astype(np.float32)
+        p_next, st_next, _ = orc.turbo_step(p, g, st, t)
+        for s0, length in ((0, 1024), (128 * 7, 128 * 5), (128 * 39, n - 128 * 39)):
+            sl = {"ucode": st["ucode"][s0 // 4:(s0 + length + 3) // 4],
+                  "umean": st["umean"][s0 // 64:(s0 + length + 63) // 64],
+                  "uscal": st["uscal"].copy(),
+                  "vidx": st["vidx"][s0 // 2:(s0 + length + 1) // 2],
+                  "vend": st["vend"][2 * (s0 // 128):2 * ((s0 + length + 127) // 128)]}
+            ps, sts, _ = orc.turbo_step(p[s0:s0 + length], g[s0:s0 + length], sl, t, index0=s0)
+            assert np.array_equal(ps.view(np.uint32), p_next[s0:s0 + length].view(np.uint32))
+            for k in ("ucode", "umean", "vidx", "vend"):
+                whole = {"ucode": st_next["ucode"][s0 // 4:(s0 + length + 3) // 4],
+                         "umean": st_next["umean"][s0 // 64:(s0 + length + 63) // 64],
+                         "vidx": st_next["vidx"][s0 // 2:(s0 + length + 1) // 2],
+                         "vend": st_next["vend"][2 * (s0 // 128):2 * ((s0 + length + 127) // 128)]}[k]
+                assert np.array_equal(sts[k], whole), (t, s0, k)
+        st_next["uscal"] = orc.turbo_finalize(st_next["uscal"], n, 1.1)
+        p, st = p_next, st_next
