@@ -252,8 +252,13 @@ __device__ __forceinline__ void turbo_encode(const TurboArgs &a, const TurboScal
 #else
         L.p[j] = __fmaf_rn(L.p[j], s.dk, nupd);  // as adamw_element in this build
 #endif
-        if (WHOLE || j < valid)
+        if (!WHOLE && j < valid)
             bad += any_nonfinite(Moments{L.p[j], L.mn[j], L.vn[j]});
+    }
+    if (WHOLE) {  // the lane's four at once (packed FMAs; counted one by one only if any)
+        const Moments2 o[2] = {{make_float2(L.p[0], L.p[1]), make_float2(L.mn[0], L.mn[1]), make_float2(L.vn[0], L.vn[1])},
+                               {make_float2(L.p[2], L.p[3]), make_float2(L.mn[2], L.mn[3]), make_float2(L.vn[2], L.vn[3])}};
+        bad += nonfinite_count4(o);
     }
     // ---- 5. recompress v with 1Q: endpoints from the block's positive values
     int nlo = 0, nhi = 0;
