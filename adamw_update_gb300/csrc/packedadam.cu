@@ -136,7 +136,7 @@ __device__ __forceinline__ float2 decode_rms_pair(uint32_t w0, uint32_t w1)
     return mul2(make_float2(__uint_as_float(b0), __uint_as_float(b1)), make_float2(0x1p112f, 0x1p112f));
 }
 
-template <int MODE, bool UNIT_BC2, bool DEFER_NAN>
+template <int MODE, bool UNIT_BC2, bool DEFER_NAN, bool PAIRED>
 __device__ __forceinline__ uint4 packed_vector(float pp[4], const float gg[4], const uint4 w,
                                                const Scalars &s, const Pairs &k, const ZeroSafe &zs,
                                                uint32_t &bad)
@@ -154,7 +154,7 @@ __device__ __forceinline__ uint4 packed_vector(float pp[4], const float gg[4], c
                                      : make_float2(decode_fp16_high(ww[2 * j]), decode_fp16_high(ww[2 * j + 1]));
         v[j] = mul2(r, r);
     }
-    adamw_vector<UNIT_BC2, true>(p, g, m, v, s, k, zs, o, rn);
+    adamw_vector<UNIT_BC2, true, PAIRED>(p, g, m, v, s, k, zs, o, rn);
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
         pp[2 * j] = o[j].p.x;
@@ -541,8 +541,11 @@ __device__ __forceinline__ void pipe_produce(unsigned char *smem, uint64_t *full
 }
 
 // One staged 16-byte vector: elements e..e+3 of the stage buffer, which are
-// elements base+e.. of the tensor (warp-collective: adamw_vector).
-template <int MODE, bool U1, typename GT>
+// elements base+e.. of the tensor (warp-collective: adamw_vector).  PAIRED:
+// the branch-free arm in packed pairs (these vectors are issue-bound: 2.7 %
+// faster on gpt2-148; the graph-replayable kernel, which holds its scalars in
+// registers, spilled with it and keeps the scalar arm).
+template <int MODE, bool U1, typename GT, bool PAIRED>
 __device__ __forceinline__ void pipe_vector_math(const unsigned char *buf, int e, const Desc &d,
                                                  int64_t base, float pp[4], const float gg[4],
                                                  const Scalars &s, const ZeroSafe &zs,
@@ -559,7 +562,7 @@ __device__ __forceinline__ void pipe_vector_math(const unsigned char *buf, int e
         const float2 v[2] = {make_float2(vv.x, vv.y), make_float2(vv.z, vv.w)};
         Moments2 o[2];
         float2 unused[2];
-        adamw_vector<U1, false>(p, g, m, v, s, k, zs, o, unused);
+        adamw_vector<U1, false, PAIRED>(p, g, m, v, s, k, zs, o, unused);
         bad += nonfinite_count4(o);
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
@@ -573,12 +576,12 @@ __device__ __forceinline__ void pipe_vector_math(const unsigned char *buf, int e
         // (the E4 vectors here are issue-bound: NaN tests deferred, 2 % faster
         // on gpt2-148; the FP16 mode measured no gain)
         store_stream(static_cast<uint32_t *>(d.s1) + base + e,
-                     packed_vector<MODE, U1, MODE == kE4>(pp, gg, wv, s, k, zs, bad));
+                     packed_vector<MODE, U1, MODE == kE4, PAIRED>(pp, gg, wv, s, k, zs, bad));
     }
 }
 
 // One staged vector whose gradients gv are already loaded.
-template <int MODE, bool U1, typename GT>
+template <int MODE, bool U1, typename GT, bool PAIRED>
 __device__ __forceinline__ void pipe_vector_g(const unsigned char *buf, int e, const Desc &d,
                                               int64_t base, const float4 gv, const Scalars &s,
                                               const ZeroSafe &zs, uint32_t &bad)
@@ -586,7 +589,7 @@ __device__ __forceinline__ void pipe_vector_g(const unsigned char *buf, int e, c
     const float4 pv = *reinterpret_cast<const float4 *>(buf + 4 * e);
     float pp[4] = {pv.x, pv.y, pv.z, pv.w};
     const float gg[4] = {gv.x, gv.y, gv.z, gv.w};
-    pipe_vector_math<MODE, U1, GT>(buf, e, d, base, pp, gg, s, zs, bad);
+    pipe_vector_math<MODE, U1, GT, PAIRED>(buf, e, d, base, pp, gg, s, zs, bad);
     store_stream(d.p + base + e, make_float4(pp[0], pp[1], pp[2], pp[3]));
 }
 
@@ -636,7 +639,7 @@ __device__ __forceinline__ void compute_vec(const RegVec<MODE> &r, int e, const 
         const float2 v[2] = {make_float2(r.v.x, r.v.y), make_float2(r.v.z, r.v.w)};
         Moments2 o[2];
         float2 unused[2];
-        adamw_vector<U1, false>(p, g, m, v, s, pairs_of(s), zs, o, unused);
+        adamw_vector<U1, false, false>(p, g, m, v, s, pairs_of(s), zs, o, unused);
         bad += nonfinite_count4(o);
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
@@ -646,11 +649,13 @@ __device__ __forceinline__ void compute_vec(const RegVec<MODE> &r, int e, const 
         store_stream(static_cast<float *>(d.s1) + base + e, make_float4(o[0].m.x, o[0].m.y, o[1].m.x, o[1].m.y));
         store_stream(static_cast<float *>(d.s2) + base + e, make_float4(o[0].v.x, o[0].v.y, o[1].v.x, o[1].v.y));
     } else {
-        // (NaN tests deferred with bfloat16 gradients, whose whole tiles are
-        // issue-bound: 4 % faster; with FP32 gradients, bound by HBM, the same
-        // measured 3-5 % slower on the 7e9-parameter flat workload)
+        // (NaN tests deferred and the branch-free arm in packed pairs with
+        // bfloat16 gradients, whose whole tiles are issue-bound: 4 % and 6 %
+        // faster; with FP32 gradients, bound by HBM, each measured 3-5 %
+        // slower on the flat workload)
         store_stream(static_cast<uint32_t *>(d.s1) + base + e,
-                     packed_vector<MODE, U1, sizeof(GT) == 2>(pp, gg, r.w, s, pairs_of(s), zs, bad));
+                     packed_vector<MODE, U1, sizeof(GT) == 2, sizeof(GT) == 2>(pp, gg, r.w, s,
+                                                                                pairs_of(s), zs, bad));
     }
     store_stream(d.p + base + e, make_float4(pp[0], pp[1], pp[2], pp[3]));
 }
@@ -686,7 +691,7 @@ __device__ __forceinline__ uint32_t pipe_scalar_run(const Desc &d, int64_t first
     return bad;
 }
 
-template <int MODE, bool U1, typename GT>
+template <int MODE, bool U1, typename GT, bool PAIRED>
 __device__ __forceinline__ void pipe_consume(const unsigned char *smem, uint64_t *full,
                                              uint64_t *empty, int64_t total, const Scalars &s,
                                              uint32_t &bad)
@@ -754,14 +759,14 @@ __device__ __forceinline__ void pipe_consume(const unsigned char *smem, uint64_t
             } else if (fast) {
 #pragma unroll
                 for (int v = 0; v < kTileVecs; ++v)
-                    pipe_vector_g<MODE, U1, GT>(buf, 4 * (ct + v * kConsumers), d, sp.base,
+                    pipe_vector_g<MODE, U1, GT, PAIRED>(buf, 4 * (ct + v * kConsumers), d, sp.base,
                                                 gv[v], s, zs, bad);
             } else {
 #pragma unroll 1
                 for (int v = 0; v < kTileVecs; ++v) {
                     const int e = 4 * (ct + v * kConsumers);
                     if (e < sp.staged)
-                        pipe_vector_g<MODE, U1, GT>(buf, e, d, sp.base, staged_grad<GT>(buf, e), s,
+                        pipe_vector_g<MODE, U1, GT, PAIRED>(buf, e, d, sp.base, staged_grad<GT>(buf, e), s,
                                                     zs, bad);
                 }
             }
@@ -788,7 +793,7 @@ __device__ __forceinline__ void pipe_consume(const unsigned char *smem, uint64_t
 
 // table == nullptr: one tensor, described by `single` (ntensors == 1).  `tile`:
 // elements per tile (kTile, or fewer for a launch too small to fill the GPU).
-template <int MODE, bool U1, typename GT = float>
+template <int MODE, bool U1, typename GT = float, bool PAIRED = true>
 __device__ __forceinline__ void pipe_body(const Desc *__restrict__ table, int32_t ntensors,
                                           int64_t total_tiles, const Desc &single,
                                           const Scalars &s, unsigned long long *nonfinite,
@@ -830,7 +835,7 @@ __device__ __forceinline__ void pipe_body(const Desc *__restrict__ table, int32_
         return;
     }
     uint32_t bad = 0;
-    pipe_consume<MODE, U1, GT>(pipe_smem, full, empty, total_tiles, s, bad);
+    pipe_consume<MODE, U1, GT, PAIRED>(pipe_smem, full, empty, total_tiles, s, bad);
     flush_nonfinite(bad, nonfinite);
 }
 
@@ -862,7 +867,7 @@ adamw_step_table_kernel(const Desc *__restrict__ table, int32_t ntensors, int64_
     }
     const Scalars s = rows[i];
     Desc none = {};
-    pipe_body<MODE, false>(table, ntensors, total_tiles, none, s, nonfinite, kTile);
+    pipe_body<MODE, false, float, false>(table, ntensors, total_tiles, none, s, nonfinite, kTile);
 }
 
 __global__ void advance_index_kernel(int64_t *index)
@@ -1193,7 +1198,7 @@ __device__ __forceinline__ void blockwise_block(const BlockwiseArgs &a, Blockwis
             const float2 V2[2] = {make_float2(v[0], v[1]), make_float2(v[2], v[3])};
             Moments2 o2[2];
             float2 unused[2];
-            adamw_vector<false, false>(P2, G2, M2, V2, s, pairs_of(s), zs, o2, unused);
+            adamw_vector<false, false, false>(P2, G2, M2, V2, s, pairs_of(s), zs, o2, unused);
             if (WHOLE)
                 bad += nonfinite_count4(o2);
 #pragma unroll

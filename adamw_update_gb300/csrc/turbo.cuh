@@ -214,17 +214,6 @@ __device__ __forceinline__ float root_of_quotient(float x, float b, float rb)
     return __fsqrt_rn(__fdiv_rn(x, b));
 }
 
-// a / den for den > 0, IEEE or branch-free (the sign of a zero a kept)
-template <bool BF>
-__device__ __forceinline__ float over_den(float a, float den)
-{
-    if (BF) {
-        const float c = quotient_by_reciprocal(a, den, reciprocal_rn(den));
-        return __uint_as_float(__float_as_uint(c) | (__float_as_uint(a) & 0x80000000u));
-    }
-    return __fdiv_rn(a, den);
-}
-
 // What turbo_block carries from the moments to the recompression.
 struct TurboLane {
     float p[4], mn[4], vn[4];
@@ -242,18 +231,36 @@ __device__ __forceinline__ void turbo_encode(const TurboArgs &a, const TurboScal
 {
     const int lane = threadIdx.x & 31;
     const Scalars &s = ts.s;
-    // ---- 4. the update (the FP32 element of every mode)
+    // ---- 4. the update (the FP32 element of every mode; pairs of elements
+    //      in packed arithmetic, each lane the scalar operations' bits)
+    {
+        const Pairs k = pairs_of(s);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const float den = __fadd_rn(root_of_quotient<BF>(L.vn[j], s.bc2, f.rb2), s.ef);
-        const float nupd = over_den<BF>(__fmul_rn(-s.ss, L.mn[j]), den);
+        for (int j = 0; j < 4; j += 2) {
+            const float2 vn = make_float2(L.vn[j], L.vn[j + 1]);
+            const float2 nu = mul2(k.nss, make_float2(L.mn[j], L.mn[j + 1]));
+            float2 nupd;
+            if (BF) {
+                nupd = pair_update_branch_free<false>(vn, nu, k, make_float2(-s.bc2, -s.bc2),
+                                                      make_float2(f.rb2, f.rb2), nullptr);
+            } else {
+                nupd.x = __fdiv_rn(nu.x, __fadd_rn(root_of_quotient<false>(vn.x, s.bc2, f.rb2), s.ef));
+                nupd.y = __fdiv_rn(nu.y, __fadd_rn(root_of_quotient<false>(vn.y, s.bc2, f.rb2), s.ef));
+            }
 #ifndef PA_FAST_MATH
-        L.p[j] = __fadd_rn(__fmul_rn(L.p[j], s.dk), nupd);
+            const float2 pn = add2x(mul2(make_float2(L.p[j], L.p[j + 1]), k.dk), nupd, k.one);
 #else
-        L.p[j] = __fmaf_rn(L.p[j], s.dk, nupd);  // as adamw_element in this build
+            const float2 pn = fma2(make_float2(L.p[j], L.p[j + 1]), k.dk, nupd);  // as adamw_element
 #endif
-        if (!WHOLE && j < valid)
-            bad += any_nonfinite(Moments{L.p[j], L.mn[j], L.vn[j]});
+            L.p[j] = pn.x;
+            L.p[j + 1] = pn.y;
+        }
+        if (!WHOLE) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (j < valid)
+                    bad += any_nonfinite(Moments{L.p[j], L.mn[j], L.vn[j]});
+        }
     }
     if (WHOLE) {  // the lane's four at once (packed FMAs; counted one by one only if any)
         const Moments2 o[2] = {{make_float2(L.p[0], L.p[1]), make_float2(L.mn[0], L.mn[1]), make_float2(L.vn[0], L.vn[1])},
@@ -270,11 +277,20 @@ __device__ __forceinline__ void turbo_encode(const TurboArgs &a, const TurboScal
     }
     const uint32_t nblo = pow2_bits(nlo), nbhi = pow2_bits(nhi);
     // lane k holds level k of the new grid and the encode's denominator for it,
-    // sqrt(level / bc2) + eps (the same value for every element that takes it)
-    const float mylevel = q1_level(nblo, nbhi, lane < 16 ? lane : 15);
+    // sqrt(level / bc2) + eps (the same value for every element that takes it);
+    // on the branch-free arm also the reciprocals that the elements' quotients
+    // take: RN(1/den) and, for k < 15, RN(1/(level k+1 - level k)) with that gap
+    const int mylane = lane < 16 ? lane : 15;
+    const float mylevel = q1_level(nblo, nbhi, mylane);
     const float myden = __fadd_rn(root_of_quotient<BF>(mylevel, s.bc2, f.rb2), s.ef);
+    float myrden = 0.0f, mygap = 0.0f, myrgap = 0.0f;
+    if (BF) {
+        myrden = reciprocal_rn(myden);
+        mygap = __fsub_rn(q1_level(nblo, nbhi, mylane < 15 ? mylane + 1 : 15), mylevel);
+        myrgap = reciprocal_rn(mygap > 0.0f ? mygap : 1.0f);
+    }
     uint32_t nvhalf = 0;
-    float den5[4];
+    float den5[4], rden5[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const float v = L.vn[j];
@@ -287,19 +303,27 @@ __device__ __forceinline__ void turbo_encode(const TurboArgs &a, const TurboScal
             k = __shfl_sync(0xFFFFFFFFu, mylevel, c) <= v ? c : k;
         }
         const float dj = __shfl_sync(0xFFFFFFFFu, mylevel, k);
-        const float dn = __shfl_sync(0xFFFFFFFFu, mylevel, k < 15 ? k + 1 : 15);
         int idx = 0;
-        if (v > 0.0f) {
-            idx = k;
-            if (!(v == dj || k == 15)) {
-                const float b = __fsub_rn(dn, dj);
-                const float frac = BF ? quotient_by_reciprocal(__fsub_rn(v, dj), b, reciprocal_rn(b))
-                                      : __fdiv_rn(__fsub_rn(v, dj), b);
-                idx = u1[j] < frac ? k + 1 : k;
+        if (BF) {
+            const float b = __shfl_sync(0xFFFFFFFFu, mygap, k);
+            const float rb = __shfl_sync(0xFFFFFFFFu, myrgap, k);
+            if (v > 0.0f) {
+                idx = k;
+                if (!(v == dj || k == 15))
+                    idx = u1[j] < quotient_by_reciprocal(__fsub_rn(v, dj), b, rb) ? k + 1 : k;
+            }
+        } else {
+            const float dn = __shfl_sync(0xFFFFFFFFu, mylevel, k < 15 ? k + 1 : 15);
+            if (v > 0.0f) {
+                idx = k;
+                if (!(v == dj || k == 15))
+                    idx = u1[j] < __fdiv_rn(__fsub_rn(v, dj), __fsub_rn(dn, dj)) ? k + 1 : k;
             }
         }
         nvhalf |= (uint32_t)idx << (4 * j);
         den5[j] = __shfl_sync(0xFFFFFFFFu, myden, idx);
+        if (BF)
+            rden5[j] = __shfl_sync(0xFFFFFFFFu, myrden, idx);
     }
     // ---- 6. encode the next UState payload
     float q[4];
@@ -310,7 +334,12 @@ __device__ __forceinline__ void turbo_encode(const TurboArgs &a, const TurboScal
             const float t = BF ? __uint_as_float(__float_as_uint(quotient_by_reciprocal(L.mn[j], ts.bc1, f.rb1)) |
                                                  (__float_as_uint(L.mn[j]) & 0x80000000u))
                                : __fdiv_rn(L.mn[j], ts.bc1);
-            q[j] = over_den<BF>(t, den);
+            if (BF) {
+                const float c = quotient_by_reciprocal(t, den, rden5[j]);
+                q[j] = __uint_as_float(__float_as_uint(c) | (__float_as_uint(t) & 0x80000000u));
+            } else {
+                q[j] = __fdiv_rn(t, den);
+            }
         } else {
             q[j] = 0.0f;  // missing positions of a short block count as 0
         }
@@ -475,24 +504,41 @@ __device__ __forceinline__ void turbo_block(const TurboArgs &a, const TurboScala
         oldden = __fadd_rn(f.okp && lo >= -100 && hi <= 99 ? root_of_quotient<true>(oldlevel, ts.bc2p, f.rb2p)
                                                             : root_of_quotient<false>(oldlevel, ts.bc2p, f.rb2p),
                            s.ef);
+    // the recentred value mu + (sdec * level(c) - delta) of UState code c,
+    // held by lane c of each half-warp (its mean block's) and fetched by shuffle
+    const float qcode = __fadd_rn(mu, __fsub_rn(__fmul_rn(sdec, ulevel((uint32_t)lane & 3u)), delta));
     float mprev[4], vdec[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const int idx = (int)((vhalf >> (4 * j)) & 15u);
         const float v = __shfl_sync(0xFFFFFFFFu, oldlevel, idx);
         const float den = __shfl_sync(0xFFFFFFFFu, oldden, idx);
-        const float d = __fmul_rn(sdec, ulevel((cbyte >> (2 * j)) & 3u));
-        const float q = __fadd_rn(mu, __fsub_rn(d, delta));
+        const float q = __shfl_sync(0xFFFFFFFFu, qcode, (lane & 16) | (int)((cbyte >> (2 * j)) & 3u));
         mprev[j] = ts.step > 1 ? __fmul_rn(__fmul_rn(q, den), ts.bc1p) : 0.0f;
         vdec[j] = v;
     }
-    // ---- 3. the fp32 moments; the block's v' range; each lane's |m'| range
+    // ---- 3. the fp32 moments (pairs of elements in packed arithmetic, each
+    //      lane the scalar b1*m + c1*g and b2*v + (c2*g)*g); the block's v'
+    //      range; each lane's |m'| range
+    {
+        const float2 one = one_pair();
+        const float2 b1 = make_float2(s.b1, s.b1), c1 = make_float2(s.c1, s.c1);
+        const float2 b2 = make_float2(s.b2, s.b2), c2 = make_float2(s.c2, s.c2);
+#pragma unroll
+        for (int j = 0; j < 4; j += 2) {
+            const float2 gp = make_float2(g[j], g[j + 1]);
+            const float2 mn = add2x(mul2(b1, make_float2(mprev[j], mprev[j + 1])), mul2(c1, gp), one);
+            const float2 vn = add2x(mul2(b2, make_float2(vdec[j], vdec[j + 1])), mul2(mul2(c2, gp), gp), one);
+            L.mn[j] = mn.x;
+            L.mn[j + 1] = mn.y;
+            L.vn[j] = vn.x;
+            L.vn[j + 1] = vn.y;
+        }
+    }
     uint32_t pmin = 0xFFFFFFFFu, pmax = 0u, vall = 0u;
     float mlo = INFINITY, mhi = 0.0f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        L.mn[j] = __fadd_rn(__fmul_rn(s.b1, mprev[j]), __fmul_rn(s.c1, g[j]));
-        L.vn[j] = __fadd_rn(__fmul_rn(s.b2, vdec[j]), __fmul_rn(__fmul_rn(s.c2, g[j]), g[j]));
         const uint32_t bits = __float_as_uint(L.vn[j]);
         if (WHOLE || j < valid) {
             const bool pos = L.vn[j] > 0.0f && bits < 0x7F800000u;

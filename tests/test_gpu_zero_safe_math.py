@@ -60,14 +60,16 @@ def test_residual_root_equals_ieee_on_its_range(lib):
     assert count.value == 0, (count.value, [hex(x) for x in first])
 
 
+@pytest.mark.parametrize("paired", [0, 1])
 @pytest.mark.parametrize("unit_bc2", [0, 1])
-def test_vector_arithmetic_equals_element(lib, unit_bc2):
+def test_vector_arithmetic_equals_element(lib, unit_bc2, paired):
     nwarps = 1 << 22
     count = ctypes.c_ulonglong(0)
     branch_free = ctypes.c_ulonglong(0)
     first = (ctypes.c_uint32 * 4)()
-    assert lib.run_vectors(ctypes.c_int(unit_bc2), ctypes.c_uint64(nwarps), ctypes.c_uint64(23),
-                           ctypes.byref(count), first, ctypes.byref(branch_free)) == 0
+    assert lib.run_vectors(ctypes.c_int(unit_bc2), ctypes.c_int(paired), ctypes.c_uint64(nwarps),
+                           ctypes.c_uint64(23), ctypes.byref(count), first,
+                           ctypes.byref(branch_free)) == 0
     assert count.value == 0, (count.value, [hex(x) for x in first])
     # both arms ran: about half of the warps are drawn in range
     assert nwarps // 5 < branch_free.value < nwarps * 4 // 5, branch_free.value
