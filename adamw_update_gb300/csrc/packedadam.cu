@@ -625,7 +625,7 @@ __device__ __forceinline__ RegVec<MODE> load_vec(const unsigned char *buf, int e
 // gradients (that step is issue-bound), once the roots took their zero case
 // by an add and the non-finite count went to packed FMAs (before that, 2.6 %
 // slower on the flat workload).
-template <int MODE, bool U1, typename GT>
+template <int MODE, bool U1, typename GT, bool PAIRED>
 __device__ __forceinline__ void compute_vec(const RegVec<MODE> &r, int e, const Desc &d,
                                             int64_t base, const Scalars &s, const ZeroSafe &zs,
                                             uint32_t &bad)
@@ -639,7 +639,7 @@ __device__ __forceinline__ void compute_vec(const RegVec<MODE> &r, int e, const 
         const float2 v[2] = {make_float2(r.v.x, r.v.y), make_float2(r.v.z, r.v.w)};
         Moments2 o[2];
         float2 unused[2];
-        adamw_vector<U1, false, false>(p, g, m, v, s, pairs_of(s), zs, o, unused);
+        adamw_vector<U1, false, PAIRED>(p, g, m, v, s, pairs_of(s), zs, o, unused);
         bad += nonfinite_count4(o);
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
@@ -654,8 +654,8 @@ __device__ __forceinline__ void compute_vec(const RegVec<MODE> &r, int e, const 
         // faster; with FP32 gradients, bound by HBM, each measured 3-5 %
         // slower on the flat workload)
         store_stream(static_cast<uint32_t *>(d.s1) + base + e,
-                     packed_vector<MODE, U1, sizeof(GT) == 2, sizeof(GT) == 2>(pp, gg, r.w, s,
-                                                                                pairs_of(s), zs, bad));
+                     packed_vector<MODE, U1, sizeof(GT) == 2, PAIRED || sizeof(GT) == 2>(
+                         pp, gg, r.w, s, pairs_of(s), zs, bad));
     }
     store_stream(d.p + base + e, make_float4(pp[0], pp[1], pp[2], pp[3]));
 }
@@ -691,7 +691,10 @@ __device__ __forceinline__ uint32_t pipe_scalar_run(const Desc &d, int64_t first
     return bad;
 }
 
-template <int MODE, bool U1, typename GT, bool PAIRED>
+// PAIR: 0 the branch-free arithmetic one lane at a time everywhere; 1 in
+// packed pairs on the per-vector path (and, as always, with bfloat16
+// gradients); 2 in packed pairs on the whole tiles too.
+template <int MODE, bool U1, typename GT, int PAIR>
 __device__ __forceinline__ void pipe_consume(const unsigned char *smem, uint64_t *full,
                                              uint64_t *empty, int64_t total, const Scalars &s,
                                              uint32_t &bad)
@@ -755,18 +758,19 @@ __device__ __forceinline__ void pipe_consume(const unsigned char *smem, uint64_t
                 released = true;
 #pragma unroll
                 for (int v = 0; v < kTileVecs; ++v)
-                    compute_vec<MODE, U1, GT>(rv[v], 4 * (ct + v * kConsumers), d, sp.base, s, zs, bad);
+                    compute_vec<MODE, U1, GT, PAIR == 2>(rv[v], 4 * (ct + v * kConsumers), d, sp.base,
+                                                         s, zs, bad);
             } else if (fast) {
 #pragma unroll
                 for (int v = 0; v < kTileVecs; ++v)
-                    pipe_vector_g<MODE, U1, GT, PAIRED>(buf, 4 * (ct + v * kConsumers), d, sp.base,
+                    pipe_vector_g<MODE, U1, GT, (PAIR >= 1)>(buf, 4 * (ct + v * kConsumers), d, sp.base,
                                                 gv[v], s, zs, bad);
             } else {
 #pragma unroll 1
                 for (int v = 0; v < kTileVecs; ++v) {
                     const int e = 4 * (ct + v * kConsumers);
                     if (e < sp.staged)
-                        pipe_vector_g<MODE, U1, GT, PAIRED>(buf, e, d, sp.base, staged_grad<GT>(buf, e), s,
+                        pipe_vector_g<MODE, U1, GT, (PAIR >= 1)>(buf, e, d, sp.base, staged_grad<GT>(buf, e), s,
                                                     zs, bad);
                 }
             }
@@ -793,7 +797,7 @@ __device__ __forceinline__ void pipe_consume(const unsigned char *smem, uint64_t
 
 // table == nullptr: one tensor, described by `single` (ntensors == 1).  `tile`:
 // elements per tile (kTile, or fewer for a launch too small to fill the GPU).
-template <int MODE, bool U1, typename GT = float, bool PAIRED = true>
+template <int MODE, bool U1, typename GT = float, int PAIR = 1>
 __device__ __forceinline__ void pipe_body(const Desc *__restrict__ table, int32_t ntensors,
                                           int64_t total_tiles, const Desc &single,
                                           const Scalars &s, unsigned long long *nonfinite,
@@ -835,17 +839,17 @@ __device__ __forceinline__ void pipe_body(const Desc *__restrict__ table, int32_
         return;
     }
     uint32_t bad = 0;
-    pipe_consume<MODE, U1, GT, PAIRED>(pipe_smem, full, empty, total_tiles, s, bad);
+    pipe_consume<MODE, U1, GT, PAIR>(pipe_smem, full, empty, total_tiles, s, bad);
     flush_nonfinite(bad, nonfinite);
 }
 
-template <int MODE, bool U1, typename GT = float>
+template <int MODE, bool U1, typename GT = float, int PAIR = 1>
 __global__ void __launch_bounds__(kPipeThreads, 1)
 adamw_step_pipe_kernel(const Desc *__restrict__ table, int32_t ntensors, int64_t total_tiles,
                        const Desc single, const Scalars s, unsigned long long *nonfinite,
                        int32_t tile)
 {
-    pipe_body<MODE, U1, GT>(table, ntensors, total_tiles, single, s, nonfinite, tile);
+    pipe_body<MODE, U1, GT, PAIR>(table, ntensors, total_tiles, single, s, nonfinite, tile);
 }
 
 // Graph-replayable variant: the scalars of the step are row *index of a
@@ -867,7 +871,7 @@ adamw_step_table_kernel(const Desc *__restrict__ table, int32_t ntensors, int64_
     }
     const Scalars s = rows[i];
     Desc none = {};
-    pipe_body<MODE, false, float, false>(table, ntensors, total_tiles, none, s, nonfinite, kTile);
+    pipe_body<MODE, false, float, 0>(table, ntensors, total_tiles, none, s, nonfinite, kTile);
 }
 
 __global__ void advance_index_kernel(int64_t *index)
@@ -1747,6 +1751,63 @@ pa_status launch_tile(int64_t tiles, int64_t elements, int32_t *tile)
     return PA_OK;
 }
 
+// Launch the staged step over `tiles` tiles (table == nullptr: the one tensor
+// `single`).  A launch of fewer than kPairedTileRounds tiles per CTA takes the
+// instantiation whose whole tiles also run the branch-free arithmetic in
+// packed pairs (PAIR 2): measured on GB300, the 9.7M-parameter gpt-52 list
+// 4 % faster that way, a 2^28-parameter flat tensor 4 % slower (HBM-bound,
+// its whole tiles keep the scalar arm).  Bfloat16 gradients always pair.
+constexpr int64_t kPairedTileRounds = 32;
+
+template <int MODE, typename GT, bool U1, int PAIR>
+void launch_pipe_as(int grid, size_t used, const Desc *table, int32_t ntensors, int64_t tiles,
+                    const Desc &single, const Scalars &s, unsigned long long *nonfinite,
+                    int32_t tile, pa_stream stream)
+{
+    pa::adamw_step_pipe_kernel<MODE, U1, GT, PAIR><<<grid, pa::kPipeThreads, used, (cudaStream_t)stream>>>(
+        table, ntensors, tiles, single, s, nonfinite, tile);
+}
+
+template <int MODE, typename GT>
+pa_status launch_pipe(const Desc *table, int32_t ntensors, int64_t tiles, const Desc &single,
+                      const Scalars &s, unsigned long long *nonfinite, int32_t tile, size_t used,
+                      pa_stream stream)
+{
+    const size_t smem = pa::PipeLayout<MODE, GT>::kBytes;  // the kernel's limit
+    const bool u1 = s.bc2 == 1.0f;
+    int grid = 0;
+    pa_status st = pipe_grid(u1 ? (const void *)pa::adamw_step_pipe_kernel<MODE, true, GT>
+                                : (const void *)pa::adamw_step_pipe_kernel<MODE, false, GT>,
+                             smem, tiles, &grid);
+    if (st != PA_OK)
+        return st;
+    if constexpr (sizeof(GT) == 4) {
+        if (tiles < kPairedTileRounds * (int64_t)grid) {
+            // same shared memory and block; its own attribute and occupancy check
+            int g2 = 0;
+            st = pipe_grid(u1 ? (const void *)pa::adamw_step_pipe_kernel<MODE, true, GT, 2>
+                              : (const void *)pa::adamw_step_pipe_kernel<MODE, false, GT, 2>,
+                           smem, tiles, &g2);
+            if (st != PA_OK)
+                return st;
+            grid = g2 < grid ? g2 : grid;
+            if (u1)
+                launch_pipe_as<MODE, GT, true, 2>(grid, used, table, ntensors, tiles, single, s,
+                                                  nonfinite, tile, stream);
+            else
+                launch_pipe_as<MODE, GT, false, 2>(grid, used, table, ntensors, tiles, single, s,
+                                                   nonfinite, tile, stream);
+            return PA_OK;
+        }
+    }
+    if (u1) {
+        launch_pipe_as<MODE, GT, true, 1>(grid, used, table, ntensors, tiles, single, s, nonfinite, tile, stream);
+    } else {
+        launch_pipe_as<MODE, GT, false, 1>(grid, used, table, ntensors, tiles, single, s, nonfinite, tile, stream);
+    }
+    return PA_OK;
+}
+
 pa_status check_launch(const char *what)
 {
     cudaError_t e = cudaGetLastError();
@@ -1837,19 +1898,9 @@ pa_status step_single(const pa_tensor &t, int64_t step, double lr, double beta1,
     if (tile != pa::kTile)
         tiles = describe(t, MODE, tile, &d, (int)sizeof(GT));
     d.chunk0 = 0;
-    const size_t smem = pa::PipeLayout<MODE, GT>::kBytes;  // the kernel's limit
     const size_t used = pa::PipeLayout<MODE, GT>::bytes_for(1);  // the descriptor, by value
-    const void *kern = s.bc2 == 1.0f ? (const void *)pa::adamw_step_pipe_kernel<MODE, true, GT>
-                                     : (const void *)pa::adamw_step_pipe_kernel<MODE, false, GT>;
-    int grid = 0;
-    if ((st = pipe_grid(kern, smem, tiles, &grid)) != PA_OK)
+    if ((st = launch_pipe<MODE, GT>(nullptr, 1, tiles, d, s, nonfinite, tile, used, stream)) != PA_OK)
         return st;
-    if (s.bc2 == 1.0f)
-        pa::adamw_step_pipe_kernel<MODE, true, GT><<<grid, pa::kPipeThreads, used, (cudaStream_t)stream>>>(
-            nullptr, 1, tiles, d, s, nonfinite, tile);
-    else
-        pa::adamw_step_pipe_kernel<MODE, false, GT><<<grid, pa::kPipeThreads, used, (cudaStream_t)stream>>>(
-            nullptr, 1, tiles, d, s, nonfinite, tile);
     return check_launch("adamw_step_pipe_kernel launch");
 }
 
@@ -1989,19 +2040,10 @@ pa_status step_multi(const pa_tensor *list, int32_t ntensors, int64_t step, doub
         return st;
     if ((st = table_for(list, ntensors, MODE, tile, &table, &tiles, (int)sizeof(GT))) != PA_OK)
         return st;
-    const size_t smem = pa::PipeLayout<MODE, GT>::kBytes;  // the kernel's limit
     const size_t used = pa::PipeLayout<MODE, GT>::bytes_for(ntensors);
-    const void *kern = s.bc2 == 1.0f ? (const void *)pa::adamw_step_pipe_kernel<MODE, true, GT>
-                                     : (const void *)pa::adamw_step_pipe_kernel<MODE, false, GT>;
-    int grid = 0;
-    if ((st = pipe_grid(kern, smem, tiles, &grid)) != PA_OK)
+    if ((st = launch_pipe<MODE, GT>(table, ntensors, tiles, none, s, nonfinite, tile, used, stream)) !=
+        PA_OK)
         return st;
-    if (s.bc2 == 1.0f)
-        pa::adamw_step_pipe_kernel<MODE, true, GT><<<grid, pa::kPipeThreads, used, (cudaStream_t)stream>>>(
-            table, ntensors, tiles, none, s, nonfinite, tile);
-    else
-        pa::adamw_step_pipe_kernel<MODE, false, GT><<<grid, pa::kPipeThreads, used, (cudaStream_t)stream>>>(
-            table, ntensors, tiles, none, s, nonfinite, tile);
     return check_launch("adamw_step_pipe_kernel (multi) launch");
 }
 
