@@ -214,6 +214,14 @@ __device__ __forceinline__ float root_of_quotient(float x, float b, float rb)
     return __fsqrt_rn(__fdiv_rn(x, b));
 }
 
+// c with the sign bits of a ORed in, lane by lane (a zero quotient keeps its
+// dividend's sign; the divisors are positive)
+__device__ __forceinline__ float2 with_sign_of(float2 c, float2 a)
+{
+    return make_float2(__uint_as_float(__float_as_uint(c.x) | (__float_as_uint(a.x) & 0x80000000u)),
+                       __uint_as_float(__float_as_uint(c.y) | (__float_as_uint(a.y) & 0x80000000u)));
+}
+
 // What turbo_block carries from the moments to the recompression.
 struct TurboLane {
     float p[4], mn[4], vn[4];
@@ -289,6 +297,9 @@ __device__ __forceinline__ void turbo_encode(const TurboArgs &a, const TurboScal
         mygap = __fsub_rn(q1_level(nblo, nbhi, mylane < 15 ? mylane + 1 : 15), mylevel);
         myrgap = reciprocal_rn(mygap > 0.0f ? mygap : 1.0f);
     }
+    // (the branch-free arm fetches the negated denominator: its quotients take
+    // the divisor negated, exact.cuh's pair forms)
+    const float mysel = BF ? -myden : myden;
     uint32_t nvhalf = 0;
     float den5[4], rden5[4];
 #pragma unroll
@@ -321,27 +332,40 @@ __device__ __forceinline__ void turbo_encode(const TurboArgs &a, const TurboScal
             }
         }
         nvhalf |= (uint32_t)idx << (4 * j);
-        den5[j] = __shfl_sync(0xFFFFFFFFu, myden, idx);
+        den5[j] = __shfl_sync(0xFFFFFFFFu, mysel, idx);  // BF: -den
         if (BF)
             rden5[j] = __shfl_sync(0xFFFFFFFFu, myrden, idx);
     }
-    // ---- 6. encode the next UState payload
+    // ---- 6. encode the next UState payload: q = (m'/bc1)/den
     float q[4];
+    if (WHOLE && BF) {  // pairs of elements (each lane the scalar form's bits)
+        const float2 nbc1 = make_float2(-ts.bc1, -ts.bc1), rb1 = make_float2(f.rb1, f.rb1);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        if (WHOLE || j < valid) {
-            const float den = den5[j];
-            const float t = BF ? __uint_as_float(__float_as_uint(quotient_by_reciprocal(L.mn[j], ts.bc1, f.rb1)) |
-                                                 (__float_as_uint(L.mn[j]) & 0x80000000u))
-                               : __fdiv_rn(L.mn[j], ts.bc1);
-            if (BF) {
-                const float c = quotient_by_reciprocal(t, den, rden5[j]);
-                q[j] = __uint_as_float(__float_as_uint(c) | (__float_as_uint(t) & 0x80000000u));
+        for (int j = 0; j < 4; j += 2) {
+            const float2 mn = make_float2(L.mn[j], L.mn[j + 1]);
+            const float2 t = with_sign_of(quotient_by_reciprocal2(mn, nbc1, rb1), mn);
+            const float2 c = with_sign_of(quotient_by_reciprocal2(t, make_float2(den5[j], den5[j + 1]),
+                                                                  make_float2(rden5[j], rden5[j + 1])),
+                                          t);
+            q[j] = c.x;
+            q[j + 1] = c.y;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (WHOLE || j < valid) {
+                const float t = BF ? __uint_as_float(__float_as_uint(quotient_by_reciprocal(L.mn[j], ts.bc1, f.rb1)) |
+                                                     (__float_as_uint(L.mn[j]) & 0x80000000u))
+                                   : __fdiv_rn(L.mn[j], ts.bc1);
+                if (BF) {
+                    const float c = quotient_by_reciprocal(t, -den5[j], rden5[j]);
+                    q[j] = __uint_as_float(__float_as_uint(c) | (__float_as_uint(t) & 0x80000000u));
+                } else {
+                    q[j] = __fdiv_rn(t, den5[j]);
+                }
             } else {
-                q[j] = __fdiv_rn(t, den);
+                q[j] = 0.0f;  // missing positions of a short block count as 0
             }
-        } else {
-            q[j] = 0.0f;  // missing positions of a short block count as 0
         }
     }
     const float tree = half_warp_tree(__fadd_rn(__fadd_rn(q[0], q[1]), __fadd_rn(q[2], q[3])));
@@ -355,19 +379,35 @@ __device__ __forceinline__ void turbo_encode(const TurboArgs &a, const TurboScal
     const float mub = __uint_as_float((uint32_t)mbits << 16);
     uint32_t ncbyte = cbyte;
     float rsum = 0.0f;
+    if (WHOLE && BF && f.sok) {  // (f.sok is uniform over the launch)
+        // pairs: r = q - mean, y = r / senc, r*r; codes and the sum in order
+        const float2 one = one_pair(), nmub = make_float2(-mub, -mub);
+        const float2 nsenc = make_float2(-senc, -senc), rs = make_float2(f.rs, f.rs);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        if (WHOLE || j < valid) {
-            const float r = __fsub_rn(q[j], mub);
-            const float u = (j & 1) ? __fsub_rn(1.0f, upair[j >> 1]) : upair[j >> 1];
-            float y;
-            if (BF && f.sok)  // uniform over the launch (|r| < 2^86 needs the BF bounds)
-                y = quotient_by_reciprocal(r, senc, f.rs);
-            else
-                y = senc > 0.0f ? __fdiv_rn(r, senc) : 0.0f;
-            const uint32_t c = ustate_code_of(y, u);
-            ncbyte = (ncbyte & ~(3u << (2 * j))) | (c << (2 * j));
-            rsum = __fadd_rn(rsum, __fmul_rn(r, r));
+        for (int j = 0; j < 4; j += 2) {
+            const float2 r = add2x(make_float2(q[j], q[j + 1]), nmub, one);
+            const float2 y = quotient_by_reciprocal2(r, nsenc, rs);
+            const float2 rr = mul2(r, r);
+            const uint32_t c0 = ustate_code_of(y.x, upair[j >> 1]);
+            const uint32_t c1 = ustate_code_of(y.y, __fsub_rn(1.0f, upair[j >> 1]));
+            ncbyte = (ncbyte & ~(15u << (2 * j))) | (c0 << (2 * j)) | (c1 << (2 * j + 2));
+            rsum = __fadd_rn(__fadd_rn(rsum, rr.x), rr.y);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (WHOLE || j < valid) {
+                const float r = __fsub_rn(q[j], mub);
+                const float u = (j & 1) ? __fsub_rn(1.0f, upair[j >> 1]) : upair[j >> 1];
+                float y;
+                if (BF && f.sok)  // uniform over the launch (|r| < 2^86 needs the BF bounds)
+                    y = quotient_by_reciprocal(r, senc, f.rs);
+                else
+                    y = senc > 0.0f ? __fdiv_rn(r, senc) : 0.0f;
+                const uint32_t c = ustate_code_of(y, u);
+                ncbyte = (ncbyte & ~(3u << (2 * j))) | (c << (2 * j));
+                rsum = __fadd_rn(rsum, __fmul_rn(r, r));
+            }
         }
     }
     // ---- stores
