@@ -603,9 +603,10 @@ __device__ __forceinline__ void turbo_block(const TurboArgs &a, const TurboScala
                                    pmin, pmax, u1, upair, bad, racc);
 }
 
-// (64 registers, four CTAs per SM: 4 % faster on GB300 than the 80 registers
-// and three CTAs the compiler picks unbounded; five CTAs lost it again.)
-__global__ void __launch_bounds__(kTurboThreads, 4)
+// (three CTAs per SM with up to 80 registers: 2.3 % faster on GB300 than four
+// CTAs at 64 registers once the update and the UState encode ran in packed
+// pairs; before them four CTAs had been 4 % faster, and five lost again.)
+__global__ void __launch_bounds__(kTurboThreads, 3)
 turbo_step_kernel(const TurboArgs a, const TurboScalars ts, unsigned long long *nonfinite)
 {
     const float sdec = a.uscal[0], senc = a.uscal[1];
