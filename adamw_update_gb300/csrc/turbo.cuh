@@ -297,33 +297,52 @@ __device__ __forceinline__ void turbo_encode(const TurboArgs &a, const TurboScal
         mygap = __fsub_rn(q1_level(nblo, nbhi, mylane < 15 ? mylane + 1 : 15), mylevel);
         myrgap = reciprocal_rn(mygap > 0.0f ? mygap : 1.0f);
     }
-    // (the branch-free arm fetches the negated denominator: its quotients take
-    // the divisor negated, exact.cuh's pair forms)
+    // (the branch-free arm fetches negated levels, gaps and denominators: its
+    // quotients take the divisor negated, exact.cuh's pair forms)
     const float mysel = BF ? -myden : myden;
     uint32_t nvhalf = 0;
     float den5[4], rden5[4];
+    int kk[4];
+    float ndj[4], ngap[4], rgap[4], frac[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const float v = L.vn[j];
         // k = the number of levels 1..15 at most v: for positive v (>= level
         // 1) the largest such level; the probes stay within 1..15
         int k = 0;
 #pragma unroll
         for (int step = 8; step >= 1; step >>= 1) {
             const int c = k + step;
-            k = __shfl_sync(0xFFFFFFFFu, mylevel, c) <= v ? c : k;
+            k = __shfl_sync(0xFFFFFFFFu, mylevel, c) <= L.vn[j] ? c : k;
         }
-        const float dj = __shfl_sync(0xFFFFFFFFu, mylevel, k);
+        kk[j] = k;
+        if (BF) {
+            ndj[j] = __shfl_sync(0xFFFFFFFFu, -mylevel, k);
+            ngap[j] = __shfl_sync(0xFFFFFFFFu, -mygap, k);
+            rgap[j] = __shfl_sync(0xFFFFFFFFu, myrgap, k);
+        }
+    }
+    if (BF) {  // the fractions (v - level k) / gap k of all four, in pairs
+        const float2 one = one_pair();
+#pragma unroll
+        for (int j = 0; j < 4; j += 2) {
+            const float2 d = add2x(make_float2(L.vn[j], L.vn[j + 1]), make_float2(ndj[j], ndj[j + 1]), one);
+            const float2 fr = quotient_by_reciprocal2(d, make_float2(ngap[j], ngap[j + 1]),
+                                                      make_float2(rgap[j], rgap[j + 1]));
+            frac[j] = fr.x;
+            frac[j + 1] = fr.y;
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float v = L.vn[j];
+        const int k = kk[j];
         int idx = 0;
         if (BF) {
-            const float b = __shfl_sync(0xFFFFFFFFu, mygap, k);
-            const float rb = __shfl_sync(0xFFFFFFFFu, myrgap, k);
-            if (v > 0.0f) {
-                idx = k;
-                if (!(v == dj || k == 15))
-                    idx = u1[j] < quotient_by_reciprocal(__fsub_rn(v, dj), b, rb) ? k + 1 : k;
-            }
+            // (level 0 and a zero gap give fractions that are not used)
+            if (v > 0.0f)
+                idx = (v == -ndj[j] || k == 15) ? k : (u1[j] < frac[j] ? k + 1 : k);
         } else {
+            const float dj = __shfl_sync(0xFFFFFFFFu, mylevel, k);
             const float dn = __shfl_sync(0xFFFFFFFFu, mylevel, k < 15 ? k + 1 : 15);
             if (v > 0.0f) {
                 idx = k;
