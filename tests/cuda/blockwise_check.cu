@@ -1,8 +1,8 @@
 // GPU check of the blockwise requantiser's helpers (test code): the bucket
 // search against the plain 8-step binary search for every binary32 c in
 // [-1, 1], the FMA division by the block scale against __fdiv_rn on random
-// (x, scale) pairs, the Newton-refined reciprocal against __frcp_rn for every
-// scale of the fast range, and whole codes (reciprocal, FMA quotient, bucket
+// (x, scale) pairs, the Newton-refined reciprocal (scalar and packed pair
+// form) against __frcp_rn for every scale of the fast range, and whole codes (reciprocal, FMA quotient, bucket
 // search, IEEE fix-up below the floor) against the count of midpoints below
 // the IEEE quotient.  Kernels only add to counters and write the first
 // mismatch into a fixed 4-word slot claimed with atomicCAS.
@@ -94,7 +94,11 @@ __global__ void reciprocal_all(unsigned long long *count, uint32_t *first)
     for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
         const float b = __uint_as_float(lo + i);
         const uint32_t got = __float_as_uint(reciprocal_rn(b)), want = __float_as_uint(__frcp_rn(b));
-        if (got != want)
+        // the pair form, b in the first lane, the range's mirror image in the second
+        const float bo = __uint_as_float(lo + n - 1u - i);
+        const float2 g2 = reciprocal_rn2(make_float2(b, bo), make_float2(-b, -bo));
+        if (got != want || __float_as_uint(g2.x) != want ||
+            __float_as_uint(g2.y) != __float_as_uint(__frcp_rn(bo)))
             note(count, first, lo + i, 0, got, want);
     }
 }
