@@ -386,3 +386,59 @@ def test_late_steps_unit_bias_correction(pa, mode):
 def test_no_pipeline_fault_after_the_steps(pa):
     """The staged kernels' bounded waits never ran out during this module."""
     assert pa.pa_device_fault(clear=True) == 0
+
+
+@pytest.mark.parametrize("first_step", [1, 100_000])
+@pytest.mark.parametrize("mode", ["e4", "fp16", "fp32"])
+def test_large_launch_sampled(pa, mode, first_step):
+    """A launch of at least 32 tiles per CTA (4,864 tiles of 6,144 elements on
+    a 152-SM GB300) takes the kernel instantiation whose whole tiles keep the
+    branch-free arithmetic one lane at a time; smaller launches pair it.  One
+    tensor of 30,000,013 elements with random prior state, two steps at early
+    and at late global steps (1 - beta2^step rounding to 1.0f takes the
+    instantiation that skips v'/bc2), 0.1 % zero gradients (warps whose share
+    holds one take the per-vector path); 16 slices of 4,096 elements (the
+    ragged end included) advanced by the oracle must match bit for bit
+    (elements are independent)."""
+    import torch
+
+    n = 30_000_013
+    rng = np.random.default_rng(first_step + len(mode))
+    starts = sorted(set(rng.integers(0, n - 4096, 15).tolist()) | {n - 4096})
+    p = torch.from_numpy(rng.normal(0, 0.02, n).astype(np.float32)).cuda()
+    if mode == "fp32":
+        state = [torch.from_numpy(rng.normal(0, 1e-4, n).astype(np.float32)).cuda(),
+                 torch.from_numpy((rng.normal(0, 1e-3, n) ** 2).astype(np.float32)).cuda()]
+    else:
+        w = rng.integers(0, 1 << 32, n, dtype=np.uint64).astype(np.uint32)
+        if mode == "fp16":
+            w &= np.uint32(0x7BFF7BFF)
+        state = [torch.from_numpy(w.view(np.int32)).cuda()]
+    host = [[p[a:a + 4096].cpu().numpy()] + [s[a:a + 4096].cpu().numpy() for s in state]
+            for a in starts]
+    if mode != "fp32":
+        for h in host:
+            h[1] = h[1].view(np.uint32)
+    bad = torch.zeros(1, dtype=torch.int64, device="cuda")
+    for t in (first_step, first_step + 1):
+        gn = rng.normal(0, 1e-3, n).astype(np.float32)
+        gn[rng.random(n) < 1e-3] = 0.0  # about a quarter of the warps' shares take the per-vector path
+        g = torch.from_numpy(gn).cuda()
+        if mode == "fp32":
+            pa.pa_adamw_step_fp32(p, g, state[0], state[1], t, nonfinite=bad, **HY)
+        else:
+            fn = pa.pa_adamw_step_packed_e4 if mode == "e4" else pa.pa_adamw_step_packed_fp16
+            fn(p, g, state[0], t, nonfinite=bad, **HY)
+        gh = [g[a:a + 4096].cpu().numpy() for a in starts]
+        for h, gs in zip(host, gh):
+            if mode == "fp32":
+                h[0], h[1], h[2], _ = oracle.step_fp32(h[0], gs, h[1], h[2], t, **HY)
+            else:
+                h[0], h[1], _ = oracle.step_packed(h[0], gs, h[1], t, mode=mode, **HY)
+    torch.cuda.synchronize()
+    for a, h in zip(starts, host):
+        assert_same_bits(p[a:a + 4096].cpu().numpy(), h[0], f"{mode} p at {a}")
+        for s, e in zip(state, h[1:]):
+            got = s[a:a + 4096].cpu().numpy()
+            got = got.view(np.uint32) if mode != "fp32" else got
+            assert_same_bits(got, e, f"{mode} state at {a}")
